@@ -1,0 +1,146 @@
+"""Pins of the oracle's schedule against what the paper fixes.
+
+"Wave Forcing" Sec. 2 Eq. 2 (width <= S+1, N = S+1 forwards per chunk),
+Sec. 3.1 Eq. 3-5, Sec. 4.2 Eq. 10, App. B.3 (N_chunk + S rounds, store
+context), App. B.4 Eq. 16 (eta = 133/137 = 97.1% at S=4).
+"""
+
+import itertools
+
+import pytest
+
+from oracle import schedule as sch
+from golden_io import read_schedule
+
+
+def _as_tuples(tasks):
+    return [(t.chunk, t.stage, t.dest_page,
+             [(e.kind, e.chunk, e.j, e.page, e.tpos) for e in t.context]) for t in tasks]
+
+
+@pytest.mark.parametrize("name,cfg", [
+    ("schedule_s2_n6_full.txt", sch.Cfg(S=2, n_chunks=6, history=-1)),
+    ("schedule_s4_n10_w3.txt", sch.Cfg(S=4, n_chunks=10, history=3)),
+])
+def test_hand_worked_rounds(name, cfg):
+    gold = read_schedule(name)
+    for k, tasks in gold.items():
+        assert _as_tuples(sch.round_tasks(cfg, k)) == tasks, f"round {k}"
+    if name.startswith("schedule_s2"):
+        assert sorted(gold) == list(range(sch.n_rounds(cfg)))
+
+
+CFGS = [sch.Cfg(S, N, W, anchor, mode)
+        for S, N, W, anchor, mode in itertools.product(
+            [1, 2, 3, 4, 5], [1, 2, 3, 6, 11], [-1, 0, 1, 3], [True, False],
+            [sch.ANCHOR_ADJACENT, sch.ANCHOR_ABSOLUTE])]
+
+
+@pytest.mark.parametrize("cfg", CFGS, ids=str)
+def test_schedule_invariants(cfg):
+    S, N = cfg.S, cfg.n_chunks
+    seen = {}
+    stores = []
+    for k in range(-2, sch.n_rounds(cfg) + 3):
+        tasks = sch.round_tasks(cfg, k)
+        if k < 0 or k >= sch.n_rounds(cfg):
+            assert tasks == []          # Algorithm 1 runs k = 0 .. N+S-1 only
+            continue
+        assert 1 <= len(tasks) <= S + 1          # Eq. 2 width
+        for t in tasks:
+            # Eq. 3: cell (i, s) runs in round k = i + s; store at (k-S, S)
+            assert t.chunk + t.stage == k
+            assert 0 <= t.chunk < N
+            seen.setdefault(t.chunk, []).append(t.stage)
+            # self first among live entries; the task reads its own K/V
+            own = [e for e in t.context if e.chunk == t.chunk and e.j == t.stage]
+            assert len(own) == 1 and own[0].page == t.dest_page
+            # a chunk never sees a later chunk (Sec. 3.1 after Eq. 4)
+            assert all(e.chunk <= t.chunk for e in t.context)
+            # Eq. 5 ordering: anchor, history (oldest first), store, live j ascending
+            kinds = [e.kind for e in t.context]
+            assert kinds == sorted(kinds)
+            hist = [e.chunk for e in t.context if e.kind == sch.KIND_HISTORY]
+            assert hist == sorted(hist)
+            live = [e.j for e in t.context if e.kind == sch.KIND_LIVE]
+            assert live == sorted(live) and all(j >= t.stage for j in live)
+            if t.stage == S:
+                # store attends to anchor, retained history and itself (App. B.3)
+                assert all(e.kind != sch.KIND_LIVE for e in t.context)
+            if cfg.history >= 0:
+                assert len(hist) <= cfg.history
+            # pages of one context are distinct (fixed slots, App. B.2 Eq. 13)
+            pages = [e.page for e in t.context]
+            assert len(set(pages)) == len(pages)
+            assert all(0 <= p < sch.n_pages(cfg) - 1 for p in pages)
+        store = [t for t in tasks if t.stage == S]
+        stores.append(store[0].chunk if store else None)
+    # every chunk gets exactly S denoising updates plus one store: N = S+1 forwards
+    assert sorted(seen) == list(range(N))
+    assert all(sorted(v) == list(range(S + 1)) for v in seen.values())
+    # after fill, exactly one completed chunk per round, in order
+    assert stores[:S] == [None] * S
+    assert stores[S:] == list(range(N))
+    # all S+1 slots busy only for S <= k < N (App. B.4); never if N <= S
+    full = [k for k in range(sch.n_rounds(cfg)) if len(sch.round_tasks(cfg, k)) == S + 1]
+    assert full == list(range(S, N))
+
+
+def test_slot_occupancy_printed_example():
+    # App. B.4: "133/137 = 97.1%" for 399 latent frames (133 chunks) at S=4
+    cfg = sch.Cfg(S=4, n_chunks=133, history=3)
+    eta = sch.slot_occupancy(cfg)
+    assert (cfg.n_chunks, cfg.n_chunks + cfg.S) == (133, 137)
+    assert round(100 * eta, 1) == 97.1
+    busy = sum(len(sch.round_tasks(cfg, k)) for k in range(sch.n_rounds(cfg)))
+    assert busy == 133 * 5                 # N_chunk (S+1) forwards in all
+    assert busy / (sch.n_rounds(cfg) * (cfg.S + 1)) == pytest.approx(eta)
+
+
+@pytest.mark.parametrize("S,W", [(4, 3), (5, 3), (2, 1), (3, 0)])
+def test_key_counts_eq10(S, W):
+    # Sec. 4.2 Eq. 10: N_s = N_prefix + (S - s) N_C in a filled round, with
+    # N_prefix covering anchor + history + store.
+    cfg = sch.Cfg(S=S, n_chunks=40, history=W)
+    nc = 7
+    k = S + W + 5
+    tasks = sch.round_tasks(cfg, k)
+    prefix = (1 + W + 1) * nc
+    for t in tasks:
+        if t.stage < S:
+            assert sch.key_count(t, nc) == prefix + (S - t.stage) * nc
+        else:
+            assert sch.key_count(t, nc) == prefix
+
+
+def test_anchor_positions():
+    cfg = sch.Cfg(S=4, n_chunks=20, history=3)
+    # anchor sits one chunk before the oldest non-anchor chunk of the round
+    for k in range(sch.n_rounds(cfg)):
+        if not sch.anchor_present(cfg, k):
+            continue
+        hist = sch.history_chunks(cfg, k)
+        assert sch.anchor_tpos(cfg, k) == max(0, (hist[0] if hist else 1) - 1)
+    absolute = sch.Cfg(S=4, n_chunks=20, history=3, anchor_mode=sch.ANCHOR_ABSOLUTE)
+    assert all(sch.anchor_tpos(absolute, k) == 0 for k in range(sch.n_rounds(absolute)))
+    full = sch.Cfg(S=4, n_chunks=20, history=-1)
+    assert all(sch.anchor_tpos(full, k) == 0 for k in range(sch.n_rounds(full)))
+
+
+def test_planted_mistake_is_caught(monkeypatch):
+    """A store that also read live chunks (a plausible slip) breaks the golden rounds."""
+    real = sch.round_tasks
+
+    def wrong(cfg, k):
+        out = []
+        for t in real(cfg, k):
+            if t.stage == cfg.S:
+                live = [e for t2 in real(cfg, k) for e in t2.context if e.kind == sch.KIND_LIVE]
+                t = sch.Task(t.chunk, t.stage, t.dest_page, t.context + tuple(live[:1]))
+            out.append(t)
+        return out
+
+    monkeypatch.setattr(sch, "round_tasks", wrong)
+    gold = read_schedule("schedule_s2_n6_full.txt")
+    cfg = sch.Cfg(S=2, n_chunks=6, history=-1)
+    assert any(_as_tuples(sch.round_tasks(cfg, k)) != v for k, v in gold.items())
