@@ -133,7 +133,7 @@ def history_chunks(cfg: Cfg, k: int) -> list[int]:
     """Bounded clean history H_k: the W newest clean non-anchor chunks, oldest first."""
     clean = [c for c in clean_before(cfg, k) if not (cfg.use_anchor and c == 0)]
     if cfg.history >= 0:
-        clean = clean[len(clean) - cfg.history:] if cfg.history > 0 else []
+        clean = clean[max(0, len(clean) - cfg.history):] if cfg.history > 0 else []
     return clean
 
 

@@ -67,8 +67,11 @@ def test_schedule_invariants(cfg):
             if t.stage == S:
                 # store attends to anchor, retained history and itself (App. B.3)
                 assert all(e.kind != sch.KIND_LIVE for e in t.context)
-            if cfg.history >= 0:
-                assert len(hist) <= cfg.history
+            # bounded window keeps the W newest clean non-anchor chunks, or all
+            # of them while fewer than W exist (App. B.3, Sec. 3.1 Eq. 5)
+            clean = [c for c in range(N) if c + S < k and not (cfg.use_anchor and c == 0)]
+            want = clean if cfg.history < 0 else clean[len(clean) - min(len(clean), cfg.history):]
+            assert hist == want
             # pages of one context are distinct (fixed slots, App. B.2 Eq. 13)
             pages = [e.page for e in t.context]
             assert len(set(pages)) == len(pages)
