@@ -1,0 +1,478 @@
+// Round attention on the 5th-generation tensor cores (bf16, head_dim 128).
+//
+// What it computes ("Wave Forcing", Sec. 3.1 Eq. 4-5): for every active task
+// of the round (chunk k - s at stage s, plus the store at stage S) and every
+// head, O = softmax(Q K^T / sqrt(D)) V over the task's ordered context --
+// anchor, bounded history, live store, live stages j >= s -- with full
+// (bidirectional) attention inside each chunk.  The mask is applied at chunk
+// granularity by construction: a task's key stream is exactly the pages of
+// its context, so masked-out chunk blocks are never loaded or multiplied.
+// Only the ragged last key tile of each chunk (N_C mod 128 valid keys) needs
+// an element mask.
+//
+// Design (one persistent CTA per SM, 384 threads):
+//  * work unit = (task, head, pair of 128-row query tiles); units are handed
+//    out longest-context-first through an atomic counter in scratch;
+//  * warp 8 (one thread): TMA producer -- both Q tiles, then K_0, K_1, V_0,
+//    K_2, V_1, ... through a 4-stage ring of 32 KB tiles (128B swizzle); the
+//    pages are read through a 3D tensor map [plane][N_C][128], so rows past
+//    N_C are zero-filled by the TMA unit;
+//  * warp 9 (one thread): tcgen05.mma issuer.  S = Q K^T (SS, fp32 in TMEM)
+//    and O += P V (P read from TMEM, V MN-major from shared memory), the two
+//    query tiles interleaved so one tile's softmax overlaps the other tile's
+//    MMAs;
+//  * warps 0-3 / 4-7: softmax of tile 0 / tile 1.  Thread r owns query row r:
+//    tcgen05.ld of its 128 scores, row max in registers, exp2, P packed to
+//    bf16 and written back over S in TMEM.  The running max is only raised
+//    when it grows by more than 2^8, and O is rescaled in TMEM only then.
+//  * TMEM (512 columns): S0 | S1 | O0 | O1, P aliasing the first 64 columns of S.
+//
+// Every wait is bounded (%globaltimer); on a timeout the kernel records it in
+// the scratch status word, drains its own copies and MMAs, frees TMEM and
+// returns.
+
+#include <cuda_bf16.h>
+
+#include "wf_internal.h"
+#include "wf_ptx.cuh"
+
+using namespace wfptx;
+
+namespace {
+
+constexpr int BM = 128;             // query rows per tile
+constexpr int BN = 128;             // keys per tile
+constexpr int HD = 128;             // head dim
+constexpr int NST = 4;              // K/V ring stages
+constexpr uint32_t TILE_BYTES = BM * HD * 2;
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
+constexpr int NUM_THREADS = 384;
+
+constexpr uint32_t SM_Q0 = 0;
+constexpr uint32_t SM_Q1 = TILE_BYTES;
+constexpr uint32_t SM_KV = 2 * TILE_BYTES;
+constexpr uint32_t SM_BAR = SM_KV + NST * TILE_BYTES;
+constexpr int B_QFULL = 0;
+constexpr int B_KVFULL = 1;
+constexpr int B_KVEMPTY = B_KVFULL + NST;
+constexpr int B_SFULL = B_KVEMPTY + NST;
+constexpr int B_PFULL = B_SFULL + 2;
+constexpr int B_ODONE = B_PFULL + 2;
+constexpr int B_DRAIN = B_ODONE + 2;
+constexpr int NBARS = B_DRAIN + 1;
+constexpr uint32_t SM_MISC = SM_BAR + ((NBARS * 8 + 63) / 64) * 64;
+constexpr uint32_t SM_TOTAL = SM_MISC + 64;
+constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;  // alignment slack
+
+constexpr uint64_t WAIT_NS = 1000000000ull;  // 1 s
+
+struct TcParams {
+    int layer;
+    int n_units;
+    int qpairs;           // pairs of query tiles per (task, head)
+    int tpc;              // key tiles per chunk
+    float sl2;            // log2(e) / sqrt(D)
+    __nv_bfloat16 *out;
+    uint32_t *ctl;        // scratch control words
+};
+
+__device__ __forceinline__ int kseq(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int vseq(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
+
+struct Ctx {
+    uint32_t sbase;
+    volatile int *abort;
+    uint32_t *status, *where;
+    __device__ uint32_t bar(int i) const { return sbase + SM_BAR + 8u * i; }
+    __device__ bool wait(int b, uint32_t parity, uint32_t site) const {
+        return mbar_wait(bar(b), parity, abort, status, where, site, WAIT_NS);
+    }
+};
+
+__device__ __forceinline__ void decode_unit(int u, const WfRoundDev &rd, const TcParams &p, int H,
+                                            int &ti, int &h, int &qp) {
+    int per_task = H * p.qpairs;
+    int oi = u / per_task;
+    int rem = u - oi * per_task;
+    ti = rd.lpt[oi];
+    h = rem / p.qpairs;
+    qp = rem - h * p.qpairs;
+}
+
+// ---- producer ----------------------------------------------------------------
+__device__ void producer(const Ctx &c, const CUtensorMap *tq, const CUtensorMap *tkv,
+                         const WfGeom &g, const WfRoundDev &rd, const TcParams &p, int ti, int h,
+                         int qp, int n, uint32_t seq, uint32_t *issued) {
+    const int plane_q = rd.slot[ti] * g.H + h;
+    mbar_arrive_expect_tx(c.bar(B_QFULL), 2 * TILE_BYTES);
+    tma_load_3d(c.sbase + SM_Q0, tq, c.bar(B_QFULL), 0, (2 * qp) * BM, plane_q);
+    tma_load_3d(c.sbase + SM_Q0 + HALF_BYTES, tq, c.bar(B_QFULL), 64, (2 * qp) * BM, plane_q);
+    tma_load_3d(c.sbase + SM_Q1, tq, c.bar(B_QFULL), 0, (2 * qp + 1) * BM, plane_q);
+    tma_load_3d(c.sbase + SM_Q1 + HALF_BYTES, tq, c.bar(B_QFULL), 64, (2 * qp + 1) * BM, plane_q);
+    for (int i = 0; i < 2 * n; ++i) {
+        int j;
+        int isv;
+        if (i == 0) {
+            j = 0; isv = 0;
+        } else if (i == 2 * n - 1) {
+            j = n - 1; isv = 1;
+        } else if (i & 1) {
+            j = (i + 1) / 2; isv = 0;
+        } else {
+            j = i / 2 - 1; isv = 1;
+        }
+        uint32_t s = seq + i;
+        int st = s % NST;
+        if (!c.wait(B_KVEMPTY + st, ((s / NST) & 1) ^ 1, 1)) return;
+        int ci = j / p.tpc;
+        int t = j - ci * p.tpc;
+        int plane = ((rd.page[ti][ci] * g.L + p.layer) * 2 + isv) * g.H + h;
+        uint32_t dst = c.sbase + SM_KV + st * TILE_BYTES;
+        mbar_arrive_expect_tx(c.bar(B_KVFULL + st), TILE_BYTES);
+        tma_load_3d(dst, tkv, c.bar(B_KVFULL + st), 0, t * BN, plane);
+        tma_load_3d(dst + HALF_BYTES, tkv, c.bar(B_KVFULL + st), 64, t * BN, plane);
+        *issued = s + 1;
+    }
+}
+
+// ---- MMA issuer ----------------------------------------------------------------
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+        mma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+               idesc, kk > 0 ? 1u : 0u);
+    }
+}
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                         bool acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, HD, true);
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+        mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, HALF_BYTES, 1024), idesc,
+               (acc || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ void mma_issuer(const Ctx &c, uint32_t tmem, int n, uint32_t seq, uint32_t it_base,
+                           uint32_t unit_iter) {
+    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+    const uint32_t q0 = c.sbase + SM_Q0, q1 = c.sbase + SM_Q1;
+    if (!c.wait(B_QFULL, unit_iter & 1, 2)) return;
+    tc_fence_after();
+    for (int j = 0; j < n; ++j) {
+        uint32_t ks = seq + kseq(j);
+        int kst = ks % NST;
+        if (!c.wait(B_KVFULL + kst, (ks / NST) & 1, 3)) return;
+        tc_fence_after();
+        uint32_t ka = c.sbase + SM_KV + kst * TILE_BYTES;
+        if (j == 0) {
+            issue_qk(tS0, q0, ka);
+            mma_commit(c.bar(B_SFULL + 0));
+            issue_qk(tS1, q1, ka);
+            mma_commit(c.bar(B_SFULL + 1));
+            mma_commit(c.bar(B_KVEMPTY + kst));
+            continue;
+        }
+        uint32_t vs = seq + vseq(j - 1, n);
+        int vst = vs % NST;
+        if (!c.wait(B_KVFULL + vst, (vs / NST) & 1, 4)) return;
+        uint32_t va = c.sbase + SM_KV + vst * TILE_BYTES;
+        uint32_t par = (it_base + j - 1) & 1;
+        if (!c.wait(B_PFULL + 0, par, 5)) return;
+        tc_fence_after();
+        issue_pv(tO0, tS0, va, j - 1 > 0);
+        issue_qk(tS0, q0, ka);
+        mma_commit(c.bar(B_SFULL + 0));
+        if (!c.wait(B_PFULL + 1, par, 6)) return;
+        tc_fence_after();
+        issue_pv(tO1, tS1, va, j - 1 > 0);
+        mma_commit(c.bar(B_KVEMPTY + vst));
+        issue_qk(tS1, q1, ka);
+        mma_commit(c.bar(B_SFULL + 1));
+        mma_commit(c.bar(B_KVEMPTY + kst));
+    }
+    uint32_t vs = seq + vseq(n - 1, n);
+    int vst = vs % NST;
+    if (!c.wait(B_KVFULL + vst, (vs / NST) & 1, 7)) return;
+    uint32_t va = c.sbase + SM_KV + vst * TILE_BYTES;
+    uint32_t par = (it_base + n - 1) & 1;
+    if (!c.wait(B_PFULL + 0, par, 8)) return;
+    tc_fence_after();
+    issue_pv(tO0, tS0, va, n - 1 > 0);
+    mma_commit(c.bar(B_ODONE + 0));
+    if (!c.wait(B_PFULL + 1, par, 9)) return;
+    tc_fence_after();
+    issue_pv(tO1, tS1, va, n - 1 > 0);
+    mma_commit(c.bar(B_ODONE + 1));
+    mma_commit(c.bar(B_KVEMPTY + vst));
+}
+
+// ---- softmax / epilogue -------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const WfRoundDev &rd,
+                             const TcParams &p, int X, int ti, int h, int qp, int n,
+                             uint32_t it_base, uint32_t unit_iter) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + X * 128;
+    const uint32_t tO = tmem + lane_off + 256 + X * 128;
+    const float sl2 = p.sl2;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    for (int j = 0; j < n; ++j) {
+        bool ok = c.wait(B_SFULL + X, (it_base + j) & 1, 10 + X);
+        if (!__all_sync(0xffffffffu, ok)) return;
+        tc_fence_after();
+        uint32_t r[4][32];
+        tmem_ld32(tS + 0, r[0]);
+        tmem_ld32(tS + 32, r[1]);
+        tmem_ld32(tS + 64, r[2]);
+        tmem_ld32(tS + 96, r[3]);
+        tmem_wait_ld(r[0]);
+        tmem_wait_ld(r[1]);
+        tmem_wait_ld(r[2]);
+        tmem_wait_ld(r[3]);
+        const int t = j % p.tpc;
+        const int valid = g.NC - t * BN;
+        if (valid < BN) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (q * 32 + i >= valid) r[q][i] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r[q][i]));
+        const float mnew = mx * sl2;
+        float alpha = 1.f;
+        if (mnew > m_run + 8.f) {
+            alpha = ex2(m_run - mnew);
+            m_run = mnew;
+        }
+        float sum = 0.f;
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float p0 = ex2(fmaf(__uint_as_float(r[q][2 * i]), sl2, -m_run));
+                float p1 = ex2(fmaf(__uint_as_float(r[q][2 * i + 1]), sl2, -m_run));
+                sum += p0 + p1;
+                pk[q >> 1][(q & 1) * 16 + i] = pack_bf16(p0, p1);
+            }
+        l_run = l_run * alpha + sum;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tO + q * 32, o);
+                tmem_wait_ld(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(tO + q * 32, o);
+            }
+        }
+        tmem_st32(tS + 0, pk[0]);
+        tmem_st32(tS + 32, pk[1]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(c.bar(B_PFULL + X));
+    }
+
+    bool ok = c.wait(B_ODONE + X, unit_iter & 1, 12 + X);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    tc_fence_after();
+    const int qrow = (2 * qp + X) * BM + row;
+    const float inv = 1.f / l_run;
+    __nv_bfloat16 *dst = p.out + (((size_t)rd.slot[ti] * g.NC + qrow) * g.H + h) * HD;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t o[32];
+        tmem_ld32(tO + q * 32, o);
+        tmem_wait_ld(o);
+        if (qrow < g.NC) {
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                d4[v] = w;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
+                   const WfGeom g, const WfRoundDev rd, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    Ctx c;
+    c.sbase = raw_u32 + pad;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM_MISC);
+    int *unit_slot = reinterpret_cast<int *>(smem + SM_MISC + 8);
+    c.abort = reinterpret_cast<volatile int *>(smem + SM_MISC + 16);
+    c.status = p.ctl + WF_SCRATCH_STATUS / 4;
+    c.where = p.ctl + WF_SCRATCH_WHERE / 4;
+    uint32_t *work = p.ctl + WF_SCRATCH_WORK / 4;
+    uint32_t *done = p.ctl + WF_SCRATCH_DONE / 4;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(c.bar(B_QFULL), 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(c.bar(B_KVFULL + i), 1);
+            mbar_init(c.bar(B_KVEMPTY + i), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(c.bar(B_SFULL + x), 1);
+            mbar_init(c.bar(B_PFULL + x), 128);
+            mbar_init(c.bar(B_ODONE + x), 1);
+        }
+        mbar_init(c.bar(B_DRAIN), 1);
+        mbar_fence_init();
+        *c.abort = 0;
+        unit_slot[0] = blockIdx.x;
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tkv);
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    uint32_t seq = 0, it_base = 0, unit_iter = 0, issued = 0;
+    int u = unit_slot[0];
+    while (u < p.n_units) {
+        int ti, h, qp;
+        decode_unit(u, rd, p, g.H, ti, h, qp);
+        const int n = rd.n_ctx[ti] * p.tpc;
+        if (warp < 8) {
+            softmax_tile(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
+        } else if (warp == 8) {
+            if (lane == 0) producer(c, &tq, &tkv, g, rd, p, ti, h, qp, n, seq, &issued);
+        } else if (warp == 9) {
+            if (lane == 0) mma_issuer(c, tmem, n, seq, it_base, unit_iter);
+        }
+        seq += 2 * n;
+        it_base += n;
+        unit_iter += 1;
+        if (threadIdx.x == 0) unit_slot[unit_iter & 1] = (int)(gridDim.x + atomicAdd(work, 1u));
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (*c.abort) break;
+        u = unit_slot[unit_iter & 1];
+    }
+
+    if (*c.abort) {
+        // give the copies and MMAs this CTA started time to land before TMEM
+        // and shared memory are released
+        if (warp == 8 && lane == 0) {
+            uint32_t first = issued > (uint32_t)NST ? issued - NST : 0;
+            for (uint32_t s = first; s < issued; ++s)
+                mbar_wait(c.bar(B_KVFULL + s % NST), (s / NST) & 1, nullptr, nullptr, nullptr, 0,
+                          WAIT_NS);
+            mbar_wait(c.bar(B_QFULL), unit_iter & 1, nullptr, nullptr, nullptr, 0, WAIT_NS);
+        }
+        if (warp == 9 && lane == 0) {
+            mma_commit(c.bar(B_DRAIN));
+            mbar_wait(c.bar(B_DRAIN), 0, nullptr, nullptr, nullptr, 0, WAIT_NS);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        uint32_t prev = atomicAdd(done, 1u);
+        if (prev == gridDim.x - 1) {
+            atomicExch(work, 0u);
+            atomicExch(done, 0u);
+        }
+    }
+}
+
+}  // namespace
+
+bool wf_attn_tc_supported(const WfGeom &g, int dtype) {
+    return dtype == WF_BF16 && g.D == HD;
+}
+
+cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out) {
+    typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return cudaErrorUnknown;
+        encode = reinterpret_cast<EncodeFn>(fn);
+    }
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)g.NC * HD * 2};
+    cuuint64_t dq[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)(g.S + 1) * g.H};
+    if (encode(&out->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qbuf, dq, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cuuint64_t dk[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)g.P * g.L * 2 * g.H};
+    if (encode(&out->kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, dk, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
+                              const WfTmaps &maps, void *out, void *scratch, int num_sms,
+                              cudaStream_t stream) {
+    if (rd.n_tasks < 1) return cudaSuccess;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    TcParams p;
+    p.layer = layer;
+    p.tpc = (g.NC + BN - 1) / BN;
+    p.qpairs = ((g.NC + BM - 1) / BM + 1) / 2;
+    p.n_units = rd.n_tasks * g.H * p.qpairs;
+    p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ctl = static_cast<uint32_t *>(scratch);
+    int grid = p.n_units < num_sms ? p.n_units : num_sms;
+    attn_tc_kernel<<<grid, NUM_THREADS, SM_ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
+    return cudaGetLastError();
+}

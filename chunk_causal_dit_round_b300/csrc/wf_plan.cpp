@@ -1,0 +1,433 @@
+// Host side of the wavefront-round library: plan, round schedule, page ring,
+// argument validation and the C ABI entry points of include/wf.h.
+//
+// Schedule: "Wave Forcing: Towards Speed-of-Light Streaming Video
+// Generation", Sec. 3.1 Eq. 3 (cell (i, s) runs in round k = i + s, store at
+// (k - S, S), active set A_k), Eq. 5 (ordered context), App. B.3 Algorithm 1
+// (N_chunk + S rounds; the store page is promoted into history after the
+// round; the first clean chunk is a persistent anchor whose unrotated key is
+// kept) and App. B.8 (fixed page capacity).  The ring is a real FIFO
+// allocator: a freed page is reused by the next stored chunk.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <vector>
+
+#include "wf_internal.h"
+
+namespace {
+
+struct CtxEntry {
+    int kind, chunk, j, page, tpos;
+};
+
+struct HostTask {
+    int chunk, stage, dest;
+    int n_ctx;
+    CtxEntry ctx[WF_MAX_CTX];
+};
+
+}  // namespace
+
+struct wf_plan_s {
+    int S, NC, H, D, W;
+    wf_plan_opts o;
+    int R, P;                // ring pages, total pages
+    WfGeom g;
+
+    // round state
+    int k = -1;
+    bool have_prev_store = false;
+    int prev_store_chunk = -1, prev_store_page = -1;
+    bool anchor_stored = false;               // chunk 0 clean and on page 0
+    std::deque<std::pair<int, int>> history;  // (chunk, page), oldest first
+    std::deque<int> free_pages;
+    int n_tasks = 0;
+    HostTask tasks[WF_MAX_TASKS];
+    int anchor_tpos = -1;
+    WfRoundDev rd{};
+    std::vector<int> anchor_rot;              // per layer: tpos the anchor page holds, -1 none
+    std::vector<int> published;               // per layer: round whose publish ran
+
+    // binding
+    bool bound = false;
+    void *pool = nullptr, *qbuf = nullptr, *scratch = nullptr;
+    int device = 0, num_sms = 0;
+    bool tmaps_ok = false;
+    WfTmaps tmaps;
+};
+
+namespace {
+
+size_t elem_size(int dtype) { return dtype == WF_FP32 ? 4 : 2; }
+
+bool mul_ok(size_t a, size_t b, size_t *out) {
+    if (a != 0 && b > SIZE_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+size_t tables_bytes(const WfGeom &g) {
+    return (size_t)(g.t_max * g.dt2 + g.gh * g.dh2 + g.gw * g.dw2) * 8;
+}
+
+// Anchor position of the round (mode ADJACENT): one chunk before the oldest
+// non-anchor chunk present in the round, clamped at 0.
+int adjacent_anchor_pos(const wf_plan_s *p, int store_chunk) {
+    int oldest = -1;
+    auto take = [&](int c) { if (oldest < 0 || c < oldest) oldest = c; };
+    for (auto &h : p->history) take(h.first);
+    if (store_chunk >= 0 && !(p->o.use_anchor && store_chunk == 0)) take(store_chunk);
+    for (int s = 0; s < p->S; ++s) {
+        int c = p->k - s;
+        if (c >= 0 && c < p->o.n_chunks) take(c);
+    }
+    return oldest <= 0 ? 0 : oldest - 1;
+}
+
+void build_round(wf_plan_s *p, int store_chunk, int store_page) {
+    const int S = p->S, k = p->k, N = p->o.n_chunks;
+    CtxEntry prefix[WF_MAX_CTX];
+    int np = 0;
+    bool anchor_in = p->o.use_anchor && p->anchor_stored;
+    p->anchor_tpos = -1;
+    if (anchor_in) {
+        p->anchor_tpos = p->o.anchor_mode == WF_ANCHOR_ABSOLUTE ? 0 : adjacent_anchor_pos(p, store_chunk);
+        prefix[np++] = {WF_KIND_ANCHOR, 0, S + 1, 0, p->anchor_tpos};
+    }
+    for (auto &h : p->history) prefix[np++] = {WF_KIND_HISTORY, h.first, S + 1, h.second, h.first};
+    if (store_chunk >= 0) prefix[np++] = {WF_KIND_STORE, store_chunk, S, store_page, store_chunk};
+
+    int act[WF_MAX_STAGES];
+    int na = 0;
+    for (int s = 0; s < S; ++s)
+        if (k - s >= 0 && k - s < N) act[na++] = s;
+
+    p->n_tasks = 0;
+    for (int a = 0; a < na; ++a) {
+        int s = act[a];
+        HostTask &t = p->tasks[p->n_tasks++];
+        t.chunk = k - s;
+        t.stage = s;
+        t.dest = 1 + p->R + s;
+        t.n_ctx = 0;
+        for (int e = 0; e < np; ++e) t.ctx[t.n_ctx++] = prefix[e];
+        for (int b = a; b < na; ++b) {
+            int j = act[b];
+            t.ctx[t.n_ctx++] = {WF_KIND_LIVE, k - j, j, 1 + p->R + j, k - j};
+        }
+    }
+    if (store_chunk >= 0) {
+        HostTask &t = p->tasks[p->n_tasks++];
+        t.chunk = store_chunk;
+        t.stage = S;
+        t.dest = store_page;
+        t.n_ctx = 0;
+        for (int e = 0; e < np; ++e) t.ctx[t.n_ctx++] = prefix[e];
+    }
+
+    // device view
+    WfRoundDev &rd = p->rd;
+    std::memset(&rd, 0, sizeof(rd));
+    rd.n_tasks = p->n_tasks;
+    rd.raw_copy_task = -1;
+    for (int i = 0; i < p->n_tasks; ++i) {
+        const HostTask &t = p->tasks[i];
+        rd.slot[i] = t.stage;
+        rd.chunk[i] = t.chunk;
+        rd.dest[i] = t.dest;
+        rd.n_ctx[i] = t.n_ctx;
+        for (int e = 0; e < t.n_ctx; ++e) rd.page[i][e] = (uint8_t)t.ctx[e].page;
+        if (t.stage == S && p->o.use_anchor && t.chunk == 0) rd.raw_copy_task = i;
+        rd.lpt[i] = i;
+    }
+    std::stable_sort(rd.lpt, rd.lpt + p->n_tasks,
+                     [&](int a, int b) { return rd.n_ctx[a] > rd.n_ctx[b]; });
+    rd.anchor_tpos = p->anchor_tpos;
+    rd.rerotate = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *wf_strerror(int code) {
+    switch (code) {
+        case WF_OK: return "ok";
+        case WF_EINVAL: return "invalid argument";
+        case WF_ERANGE: return "size or index out of range";
+        case WF_ENOMEM: return "buffer too small";
+        case WF_ECUDA: return "CUDA call failed";
+        case WF_ETIMEOUT: return "device-side bounded wait timed out";
+        case WF_EDONE: return "request finished: no more rounds";
+        case WF_EUNBOUND: return "plan has no bound device buffers";
+        case WF_ENOROUND: return "no current round (call wf_round_step)";
+        case WF_EUNSUPPORTED: return "kernel does not support this dtype/shape";
+        case WF_EORDER: return "layer not published in the current round";
+        default: return "unknown error";
+    }
+}
+
+void wf_plan_opts_default(wf_plan_opts *o) {
+    if (!o) return;
+    std::memset(o, 0, sizeof(*o));
+    o->n_chunks = 1;
+    o->layers = 1;
+    o->grid_t = 3;
+    o->grid_h = 0;
+    o->grid_w = 0;
+    o->dtype = WF_BF16;
+    o->use_anchor = 1;
+    o->anchor_mode = WF_ANCHOR_ADJACENT;
+    o->rope_theta = 10000.0;
+}
+
+int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks,
+            const wf_plan_opts *opts, wf_plan_t *out) {
+    if (!out) return WF_EINVAL;
+    *out = nullptr;
+    wf_plan_opts o;
+    if (opts) o = *opts; else wf_plan_opts_default(&o);
+    if (S < 1 || S > WF_MAX_STAGES) return WF_ERANGE;
+    if (chunk_tokens < 1 || heads < 1 || head_dim < 8 || (head_dim % 8)) return WF_EINVAL;
+    if (head_dim > 256) return WF_ERANGE;
+    if (history_chunks < -1) return WF_EINVAL;
+    if (o.n_chunks < 1 || o.layers < 1) return WF_ERANGE;
+    if (o.dtype != WF_FP32 && o.dtype != WF_BF16) return WF_EINVAL;
+    if (o.anchor_mode != WF_ANCHOR_ADJACENT && o.anchor_mode != WF_ANCHOR_ABSOLUTE) return WF_EINVAL;
+    if (o.use_anchor != 0 && o.use_anchor != 1) return WF_EINVAL;
+    if (!(o.rope_theta > 1.0) || !std::isfinite(o.rope_theta)) return WF_EINVAL;
+    if (o.grid_t < 1) return WF_EINVAL;
+    if (o.grid_h == 0 && o.grid_w == 0) {
+        if (chunk_tokens % o.grid_t) return WF_EINVAL;
+        o.grid_h = chunk_tokens / o.grid_t;
+        o.grid_w = 1;
+    }
+    if (o.grid_h < 1 || o.grid_w < 1 ||
+        (long long)o.grid_t * o.grid_h * o.grid_w != (long long)chunk_tokens)
+        return WF_EINVAL;
+
+    int R = history_chunks >= 0 ? history_chunks + 1
+                                : std::max(1, o.n_chunks - (o.use_anchor ? 1 : 0));
+    // longest context: anchor + history + store + S live chunks
+    int hist_max = history_chunks >= 0 ? history_chunks : std::max(0, o.n_chunks - 1);
+    if (1 + hist_max + 1 + S > WF_MAX_CTX) return WF_ERANGE;
+    int P = 1 + R + S + 1;
+    if (P > 255) return WF_ERANGE;
+
+    wf_plan_s *p = new (std::nothrow) wf_plan_s();
+    if (!p) return WF_ENOMEM;
+    p->S = S; p->NC = chunk_tokens; p->H = heads; p->D = head_dim; p->W = history_chunks;
+    p->o = o; p->R = R; p->P = P;
+    WfGeom &g = p->g;
+    g.S = S; g.NC = chunk_tokens; g.H = heads; g.D = head_dim; g.L = o.layers;
+    g.gt = o.grid_t; g.gh = o.grid_h; g.gw = o.grid_w;
+    g.P = P; g.raw_anchor_page = 1 + R + S;
+    int q6 = head_dim / 6;
+    g.dt2 = (head_dim - 4 * q6) / 2; g.dh2 = q6; g.dw2 = q6;
+    g.t_max = o.grid_t * o.n_chunks;
+    g.rope_t_off = 0;
+    g.rope_h_off = g.t_max * g.dt2;
+    g.rope_w_off = g.rope_h_off + g.gh * g.dh2;
+    for (int i = 1; i <= R; ++i) p->free_pages.push_back(i);
+    p->anchor_rot.assign(o.layers, -1);
+    p->published.assign(o.layers, -1);
+    *out = p;
+    return WF_OK;
+}
+
+int wf_plan_buffer_sizes(wf_plan_t p, wf_buffer_sizes *out) {
+    if (!p || !out) return WF_EINVAL;
+    size_t es = elem_size(p->o.dtype);
+    size_t tok = (size_t)p->NC * p->H * p->D * es;  // one slot, one of Q/K/V
+    size_t slots = (size_t)p->S + 1;
+    size_t a, b;
+    std::memset(out, 0, sizeof(*out));
+    if (!mul_ok(tok, slots * 3, &out->qkv)) return WF_ERANGE;
+    out->qbuf = tok * slots;
+    out->out = tok * slots;
+    if (!mul_ok(tok, (size_t)p->P * p->o.layers, &a) || !mul_ok(a, 2, &b)) return WF_ERANGE;
+    out->pool = b;
+    out->scratch = WF_SCRATCH_TABLES + tables_bytes(p->g);
+    out->n_pages = p->P;
+    out->ring_pages = p->R;
+    return WF_OK;
+}
+
+int wf_bind(wf_plan_t p, void *pool, void *qbuf, void *scratch) {
+    if (!p || !pool || !qbuf || !scratch) return WF_EINVAL;
+    if (((uintptr_t)pool | (uintptr_t)qbuf | (uintptr_t)scratch) & 255) return WF_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ECUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return WF_ECUDA;
+    // RoPE tables (cos, sin) computed in double and rounded to float
+    const WfGeom &g = p->g;
+    std::vector<float> tab(tables_bytes(g) / 4);
+    auto fill = [&](int off, int rows, int pairs, int part) {
+        for (int r = 0; r < rows; ++r)
+            for (int m = 0; m < pairs; ++m) {
+                double inv = std::pow(p->o.rope_theta, -2.0 * m / part);
+                double a = r * inv;
+                tab[2 * (off + r * pairs + m)] = (float)std::cos(a);
+                tab[2 * (off + r * pairs + m) + 1] = (float)std::sin(a);
+            }
+    };
+    fill(g.rope_t_off, g.t_max, g.dt2, 2 * g.dt2);
+    fill(g.rope_h_off, g.gh, g.dh2, 2 * g.dh2);
+    fill(g.rope_w_off, g.gw, g.dw2, 2 * g.dw2);
+    if (cudaMemset(scratch, 0, WF_SCRATCH_TABLES) != cudaSuccess) return WF_ECUDA;
+    if (!tab.empty() &&
+        cudaMemcpy((char *)scratch + WF_SCRATCH_TABLES, tab.data(), tab.size() * 4,
+                   cudaMemcpyHostToDevice) != cudaSuccess)
+        return WF_ECUDA;
+    p->tmaps_ok = false;
+    if (wf_attn_tc_supported(g, p->o.dtype)) {
+        if (wf_encode_tmaps(g, qbuf, pool, &p->tmaps) != cudaSuccess) return WF_ECUDA;
+        p->tmaps_ok = true;
+    }
+    p->pool = pool; p->qbuf = qbuf; p->scratch = scratch;
+    p->device = dev; p->num_sms = sms;
+    p->bound = true;
+    std::fill(p->anchor_rot.begin(), p->anchor_rot.end(), -1);
+    return WF_OK;
+}
+
+int wf_round_step(wf_plan_t p, wf_round_info *info) {
+    if (!p) return WF_EINVAL;
+    const int S = p->S, N = p->o.n_chunks;
+    if (p->k + 1 >= N + S) return WF_EDONE;
+    p->k += 1;
+    // round boundary: the previous store page becomes history (App. B.3)
+    if (p->have_prev_store) {
+        if (p->o.use_anchor && p->prev_store_chunk == 0) {
+            p->anchor_stored = true;
+        } else {
+            p->history.emplace_back(p->prev_store_chunk, p->prev_store_page);
+            while (p->W >= 0 && (int)p->history.size() > p->W) {
+                p->free_pages.push_back(p->history.front().second);
+                p->history.pop_front();
+            }
+        }
+        p->have_prev_store = false;
+    }
+    int u = p->k - S;
+    int store_chunk = -1, store_page = -1;
+    if (u >= 0 && u < N) {
+        store_chunk = u;
+        if (p->o.use_anchor && u == 0) {
+            store_page = 0;
+        } else {
+            if (p->free_pages.empty()) return WF_ERANGE;  // cannot happen with R = W + 1
+            store_page = p->free_pages.front();
+            p->free_pages.pop_front();
+        }
+        p->have_prev_store = true;
+        p->prev_store_chunk = store_chunk;
+        p->prev_store_page = store_page;
+    }
+    build_round(p, store_chunk, store_page);
+    if (info) {
+        std::memset(info, 0, sizeof(*info));
+        info->k = p->k;
+        info->n_tasks = p->n_tasks;
+        info->store_chunk = store_chunk;
+        info->anchor_tpos = p->anchor_tpos;
+        double fl = 0;
+        for (int i = 0; i < p->n_tasks; ++i) {
+            info->task_chunk[i] = p->tasks[i].chunk;
+            info->task_stage[i] = p->tasks[i].stage;
+            info->task_ctx[i] = p->tasks[i].n_ctx;
+            fl += 4.0 * p->NC * (double)p->tasks[i].n_ctx * p->NC * p->D * p->H;
+        }
+        info->attn_flops = fl;
+    }
+    return WF_OK;
+}
+
+int wf_page_table(wf_plan_t p, int32_t *out, int cap, int *n_rows) {
+    if (!p || !n_rows || (cap > 0 && !out) || cap < 0) return WF_EINVAL;
+    if (p->k < 0) return WF_ENOROUND;
+    int n = 0;
+    for (int i = 0; i < p->n_tasks; ++i) {
+        const HostTask &t = p->tasks[i];
+        for (int e = 0; e < t.n_ctx; ++e, ++n) {
+            if (n >= cap) continue;
+            int32_t *r = out + 10 * n;
+            r[0] = t.stage; r[1] = t.chunk; r[2] = t.stage; r[3] = t.dest; r[4] = e;
+            r[5] = t.ctx[e].kind; r[6] = t.ctx[e].chunk; r[7] = t.ctx[e].j;
+            r[8] = t.ctx[e].page; r[9] = t.ctx[e].tpos;
+        }
+    }
+    *n_rows = n;
+    return WF_OK;
+}
+
+int wf_qkv_rope_publish(wf_plan_t p, int layer, const void *qkv, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (p->k < 0) return WF_ENOROUND;
+    if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
+    if (!qkv || ((uintptr_t)qkv & 15)) return WF_EINVAL;
+    WfRoundDev rd = p->rd;
+    int new_rot = p->anchor_rot[layer];
+    if (rd.raw_copy_task >= 0) {
+        new_rot = 0;  // the store of chunk 0 writes the anchor at its own position
+    } else if (p->anchor_tpos >= 0 && p->anchor_rot[layer] != p->anchor_tpos) {
+        rd.rerotate = 1;
+        new_rot = p->anchor_tpos;
+    }
+    if (wf_launch_publish(p->g, rd, layer, p->o.dtype, qkv, p->qbuf, p->pool, p->scratch,
+                          stream) != cudaSuccess)
+        return WF_ECUDA;
+    p->anchor_rot[layer] = new_rot;
+    p->published[layer] = p->k;
+    return WF_OK;
+}
+
+int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (p->k < 0) return WF_ENOROUND;
+    if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
+    if (!out || ((uintptr_t)out & 15)) return WF_EINVAL;
+    if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
+    if (p->published[layer] != p->k) return WF_EORDER;
+    bool tc_ok = p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype);
+    bool simt_ok = p->D % 32 == 0 && p->D <= 128;
+    if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
+    cudaError_t e;
+    if (kernel == WF_ATTN_TC) {
+        if (!tc_ok) return WF_EUNSUPPORTED;
+        e = wf_launch_attn_tc(p->g, p->rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream);
+    } else {
+        if (!simt_ok) return WF_EUNSUPPORTED;
+        e = wf_launch_attn_simt(p->g, p->rd, layer, p->o.dtype, p->qbuf, p->pool, out, stream);
+    }
+    return e == cudaSuccess ? WF_OK : WF_ECUDA;
+}
+
+int wf_sync_status(wf_plan_t p, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    uint32_t st[4] = {0, 0, 0, 0};
+    if (cudaMemcpyAsync(st, p->scratch, sizeof(st), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return WF_ECUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return WF_ECUDA;
+    if (st[0] != 0) {
+        uint32_t z[4] = {0, 0, 0, 0};
+        if (cudaMemcpy(p->scratch, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
+            return WF_ECUDA;
+        return WF_ETIMEOUT;
+    }
+    return WF_OK;
+}
+
+void wf_plan_destroy(wf_plan_t p) { delete p; }
+
+}  // extern "C"

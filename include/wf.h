@@ -1,0 +1,186 @@
+/*
+ * wf.h -- C ABI of the wavefront-round library (libwf.so).
+ *
+ * One wavefront round of the chunk-wise causal DiT forward of "Wave Forcing:
+ * Towards Speed-of-Light Streaming Video Generation" (arXiv 2611.00859), on
+ * one GPU.  In round k the S+1 tasks -- chunk i = k - s at denoising stage s
+ * for every active s < S, plus the store pass of chunk k - S (stage S) -- are
+ * batched into the same kernels (Sec. 3.1 Eq. 3).  Each query token attends
+ * bidirectionally inside its own chunk and to the paged K/V of earlier,
+ * cleaner chunks under M_WF(s, j) = 1[j >= s] (Sec. 3.1 Eq. 4), in the
+ * ordered context anchor, history, live store, live stages j >= s (Eq. 5).
+ *
+ * Conventions shared by every entry point:
+ *  - Every function returns an int: WF_OK (0) on success, a negative WF_E*
+ *    code otherwise.  Arguments are validated on the host before anything is
+ *    launched; a rejected call launches nothing and changes no state.
+ *  - Device pointers are caller-owned (the library never frees caller memory
+ *    and allocates no device memory of its own: every device buffer, scratch
+ *    included, is passed in through wf_bind).  The plan owns host state only.
+ *  - Launching calls are asynchronous on the caller's stream; a plan is not
+ *    thread-safe (one plan per host thread).
+ *  - "slot" s in [0, S] indexes the fixed per-stage buffers: slot s < S holds
+ *    the task at denoising stage s, slot S the store task.  Slots of inactive
+ *    stages (pipeline fill/drain) are neither read nor written.
+ *  - Element type of every activation buffer is the plan's dtype
+ *    (WF_BF16: bfloat16, WF_FP32: float).
+ *
+ * Layouts (row-major, innermost last; N_C = chunk_tokens, H = heads,
+ * D = head_dim, L = layers, P = n_pages from wf_plan_buffer_sizes):
+ *   qkv      [S+1][N_C][3][H][D]   raw (pre-RoPE) Q/K/V of each slot, the
+ *                                   token-major order a QKV projection writes
+ *   qbuf     [S+1][H][N_C][D]       RoPE-applied queries (library workspace)
+ *   pool     [P][L][2][H][N_C][D]   K/V pages (index 0 = K, 1 = V); page ids
+ *                                   follow wf_page_table
+ *   out      [S+1][N_C][H][D]       attention output, token-major
+ */
+#ifndef WF_H
+#define WF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t; /* identical to CUDA's own typedef */
+
+/* ---- return codes ------------------------------------------------------ */
+#define WF_OK            0
+#define WF_EINVAL       -1  /* bad argument (null pointer, bad enum, misaligned) */
+#define WF_ERANGE       -2  /* size or index out of the supported range */
+#define WF_ENOMEM       -3  /* a caller buffer is smaller than required */
+#define WF_ECUDA        -4  /* a CUDA runtime/driver call failed */
+#define WF_ETIMEOUT     -5  /* a device-side bounded wait gave up (see wf_sync_status) */
+#define WF_EDONE        -6  /* the request has no more rounds (k >= N_chunk + S) */
+#define WF_EUNBOUND     -7  /* wf_bind has not been called */
+#define WF_ENOROUND     -8  /* no current round: call wf_round_step first */
+#define WF_EUNSUPPORTED -9  /* shape/dtype not supported by the requested kernel */
+#define WF_EORDER      -10  /* attention before this round's publication of that layer */
+
+#define WF_FP32 0
+#define WF_BF16 1
+
+#define WF_ANCHOR_ADJACENT 0 /* anchor re-rotated just before the oldest retained chunk */
+#define WF_ANCHOR_ABSOLUTE 1 /* anchor keeps its own position (frames 0..grid_t-1) */
+
+#define WF_KIND_ANCHOR  0
+#define WF_KIND_HISTORY 1
+#define WF_KIND_STORE   2
+#define WF_KIND_LIVE    3
+
+#define WF_MAX_STAGES 8   /* S <= 8, so at most 9 tasks per round */
+#define WF_MAX_CTX    32  /* at most 32 chunks in one task's ordered context */
+
+#define WF_ATTN_AUTO 0    /* tensor-core kernel when supported, else the SIMT kernel */
+#define WF_ATTN_TC   1    /* tcgen05/TMEM/TMA kernel (bf16, head_dim 128) */
+#define WF_ATTN_SIMT 2    /* CUDA-core kernel (fp32 or bf16, head_dim 32..128, %32) */
+
+typedef struct wf_plan_s *wf_plan_t; /* opaque, library-owned host state */
+
+typedef struct wf_plan_opts {
+    int n_chunks;       /* N_chunk, chunks in the request (>= 1) */
+    int layers;         /* L, transformer layers with a K/V page each (>= 1) */
+    int grid_t;         /* latent frames per chunk (3 in the paper, App. A) */
+    int grid_h, grid_w; /* patch grid; grid_t*grid_h*grid_w == chunk_tokens */
+    int dtype;          /* WF_BF16 (default) or WF_FP32 */
+    int use_anchor;     /* 1 (default): first clean chunk is a persistent anchor (App. B.3) */
+    int anchor_mode;    /* WF_ANCHOR_ADJACENT (default) or WF_ANCHOR_ABSOLUTE */
+    double rope_theta;  /* RoPE base, default 10000 */
+} wf_plan_opts;
+
+typedef struct wf_buffer_sizes {
+    size_t qkv;      /* bytes of one round's raw Q/K/V input */
+    size_t qbuf;     /* bytes of the query workspace */
+    size_t pool;     /* bytes of the K/V page pool */
+    size_t out;      /* bytes of one attention output */
+    size_t scratch;  /* bytes of library scratch (RoPE tables, scheduler counters, status) */
+    int n_pages;     /* P */
+    int ring_pages;  /* R: clean-history ring incl. the live store page */
+} wf_buffer_sizes;
+
+typedef struct wf_round_info {
+    int k;                 /* round just entered, 0 .. N_chunk+S-1 */
+    int n_tasks;           /* active tasks, 1 .. S+1 */
+    int store_chunk;       /* chunk whose store pass runs (its clean output B_i completes), or -1 */
+    int anchor_tpos;       /* temporal chunk position of the anchor's keys this round, or -1 */
+    int task_chunk[WF_MAX_STAGES + 1];  /* per active task (slot order): chunk i */
+    int task_stage[WF_MAX_STAGES + 1];  /* stage s (== slot); S for the store */
+    int task_ctx[WF_MAX_STAGES + 1];    /* chunks in its ordered context */
+    double attn_flops;     /* algorithmic attention FLOPs of one layer: sum 4*N_C*keys*D*H */
+} wf_round_info;
+
+/* Fill *opts with the defaults listed above (n_chunks = 1, layers = 1,
+ * grid_t = 3, grid_h = grid_w = 0 meaning "chunk_tokens/3 x 1"). */
+void wf_plan_opts_default(wf_plan_opts *opts);
+
+/* Create a plan for one request: S denoising stages (store = stage S),
+ * chunk_tokens = N_C, heads = H, head_dim = D, history_chunks = W clean
+ * chunks kept besides the anchor (-1 = all).  "Wave Forcing" Sec. 3.1
+ * Eq. 3-5; App. B.2 Eq. 13 and App. B.8 (fixed page capacity: anchor,
+ * W history + live store ring, S live pages, plus one page that keeps the
+ * anchor's unrotated key, App. B.3).  No CUDA call is made.
+ * Errors: WF_EINVAL (null out, bad enum, odd D, grid mismatch), WF_ERANGE
+ * (S > WF_MAX_STAGES, context longer than WF_MAX_CTX, sizes overflow). */
+int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks,
+            const wf_plan_opts *opts, wf_plan_t *out);
+
+/* Bytes of every caller-owned buffer this plan needs.  No CUDA call. */
+int wf_plan_buffer_sizes(wf_plan_t plan, wf_buffer_sizes *out);
+
+/* Attach caller-owned device memory (all 256-byte aligned, sizes from
+ * wf_plan_buffer_sizes) and the current CUDA device.  Uploads the RoPE
+ * tables into scratch (synchronous), zeroes the scratch control words, and
+ * encodes the TMA descriptors.  May be called again to re-bind.
+ * Errors: WF_EINVAL (null/misaligned), WF_ECUDA. */
+int wf_bind(wf_plan_t plan, void *pool, void *qbuf, void *scratch);
+
+/* Advance to the next round k (the first call enters k = 0).  Host only:
+ * promotes the previous round's store page into history, evicts the oldest
+ * history page beyond W, allocates the store page of chunk k - S, and builds
+ * the ordered contexts of the round (Algorithm 1, App. B.3).  info may be
+ * NULL.  Errors: WF_EDONE after round N_chunk + S - 1 (state unchanged). */
+int wf_round_step(wf_plan_t plan, wf_round_info *info);
+
+/* Export the current round's table as int32 rows, one per context entry:
+ *   {slot, chunk, stage, dest_page, ctx_index, kind, entry_chunk, j, page, tpos}
+ * (10 ints per row, tasks in slot order, entries in Eq. 5 order).  Writes at
+ * most cap rows and stores the row count in *n_rows.  Errors: WF_ENOROUND. */
+int wf_page_table(wf_plan_t plan, int32_t *out, int cap, int *n_rows);
+
+/* QKV publication of one layer (Sec. 4.2: "publishes K/V after QKV
+ * projection and RoPE"; App. B.2 paged placement Eq. 13).  For every active
+ * task: applies 3D RoPE to Q and K at the task chunk's absolute positions,
+ * writes Q to qbuf[slot] and K/V straight into the task's fixed page (live
+ * page of its stage; ring page of the stored chunk; the anchor page -- plus
+ * its unrotated key -- when chunk 0 is stored).  When the anchor's position
+ * differs from the one its page of this layer was last rotated at, the same
+ * launch re-rotates the anchor key from its unrotated copy (App. B.3).
+ * qkv: device pointer, layout above.  Errors: WF_EUNBOUND, WF_ENOROUND,
+ * WF_ERANGE (layer), WF_EINVAL (null), WF_ECUDA (launch). */
+int wf_qkv_rope_publish(wf_plan_t plan, int layer, const void *qkv, cudaStream_t stream);
+
+/* Round attention of one layer: one launch computes, for every active task
+ * and head, softmax(Q K^T / sqrt(D)) V over the task's ordered context
+ * (Eq. 5) read from the page pool, bidirectional inside each chunk; keys of
+ * chunks outside the context are never visited (Sec. 3.1 Eq. 4).
+ * out: device pointer [S+1][N_C][H][D].  kernel: WF_ATTN_*.
+ * Uses scratch (scheduler counters; calls that overlap on the GPU with the
+ * same scratch race).  Errors: WF_EUNBOUND, WF_ENOROUND, WF_ERANGE,
+ * WF_EINVAL, WF_EORDER (wf_qkv_rope_publish of this layer has not run in
+ * this round: the pages would hold stale K/V), WF_EUNSUPPORTED (kernel not
+ * available for dtype/head_dim), WF_ECUDA. */
+int wf_round_attention(wf_plan_t plan, int layer, void *out, int kernel, cudaStream_t stream);
+
+/* Read and clear the device status word in scratch (synchronises stream).
+ * Returns WF_OK, WF_ETIMEOUT if a kernel's bounded wait gave up, or WF_ECUDA. */
+int wf_sync_status(wf_plan_t plan, cudaStream_t stream);
+
+void wf_plan_destroy(wf_plan_t plan);
+const char *wf_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WF_H */

@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and exports
+every symbol include/wf.h declares, argument validation returns the
+documented codes, and the library's schedule / page ring matches the oracle
+bit for bit ("Wave Forcing" Sec. 3.1 Eq. 3-5, App. B.3)."""
+
+import ctypes
+import itertools
+import os
+import re
+
+import pytest
+
+import chunk_causal_dit_round_b300 as wf
+from oracle import schedule as sch
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "wf.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wf_[a-z_]+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported():
+    names = declared_functions()
+    assert len(names) >= 10
+    assert sorted(names) == sorted(wf.SYMBOLS)
+    for n in names:
+        assert hasattr(wf.lib, n), n
+
+
+def _plan(S, NC, H, D, W, **kw):
+    o = wf.default_opts()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    h = ctypes.c_void_p()
+    rc = wf.lib.wf_plan(S, NC, H, D, W, ctypes.byref(o), ctypes.byref(h))
+    return rc, h
+
+
+def test_validation_codes():
+    assert _plan(0, 48, 2, 32, -1, n_chunks=6)[0] == wf.WF_ERANGE
+    assert _plan(9, 48, 2, 32, -1, n_chunks=6)[0] == wf.WF_ERANGE
+    assert _plan(2, 48, 2, 30, -1, n_chunks=6)[0] == wf.WF_EINVAL       # D % 8
+    assert _plan(2, 48, 2, 32, -2, n_chunks=6)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=6, grid_h=5, grid_w=4)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=6, dtype=7)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=6, anchor_mode=3)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=40)[0] == wf.WF_ERANGE      # context > 32 chunks
+    assert wf.lib.wf_plan(2, 48, 2, 32, -1, None, None) == wf.WF_EINVAL
+    rc, h = _plan(2, 48, 2, 32, -1, n_chunks=6, grid_h=4, grid_w=4)
+    assert rc == wf.WF_OK
+    try:
+        n = ctypes.c_int()
+        buf = (ctypes.c_int32 * 10)()
+        assert wf.lib.wf_page_table(h, buf, 1, ctypes.byref(n)) == wf.WF_ENOROUND
+        assert wf.lib.wf_qkv_rope_publish(h, 0, ctypes.c_void_p(256), None) == wf.WF_EUNBOUND
+        assert wf.lib.wf_round_attention(h, 0, ctypes.c_void_p(256), 0, None) == wf.WF_EUNBOUND
+        assert wf.lib.wf_bind(h, None, None, None) == wf.WF_EINVAL
+        assert wf.lib.wf_bind(h, ctypes.c_void_p(256), ctypes.c_void_p(257),
+                              ctypes.c_void_p(512)) == wf.WF_EINVAL
+        info = wf.wf_round_info()
+        for k in range(8):
+            assert wf.lib.wf_round_step(h, ctypes.byref(info)) == wf.WF_OK
+            assert info.k == k
+        assert wf.lib.wf_round_step(h, ctypes.byref(info)) == wf.WF_EDONE
+        assert info.k == 7
+    finally:
+        wf.lib.wf_plan_destroy(h)
+    for c in (0, -1, -5, -10, -99):
+        assert wf.lib.wf_strerror(c)
+
+
+def test_buffer_sizes():
+    rc, h = _plan(4, 4680, 12, 128, 3, n_chunks=133, layers=30, grid_h=30, grid_w=52)
+    assert rc == 0
+    s = wf.wf_buffer_sizes()
+    assert wf.lib.wf_plan_buffer_sizes(h, ctypes.byref(s)) == 0
+    # pages: anchor + (W+1) ring + S live + unrotated-anchor page (App. B.8)
+    assert s.n_pages == 1 + 4 + 4 + 1 and s.ring_pages == 4
+    tok = 4680 * 12 * 128 * 2
+    assert s.qkv == 5 * 3 * tok and s.qbuf == 5 * tok and s.out == 5 * tok
+    assert s.pool == 10 * 30 * 2 * tok
+    wf.lib.wf_plan_destroy(h)
+
+
+def _oracle_rows(cfg, k):
+    rows = []
+    for t in sch.round_tasks(cfg, k):
+        for i, e in enumerate(t.context):
+            rows.append((t.stage, t.chunk, t.stage, t.dest_page, i, e.kind, e.chunk, e.j, e.page, e.tpos))
+    return rows
+
+
+CFGS = [sch.Cfg(S, N, W, a, m) for S, N, W, a, m in itertools.product(
+    [1, 2, 4, 5], [1, 3, 6, 12], [-1, 0, 1, 3], [True, False],
+    [sch.ANCHOR_ADJACENT, sch.ANCHOR_ABSOLUTE])] + [sch.Cfg(4, 133, 3), sch.Cfg(5, 135, 3)]
+
+
+@pytest.mark.parametrize("cfg", CFGS, ids=str)
+def test_page_table_bit_exact_vs_oracle(cfg):
+    rc, h = _plan(cfg.S, 12, 1, 8, cfg.history, n_chunks=cfg.n_chunks, grid_h=2, grid_w=2,
+                  use_anchor=int(cfg.use_anchor), anchor_mode=cfg.anchor_mode)
+    if 1 + (cfg.history if cfg.history >= 0 else cfg.n_chunks - 1) + 1 + cfg.S > wf.WF_MAX_CTX:
+        assert rc == wf.WF_ERANGE
+        return
+    assert rc == wf.WF_OK
+    s = wf.wf_buffer_sizes()
+    wf.lib.wf_plan_buffer_sizes(h, ctypes.byref(s))
+    assert s.n_pages == sch.n_pages(cfg)
+    try:
+        info = wf.wf_round_info()
+        cap = 512
+        buf = (ctypes.c_int32 * (10 * cap))()
+        n = ctypes.c_int()
+        for k in range(sch.n_rounds(cfg)):
+            assert wf.lib.wf_round_step(h, ctypes.byref(info)) == wf.WF_OK
+            assert wf.lib.wf_page_table(h, buf, cap, ctypes.byref(n)) == wf.WF_OK
+            got = [tuple(buf[10 * i:10 * i + 10]) for i in range(n.value)]
+            assert got == _oracle_rows(cfg, k), f"round {k}"
+            tasks = sch.round_tasks(cfg, k)
+            assert info.n_tasks == len(tasks)
+            u = sch.store_chunk(cfg, k)
+            assert info.store_chunk == (u if u is not None else -1)
+            fl = sum(4 * 12 * 12 * len(t.context) * 8 for t in tasks)
+            assert info.attn_flops == fl
+        assert wf.lib.wf_round_step(h, ctypes.byref(info)) == wf.WF_EDONE
+    finally:
+        wf.lib.wf_plan_destroy(h)
