@@ -22,6 +22,12 @@ K/V of a cached chunk are those its store pass produced (stage S), rotated at
 the chunk's own position; the anchor's key is its unrotated store key rotated
 at the anchor's position for this round (App. B.3).  Raw per-task Q/K/V come
 from a caller-supplied function ``raw(chunk, stage, layer) -> [N_C, 3, H, D]``.
+
+``qk_dtype="bf16"`` models the pages' BF16 execution (App. B.1: BF16/FA3
+reference backend; App. B.2: K/V pages hold the published tensors): Q and K
+enter attention as bf16 values after RoPE, so the fp64 rotation is rounded
+to bf16 (round-to-nearest-even) before the fp64 attention.  Default None
+keeps exact fp64 Q/K.
 """
 
 from __future__ import annotations
@@ -33,6 +39,16 @@ import numpy as np
 from . import schedule as sch
 from .attention import masked_attention
 from .rope import rope_chunk
+
+
+def round_to(x: np.ndarray, qk_dtype):
+    """Round fp64 values to the attention input dtype (None: unchanged)."""
+    if qk_dtype is None:
+        return x
+    if qk_dtype != "bf16":
+        raise ValueError(qk_dtype)
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
 
 
 @dataclass(frozen=True)
@@ -53,20 +69,20 @@ class Geom:
         return (self.grid_t, self.grid_h, self.grid_w)
 
 
-def entry_kv(cfg: sch.Cfg, geom: Geom, e: sch.Entry, layer: int, raw):
+def entry_kv(cfg: sch.Cfg, geom: Geom, e: sch.Entry, layer: int, raw, qk_dtype=None):
     """K (RoPE applied at e.tpos) and V of one context entry: [N_C, H, D] each."""
     producer_stage = e.j if e.kind == sch.KIND_LIVE else cfg.S
     x = np.asarray(raw(e.chunk, producer_stage, layer), dtype=np.float64)
     k = rope_chunk(x[:, 1], e.tpos, geom.grid, geom.theta)
-    return k, x[:, 2]
+    return round_to(k, qk_dtype), x[:, 2]
 
 
-def task_queries(geom: Geom, t: sch.Task, layer: int, raw) -> np.ndarray:
+def task_queries(geom: Geom, t: sch.Task, layer: int, raw, qk_dtype=None) -> np.ndarray:
     x = np.asarray(raw(t.chunk, t.stage, layer), dtype=np.float64)
-    return rope_chunk(x[:, 0], t.chunk, geom.grid, geom.theta)
+    return round_to(rope_chunk(x[:, 0], t.chunk, geom.grid, geom.theta), qk_dtype)
 
 
-def round_universe(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw):
+def round_universe(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw, qk_dtype=None):
     """All key tokens of round k: K, V [H, n_keys, D], labels j, page ids and
     chunk ids [n_keys]."""
     seen = {}
@@ -77,7 +93,7 @@ def round_universe(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw):
     ks, vs, lab, pg, ch = [], [], [], [], []
     n = geom.chunk_tokens
     for e in ents:
-        kk, vv = entry_kv(cfg, geom, e, layer, raw)
+        kk, vv = entry_kv(cfg, geom, e, layer, raw, qk_dtype)
         ks.append(kk)
         vs.append(vv)
         lab.append(np.full(n, e.j))
@@ -89,15 +105,16 @@ def round_universe(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw):
 
 
 def round_attention(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw,
-                    rows=None, universe=None):
+                    rows=None, universe=None, qk_dtype=None):
     """Mask formulation.  Returns one array [n_rows, H, D] per task (slot order).
 
     ``rows`` (optional) selects query rows of every task (same indices for all
     tasks); each output row depends on its own query row only."""
-    K, V, lab, _, _ = universe if universe is not None else round_universe(cfg, geom, k, layer, raw)
+    K, V, lab, _, _ = (universe if universe is not None
+                       else round_universe(cfg, geom, k, layer, raw, qk_dtype))
     outs = []
     for t in sch.round_tasks(cfg, k):
-        q = task_queries(geom, t, layer, raw)
+        q = task_queries(geom, t, layer, raw, qk_dtype)
         if rows is not None:
             q = q[np.asarray(rows)]
         mask = np.broadcast_to(lab[None, :] >= t.stage, (q.shape[0], lab.shape[0]))

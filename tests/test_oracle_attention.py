@@ -157,3 +157,15 @@ def test_planted_mask_mistake_is_caught():
             if m.any() and not np.array_equal(m, lab >= t.stage):
                 bad = masked_attention(q0, K, V, m[None, :])
                 assert not np.allclose(bad[:, 0], want[None], atol=1e-6)
+
+
+def test_bf16_rounding_of_attention_inputs():
+    """round_to('bf16') is IEEE round-to-nearest-even onto 8 significant bits."""
+    from oracle.round import round_to
+    x = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -7, -3.0 - 2 ** -7, 2 ** -130 * 3])
+    want = np.array([1.0, 1.0, 1 + 2 ** -6, 1 + 2 ** -7, -3.0, 2 ** -130 * 3])
+    assert np.array_equal(round_to(x, "bf16"), want)
+    assert round_to(x, None) is x
+    y = np.random.default_rng(0).standard_normal(1000)
+    r = round_to(y, "bf16")
+    assert np.all(np.abs(r - y) <= 2.0 ** -8 * np.abs(y))
