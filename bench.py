@@ -34,6 +34,11 @@ sys.path.insert(0, ROOT)
 METRIC = "chunk-causal attention TFLOP/s (% bf16 peak); DiT chunks/s per 1F1C round"
 UNIT = "TFLOP/s"
 
+# DRAM bytes (read + write) of one steady attn_tc_kernel launch, from the ncu
+# capture summarised in profiles/attn_tc_kernel_wan13_round.md.  Set to None
+# whenever the kernel changes, until it is captured again.
+ATTN_TC_TRAFFIC_BYTES = 1.260e9
+
 CONFIGS = {
     # name: (S, grid (t,h,w), heads, head_dim, history W)
     "wan13_attn": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3,
@@ -243,7 +248,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak_tf, 4),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
                      "avg_launch_ms": round(attn_avg, 4),
-                     "flops_per_launch": per_launch, "traffic": None},
+                     "flops_per_launch": per_launch, "traffic": ATTN_TC_TRAFFIC_BYTES},
         "clocks": clocks,
     }
     return res
@@ -303,7 +308,7 @@ def _threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(rows=1024):
+def cpu_baseline(rows=3072):
     fl, dt = OracleSample().run(rows)
     return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": _threads(),
             "kind": "oracle",
