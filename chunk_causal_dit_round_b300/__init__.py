@@ -39,11 +39,12 @@ WF_ATTN_TC = 1
 WF_ATTN_SIMT = 2
 WF_MAX_STAGES = 8
 WF_MAX_CTX = 32
+WF_NOALLOC_SCRATCH_BYTES = 256
 
 # every symbol include/wf.h declares
 SYMBOLS = ["wf_plan_opts_default", "wf_plan", "wf_plan_buffer_sizes", "wf_bind",
            "wf_round_step", "wf_page_table", "wf_qkv_rope_publish", "wf_round_attention",
-           "wf_sync_status", "wf_plan_destroy", "wf_strerror"]
+           "wf_round_attention_noalloc", "wf_sync_status", "wf_plan_destroy", "wf_strerror"]
 
 
 class wf_plan_opts(ctypes.Structure):
@@ -72,7 +73,7 @@ class wf_round_info(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libwf.so is not built ({LIB_PATH}); run "
-                          "`python -m chunk_causal_dit_round_b300.build`")
+                          "`python chunk_causal_dit_round_b300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, VP = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
     sig = {
@@ -84,6 +85,7 @@ def _load():
         "wf_page_table": (I, [P, ctypes.POINTER(ctypes.c_int32), I, ctypes.POINTER(I)]),
         "wf_qkv_rope_publish": (I, [P, I, VP, VP]),
         "wf_round_attention": (I, [P, I, VP, I, VP]),
+        "wf_round_attention_noalloc": (I, [P, I, VP, VP]),
         "wf_sync_status": (I, [P, VP]),
         "wf_plan_destroy": (None, [P]),
         "wf_strerror": (ctypes.c_char_p, [I]),
@@ -199,6 +201,12 @@ class Round:
     def attention(self, layer, out, kernel=WF_ATTN_AUTO, stream=None):
         check(lib.wf_round_attention(self.plan, layer, ctypes.c_void_p(out.data_ptr()), kernel,
                                      _stream_handle(stream)), "wf_round_attention")
+
+    def attention_noalloc(self, layer, out, stream=None):
+        """wf_round_attention_noalloc: the tensor-core kernel with its control
+        words in the library's static device block (no caller scratch)."""
+        check(lib.wf_round_attention_noalloc(self.plan, layer, ctypes.c_void_p(out.data_ptr()),
+                                             _stream_handle(stream)), "wf_round_attention_noalloc")
 
     def sync_status(self, stream=None):
         return lib.wf_sync_status(self.plan, _stream_handle(stream))

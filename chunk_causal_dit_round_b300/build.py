@@ -1,6 +1,7 @@
 """Build libwf.so in-tree with nvcc for sm_103a.
 
-Usage: ``python -m chunk_causal_dit_round_b300.build [--force]``.
+Usage: ``python chunk_causal_dit_round_b300/build.py [--force] [-v]`` (run by
+path: importing the package loads the library, which may not exist yet).
 The library is rebuilt when any source under ``csrc/`` or ``include/`` is
 newer than the shared object.
 """

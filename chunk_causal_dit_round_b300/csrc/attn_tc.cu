@@ -33,6 +33,8 @@
 
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "wf_internal.h"
 #include "wf_ptx.cuh"
 
@@ -472,6 +474,74 @@ cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
     p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.ctl = static_cast<uint32_t *>(scratch);
+    int grid = p.n_units < num_sms ? p.n_units : num_sms;
+    attn_tc_kernel<<<grid, NUM_THREADS, SM_ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
+    return cudaGetLastError();
+}
+
+// ---- launch without caller scratch ------------------------------------------
+// The attention kernel's control words (status, work counter, finished-CTA
+// counter, wait site) in a fixed device block owned by the library.  Static
+// device memory starts zeroed when the module loads; each call clears the
+// control words on its stream before launching, so a call never inherits a
+// previous call's counters.  All calls share this block: kernels that overlap
+// on the GPU race on it.
+static __device__ __align__(256) uint32_t wf_noalloc_scratch[WF_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};  // device address of the block, per device
+}  // namespace
+
+cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int layer,
+                                      const WfTmaps &maps, void *out, int num_sms,
+                                      cudaStream_t stream, int *wf_err) {
+    *wf_err = WF_OK;
+    // bytes of control words the kernel reads and writes (up to the wait-site word)
+    const size_t need = WF_SCRATCH_WHERE + sizeof(uint32_t);
+    if (need > WF_NOALLOC_SCRATCH_BYTES) {
+        *wf_err = WF_ERANGE;
+        return cudaSuccess;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *wf_err = WF_ERANGE;
+        return cudaSuccess;
+    }
+    void *ctl = nullptr;
+    {
+        // once per device, with that device current: the host-side name of a
+        // __device__ array is not a device address, so look the address up.
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {
+            void *a = nullptr;
+            e = cudaGetSymbolAddress(&a, wf_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            g_noalloc_addr[dev] = a;
+        }
+        ctl = g_noalloc_addr[dev];
+    }
+    if (rd.n_tasks < 1) return cudaSuccess;
+    e = cudaMemsetAsync(ctl, 0, need, stream);
+    if (e != cudaSuccess) return e;
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SM_ALLOC);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    TcParams p;
+    p.layer = layer;
+    p.tpc = (g.NC + BN - 1) / BN;
+    p.qpairs = ((g.NC + BM - 1) / BM + 1) / 2;
+    p.n_units = rd.n_tasks * g.H * p.qpairs;
+    p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ctl = static_cast<uint32_t *>(ctl);
     int grid = p.n_units < num_sms ? p.n_units : num_sms;
     attn_tc_kernel<<<grid, NUM_THREADS, SM_ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
     return cudaGetLastError();

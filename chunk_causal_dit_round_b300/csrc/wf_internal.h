@@ -64,3 +64,9 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
 cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
                               cudaStream_t stream);
+
+// Variant of wf_launch_attn_tc whose control words live in a static device
+// block inside the library (no caller scratch); see wf_round_attention_noalloc.
+cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int layer,
+                                      const WfTmaps &maps, void *out, int num_sms,
+                                      cudaStream_t stream, int *wf_err);

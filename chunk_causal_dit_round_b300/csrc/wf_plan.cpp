@@ -412,6 +412,21 @@ int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream
     return e == cudaSuccess ? WF_OK : WF_ECUDA;
 }
 
+int wf_round_attention_noalloc(wf_plan_t p, int layer, void *out, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (p->k < 0) return WF_ENOROUND;
+    if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
+    if (!out || ((uintptr_t)out & 15)) return WF_EINVAL;
+    if (p->published[layer] != p->k) return WF_EORDER;
+    if (!(p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype))) return WF_EUNSUPPORTED;
+    int wf_err = WF_OK;
+    cudaError_t e = wf_launch_attn_tc_noalloc(p->g, p->rd, layer, p->tmaps, out, p->num_sms,
+                                              stream, &wf_err);
+    if (e != cudaSuccess) return WF_ECUDA;
+    return wf_err;
+}
+
 int wf_sync_status(wf_plan_t p, cudaStream_t stream) {
     if (!p) return WF_EINVAL;
     if (!p->bound) return WF_EUNBOUND;

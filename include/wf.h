@@ -173,6 +173,38 @@ int wf_qkv_rope_publish(wf_plan_t plan, int layer, const void *qkv, cudaStream_t
  * available for dtype/head_dim), WF_ECUDA. */
 int wf_round_attention(wf_plan_t plan, int layer, void *out, int kernel, cudaStream_t stream);
 
+/* Round attention without caller-provided scratch.  The paper has no
+ * counterpart: this is a library convenience.
+ *
+ * Same computation, kernel and output as wf_round_attention(plan, layer, out,
+ * WF_ATTN_TC, stream) -- the tensor-core kernel, so bf16 with head_dim 128
+ * only (else WF_EUNSUPPORTED) -- but the kernel's scheduler counters and
+ * status word live in a fixed block of WF_NOALLOC_SCRATCH_BYTES inside
+ * libwf.so instead of the plan's scratch buffer.  It is meant for callers
+ * that cannot allocate device memory at the point where they launch
+ * attention: code running under a memory manager that owns every device
+ * byte (a caching allocator or an arena sized at start-up), or a
+ * steady-state loop that must not call cudaMalloc because it can
+ * synchronise the whole device.  This call itself calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * - The first call on a device (the current device) looks up the block's
+ *   device address once (cudaGetSymbolAddress); make that first call before
+ *   any stream capture.  Every GPU that loads the library holds the block
+ *   until the process exits.
+ * - Each call clears the block's counters on `stream` (cudaMemsetAsync of
+ *   the control words) before the launch.  All calls share the one block,
+ *   so calls whose kernels overlap on the GPU (different streams, or
+ *   different plans on the same device) race; serialise them.
+ * - The control words the kernel needs must fit in the block; a larger need
+ *   is rejected with WF_ERANGE before anything is launched.
+ * - A bounded-wait timeout inside the kernel is recorded in the block, not
+ *   in the plan's scratch, so wf_sync_status does not see it.
+ * Errors: as wf_round_attention, plus WF_ERANGE (control block too small)
+ * and WF_ECUDA (symbol lookup, memset or launch failed). */
+#define WF_NOALLOC_SCRATCH_BYTES 256
+int wf_round_attention_noalloc(wf_plan_t plan, int layer, void *out, cudaStream_t stream);
+
 /* Read and clear the device status word in scratch (synchronises stream).
  * Returns WF_OK, WF_ETIMEOUT if a kernel's bounded wait gave up, or WF_ECUDA. */
 int wf_sync_status(wf_plan_t plan, cudaStream_t stream);
