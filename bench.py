@@ -37,7 +37,7 @@ UNIT = "TFLOP/s"
 # DRAM bytes (read + write) of one steady attn_tc_kernel launch, from the ncu
 # capture summarised in profiles/attn_tc_kernel_wan13_round.md.  Set to None
 # whenever the kernel changes, until it is captured again.
-ATTN_TC_TRAFFIC_BYTES = 1.260e9
+ATTN_TC_TRAFFIC_BYTES = None
 
 CONFIGS = {
     # name: (S, grid (t,h,w), heads, head_dim, history W)

@@ -68,6 +68,16 @@ constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;  // alignment slack
 
 constexpr uint64_t WAIT_NS = 1000000000ull;  // 1 s
 
+// Register split: the kernel is launched with LAUNCH_REGS per thread (384 x
+// 168 = 64512 of the SM's 65536); the producer/MMA warpgroup gives up
+// 4 warps x 32 x (168 - 56) registers and the two softmax warpgroups take
+// 8 warps x 32 x (224 - 168) -- the same 14336, so the increase never waits.
+constexpr int LAUNCH_REGS = 168;
+constexpr int REGS_SOFTMAX = 224;
+constexpr int REGS_AUX = 56;
+static_assert(8 * (REGS_SOFTMAX - LAUNCH_REGS) <= 4 * (LAUNCH_REGS - REGS_AUX),
+              "register split exceeds the launch pool");
+
 struct TcParams {
     int layer;
     int n_units;
@@ -251,28 +261,46 @@ __device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const
                 for (int i = 0; i < 32; ++i)
                     if (q * 32 + i >= valid) r[q][i] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row max: 8 independent chains of 3-input max over 16 scores each
+        float pm[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int a = 0; a < 8; ++a) {
+            const uint32_t *v = &r[a >> 1][(a & 1) * 16];
+            float m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r[q][i]));
+            for (int i = 3; i < 15; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+            pm[a] = fmaxf(m, __uint_as_float(v[15]));
+        }
+        const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                               fmaxf(pm[6], pm[7]));
         const float mnew = mx * sl2;
         float alpha = 1.f;
         if (mnew > m_run + 8.f) {
             alpha = ex2(m_run - mnew);
             m_run = mnew;
         }
-        float sum = 0.f;
+        // p = 2^(s*sl2 - m_run) on packed pairs; 4 independent packed partial sums
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm2 = f2_pack(-m_run, -m_run);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[2][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 4; ++q) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float p0 = ex2(fmaf(__uint_as_float(r[q][2 * i]), sl2, -m_run));
-                float p1 = ex2(fmaf(__uint_as_float(r[q][2 * i + 1]), sl2, -m_run));
-                sum += p0 + p1;
+                uint64_t x = f2_fma(f2_pack(__uint_as_float(r[q][2 * i]), __uint_as_float(r[q][2 * i + 1])),
+                                    sl2x2, negm2);
+                float a0, a1;
+                f2_unpack(x, a0, a1);
+                const float p0 = ex2(a0), p1 = ex2(a1);
+                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
                 pk[q >> 1][(q & 1) * 16 + i] = pack_bf16(p0, p1);
             }
+        }
+        float s0, s1, s2, s3;
+        f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
+        f2_unpack(f2_add(acc[2], acc[3]), s2, s3);
+        const float sum = (s0 + s1) + (s2 + s3);
         l_run = l_run * alpha + sum;
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -365,28 +393,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Every role walks the same unit sequence; units end on named barrier 1
+    // over all 384 threads, after which the next unit index (fetched by
+    // thread 0) is read.  Each role has its own loop so that the register
+    // budget set right before it applies to the whole loop.
     uint32_t seq = 0, it_base = 0, unit_iter = 0, issued = 0;
-    int u = unit_slot[0];
-    while (u < p.n_units) {
-        int ti, h, qp;
-        decode_unit(u, rd, p, g.H, ti, h, qp);
-        const int n = rd.n_ctx[ti] * p.tpc;
-        if (warp < 8) {
-            softmax_tile(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
-        } else if (warp == 8) {
-            if (lane == 0) producer(c, &tq, &tkv, g, rd, p, ti, h, qp, n, seq, &issued);
-        } else if (warp == 9) {
-            if (lane == 0) mma_issuer(c, tmem, n, seq, it_base, unit_iter);
-        }
+    auto next_unit = [&](int n) -> int {
         seq += 2 * n;
         it_base += n;
         unit_iter += 1;
         if (threadIdx.x == 0) unit_slot[unit_iter & 1] = (int)(gridDim.x + atomicAdd(work, 1u));
         tc_fence_before();
-        __syncthreads();
+        named_bar_sync(1, NUM_THREADS);
         tc_fence_after();
-        if (*c.abort) break;
-        u = unit_slot[unit_iter & 1];
+        return *c.abort ? p.n_units : unit_slot[unit_iter & 1];
+    };
+    if (warp < 8) {
+        reg_inc<REGS_SOFTMAX>();
+        for (int u = unit_slot[0]; u < p.n_units;) {
+            int ti, h, qp;
+            decode_unit(u, rd, p, g.H, ti, h, qp);
+            const int n = rd.n_ctx[ti] * p.tpc;
+            softmax_tile(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
+            u = next_unit(n);
+        }
+    } else {
+        reg_dec<REGS_AUX>();
+        for (int u = unit_slot[0]; u < p.n_units;) {
+            int ti, h, qp;
+            decode_unit(u, rd, p, g.H, ti, h, qp);
+            const int n = rd.n_ctx[ti] * p.tpc;
+            if (warp == 8 && lane == 0)
+                producer(c, &tq, &tkv, g, rd, p, ti, h, qp, n, seq, &issued);
+            else if (warp == 9 && lane == 0)
+                mma_issuer(c, tmem, n, seq, it_base, unit_iter);
+            u = next_unit(n);
+        }
     }
 
     if (*c.abort) {
@@ -397,7 +439,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (uint32_t s = first; s < issued; ++s)
                 mbar_wait(c.bar(B_KVFULL + s % NST), (s / NST) & 1, nullptr, nullptr, nullptr, 0,
                           WAIT_NS);
-            mbar_wait(c.bar(B_QFULL), unit_iter & 1, nullptr, nullptr, nullptr, 0, WAIT_NS);
+            if (unit_iter > 0)  // the Q tiles of the unit that was cut short
+                mbar_wait(c.bar(B_QFULL), (unit_iter - 1) & 1, nullptr, nullptr, nullptr, 0,
+                          WAIT_NS);
         }
         if (warp == 9 && lane == 0) {
             mma_commit(c.bar(B_DRAIN));
@@ -416,6 +460,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             atomicExch(done, 0u);
         }
     }
+}
+
+// Opt in to the shared-memory size and refuse to launch unless the kernel was
+// compiled to exactly the register count the setmaxnreg split assumes.
+cudaError_t prepare_kernel() {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SM_ALLOC);
 }
 
 }  // namespace
@@ -461,8 +516,7 @@ cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
     if (rd.n_tasks < 1) return cudaSuccess;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
+        cudaError_t e = prepare_kernel();
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -529,8 +583,7 @@ cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int
     if (e != cudaSuccess) return e;
     static bool attr_set = false;
     if (!attr_set) {
-        e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SM_ALLOC);
+        e = prepare_kernel();
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
