@@ -59,3 +59,43 @@ def qkv_raw(seed: int, chunk: int, stage: int, layer: int, n_tokens: int,
     """Raw Q/K/V of task (chunk, stage) at ``layer``: ``[n_tokens, 3, heads, head_dim]``."""
     return normal(key_of(seed, 1, chunk, stage, layer),
                   (n_tokens, 3, heads, head_dim), scale, dtype)
+
+
+def dit_params(seed: int, dim: int, ffn: int, layers: int, channels: int = 16,
+               freq: int = 256, std: float = 0.02, dtype=torch.bfloat16) -> dict:
+    """Random-initialised DiT parameters ~ N(0, std^2), rounded to ``dtype``.
+
+    Matrices are [out, in] (the layout of a linear layer's weight).  Keys:
+    patch_w [dim, 4C], patch_b, t1_w [dim, freq], t1_b, t2_w [dim, dim],
+    t2_b, tp_w [6 dim, dim], tp_b, head_w [4C, dim], head_b, head_mod
+    [2, dim]; per layer (lists of length ``layers``): qkv_w [3 dim, dim],
+    qkv_b, o_w [dim, dim], o_b, f1_w [ffn, dim], f1_b, f2_w [dim, ffn], f2_b,
+    mod [6, dim]."""
+    p = 4 * channels
+
+    def g(tag, *shape):
+        return normal(key_of(seed, 7, *tag), shape, std, dtype)
+
+    out = {
+        "patch_w": g((0, 0), dim, p), "patch_b": g((0, 1), dim),
+        "t1_w": g((1, 0), dim, freq), "t1_b": g((1, 1), dim),
+        "t2_w": g((2, 0), dim, dim), "t2_b": g((2, 1), dim),
+        "tp_w": g((3, 0), 6 * dim, dim), "tp_b": g((3, 1), 6 * dim),
+        "head_w": g((4, 0), p, dim), "head_b": g((4, 1), p),
+        "head_mod": g((4, 2), 2, dim),
+    }
+    per = {"qkv_w": (3 * dim, dim), "qkv_b": (3 * dim,), "o_w": (dim, dim), "o_b": (dim,),
+           "f1_w": (ffn, dim), "f1_b": (ffn,), "f2_w": (dim, ffn), "f2_b": (dim,),
+           "mod": (6, dim)}
+    for i, (name, shape) in enumerate(per.items()):
+        out[name] = [g((10, l, i), *shape) for l in range(layers)]
+    return out
+
+
+def latent(seed: int, chunk: int, stage: int, channels: int, frames: int, height: int,
+           width: int) -> torch.Tensor:
+    """N(0, 1) fp32 latent draw keyed by (chunk, stage): [C, F, H, W].  Used
+    both as the fresh noise of a chunk (stage -1) and as the transition draw
+    eps_{chunk, stage}."""
+    return normal(key_of(seed, 2, chunk, stage), (channels, frames, height, width), 1.0,
+                  torch.float32)
