@@ -47,6 +47,124 @@ CONFIGS = {
 }
 
 
+DIT_CONFIGS = {
+    # name: Wan2.1-shaped DiT rounds (random-init weights ~ N(0, 0.02), bf16)
+    "dit13": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
+                  layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0],
+                  desc="random-init Wan2.1-1.3B-shaped DiT, 4-step (S=4), 30 blocks, dim 1536, "
+                       "12x128 heads, FFN 8960, 4680-token chunks, W=3 + anchor, 64 chunks"),
+    "dit13_s5": dict(S=5, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
+                     layers=30, n_chunks=135, steps=[1000.0, 800.0, 600.0, 400.0, 200.0],
+                     desc="long rollout, 5-step (S=5), same 1.3B shapes, 135 chunks, paged K/V "
+                          "ring with oldest-chunk eviction, W=3 + anchor"),
+}
+
+
+def _sustained_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return d["bf16_tflops_sustained"], "measured"
+    return 1400.0, "fallback"
+
+
+def run_dit(args, name, rank, world, steps=None, warmup=None):
+    """Steady wavefront rounds of the whole DiT forward (wf_dit_round): per
+    layer LN + modulation, QKV projection + RoPE + paged publish, round
+    attention, output projection + gated residual, LN, FFN; then the head and
+    the stage transition.  One completed chunk per steady round (1F1C)."""
+    import torch
+    import chunk_causal_dit_round_b300 as wf
+
+    cfg = DIT_CONFIGS[name]
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    S, W, L = cfg["S"], cfg["history"], cfg["layers"]
+    NC = math.prod(cfg["grid"])
+    H, D, dim, ffn = cfg["heads"], cfg["head_dim"], cfg["dim"], cfg["ffn"]
+    C = 16
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    k_steady = S + W + 2
+    n_chunks = max(cfg["n_chunks"], k_steady + warmup + steps + 1)
+    r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321 + rank)
+
+    def rnd(*shape, std=0.02):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    P = {"patch_w": rnd(dim, 4 * C), "patch_b": rnd(dim), "t1_w": rnd(dim, 256), "t1_b": rnd(dim),
+         "t2_w": rnd(dim, dim), "t2_b": rnd(dim), "tp_w": rnd(6 * dim, dim), "tp_b": rnd(6 * dim),
+         "head_w": rnd(4 * C, dim), "head_b": rnd(4 * C), "head_mod": rnd(2, dim)}
+    for k_, shp in (("qkv_w", (3 * dim, dim)), ("qkv_b", (3 * dim,)), ("o_w", (dim, dim)),
+                    ("o_b", (dim,)), ("f1_w", (ffn, dim)), ("f1_b", (ffn,)), ("f2_w", (dim, ffn)),
+                    ("f2_b", (dim,)), ("mod", (6, dim))):
+        P[k_] = [rnd(*shp) for _ in range(L)]
+    model = wf.Dit(r, P, ffn=ffn, channels=C, freq=256, timesteps=cfg["steps"])
+    latent = C * cfg["grid"][0] * 4 * cfg["grid"][1] * cfg["grid"][2]
+    n_in = 3
+    zs = [torch.randn(latent, generator=g, device=dev) for _ in range(n_in)]
+    epss = [torch.randn((S, latent), generator=g, device=dev) for _ in range(n_in)]
+    chunk = torch.empty(latent, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def round_flops(info):
+        T = info.n_tasks * NC
+        lin = 2.0 * T * (3 * dim * dim + dim * dim + 2 * dim * ffn) * L
+        return info.attn_flops * L + lin + 2.0 * T * (4 * C) * dim * 2
+
+    i = 0
+    for _ in range(k_steady + warmup):
+        r.step()
+        model.round(zs[i % n_in], epss[i % n_in], None, chunk, stream)
+        i += 1
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    flops = 0.0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for j in range(steps):
+            info = r.step()
+            evs[j][0].record(stream)
+            model.round(zs[i % n_in], epss[i % n_in], None, chunk, stream)
+            evs[j][1].record(stream)
+            flops += round_flops(info)
+            i += 1
+        t1.record(stream)
+        torch.cuda.synchronize()
+    st = r.sync_status()
+    if st != wf.WF_OK:
+        raise RuntimeError(f"device status {st}")
+    ms = t0.elapsed_time(t1)
+    per = sorted(a.elapsed_time(b) for a, b in evs)
+    times = torch.tensor([ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    ms = times.item()
+    chunks_s = world * steps / (ms * 1e-3)
+    peak, src = _sustained_peak()
+    tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
+    res = {"workload": name, "desc": cfg["desc"], "value": round(chunks_s, 3), "unit": "chunks/s",
+           "frames_per_s": round(12 * chunks_s, 2), "round_ms_p50": round(statistics.median(per), 3),
+           "rounds": steps, "eta_slot": round(cfg["n_chunks"] / (cfg["n_chunks"] + S), 4),
+           "flops_per_round": flops / steps,
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                        "peak_source": f"{src} bf16 dense (sustained)"},
+           "gpu_launches_per_round": 4 + 8 * L, "clocks": clk.summary()}
+    del model, r, P
+    torch.cuda.empty_cache()
+    return res
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -346,7 +464,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="wan13_attn", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="wan13_attn", choices=sorted(CONFIGS) + sorted(DIT_CONFIGS))
+    ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -362,7 +481,16 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    if args.config in DIT_CONFIGS:
+        d = run_dit(args, args.config, rank, world)
+        if rank == 0:
+            print(json.dumps(d), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     res = run_ours(args, rank, world)
+    if not args.no_dit:
+        res["dit"] = run_dit(args, "dit13", rank, world, steps=5, warmup=3)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()

@@ -37,6 +37,10 @@ WF_ANCHOR_ABSOLUTE = 1
 WF_ATTN_AUTO = 0
 WF_ATTN_TC = 1
 WF_ATTN_SIMT = 2
+WF_EPI_BF16 = 0
+WF_EPI_F32 = 1
+WF_EPI_GELU_BF16 = 2
+WF_EPI_GATED_RESIDUAL = 3
 WF_MAX_STAGES = 8
 WF_MAX_CTX = 32
 WF_NOALLOC_SCRATCH_BYTES = 256
@@ -44,7 +48,9 @@ WF_NOALLOC_SCRATCH_BYTES = 256
 # every symbol include/wf.h declares
 SYMBOLS = ["wf_plan_opts_default", "wf_plan", "wf_plan_buffer_sizes", "wf_bind",
            "wf_round_step", "wf_page_table", "wf_qkv_rope_publish", "wf_round_attention",
-           "wf_round_attention_noalloc", "wf_sync_status", "wf_plan_destroy", "wf_strerror"]
+           "wf_round_attention_noalloc", "wf_sync_status", "wf_plan_destroy", "wf_strerror",
+           "wf_linear", "wf_qkv_proj_rope_publish", "wf_dit_workspace_size", "wf_dit_bind",
+           "wf_dit_round"]
 
 
 class wf_plan_opts(ctypes.Structure):
@@ -70,6 +76,20 @@ class wf_round_info(ctypes.Structure):
                 ("attn_flops", ctypes.c_double)]
 
 
+class wf_dit_layer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("qkv_w", "qkv_b", "o_w", "o_b", "ffn1_w", "ffn1_b",
+                                               "ffn2_w", "ffn2_b", "modulation")]
+
+
+class wf_dit_model(ctypes.Structure):
+    _fields_ = [("model_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("channels", ctypes.c_int),
+                ("freq_dim", ctypes.c_int), ("shift", ctypes.c_double),
+                ("context_noise", ctypes.c_double), ("timesteps", ctypes.c_double * WF_MAX_STAGES)] + \
+        [(n, ctypes.c_void_p) for n in ("patch_w", "patch_b", "t1_w", "t1_b", "t2_w", "t2_b", "tp_w",
+                                        "tp_b", "head_w", "head_b", "head_mod")] + \
+        [("layers", ctypes.POINTER(wf_dit_layer))]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libwf.so is not built ({LIB_PATH}); run "
@@ -89,6 +109,11 @@ def _load():
         "wf_sync_status": (I, [P, VP]),
         "wf_plan_destroy": (None, [P]),
         "wf_strerror": (ctypes.c_char_p, [I]),
+        "wf_linear": (I, [P, VP, ctypes.c_longlong, I, I, I, VP, VP, I, I, I, VP, I, VP, I, I, VP]),
+        "wf_qkv_proj_rope_publish": (I, [P, I, VP, VP, VP, VP]),
+        "wf_dit_workspace_size": (I, [P, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
+        "wf_dit_bind": (I, [P, ctypes.POINTER(wf_dit_model), VP, VP]),
+        "wf_dit_round": (I, [P, VP, VP, VP, VP, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -116,6 +141,10 @@ def default_opts() -> wf_plan_opts:
     o = wf_plan_opts()
     lib.wf_plan_opts_default(ctypes.byref(o))
     return o
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
 def _stream_handle(stream):
@@ -208,6 +237,23 @@ class Round:
         check(lib.wf_round_attention_noalloc(self.plan, layer, ctypes.c_void_p(out.data_ptr()),
                                              _stream_handle(stream)), "wf_round_attention_noalloc")
 
+    def publish_proj(self, layer, x, w_qkv, b_qkv=None, stream=None):
+        """wf_qkv_proj_rope_publish: QKV projection of x [S+1, N_C, dim] fused
+        with RoPE and paged publication."""
+        check(lib.wf_qkv_proj_rope_publish(self.plan, layer, _ptr(x), _ptr(w_qkv), _ptr(b_qkv),
+                                           _stream_handle(stream)), "wf_qkv_proj_rope_publish")
+
+    def linear(self, a, w, bias, out, epilogue, row_begin=0, row_end=None, gate=None,
+               rows_per_group=1, stream=None):
+        """wf_linear on 2-D tensors: a [rows, K] bf16, w [N, K] bf16."""
+        rows, K = a.shape
+        N = w.shape[0]
+        row_end = rows if row_end is None else row_end
+        check(lib.wf_linear(self.plan, _ptr(a), rows, a.stride(0), row_begin, row_end, _ptr(w),
+                            _ptr(bias), N, K, epilogue, _ptr(out), out.stride(0), _ptr(gate),
+                            gate.stride(0) if gate is not None else 0, rows_per_group,
+                            _stream_handle(stream)), "wf_linear")
+
     def sync_status(self, stream=None):
         return lib.wf_sync_status(self.plan, _stream_handle(stream))
 
@@ -227,3 +273,47 @@ class Round:
             self.close()
         except Exception:
             pass
+
+
+class Dit:
+    """A DiT model bound to a Round: device weights (torch bf16 tensors, kept
+    alive here), the workspace, and ``round(z_new, eps, x0_out, chunk_out)``
+    launching wf_dit_round for the round the plan is in."""
+
+    def __init__(self, rnd: Round, params: dict, *, ffn, channels=16, freq=256, timesteps,
+                 shift=5.0, context_noise=0.0, stream=None):
+        import torch
+        self.r = rnd
+        dev = rnd.pool.device
+        self.params = {k: ([t.to(dev).contiguous() for t in v] if isinstance(v, list)
+                           else v.to(dev).contiguous()) for k, v in params.items()}
+        P = self.params
+        dim = rnd.H * rnd.D
+        L = len(P["qkv_w"])
+        m = wf_dit_model()
+        m.model_dim, m.ffn_dim, m.channels, m.freq_dim = dim, ffn, channels, freq
+        m.shift, m.context_noise = shift, context_noise
+        for i, t in enumerate(timesteps):
+            m.timesteps[i] = t
+        for n in ("patch_w", "patch_b", "t1_w", "t1_b", "t2_w", "t2_b", "tp_w", "tp_b", "head_w",
+                  "head_b", "head_mod"):
+            setattr(m, n, P[n].data_ptr())
+        self._layers = (wf_dit_layer * L)()
+        names = [("qkv_w", "qkv_w"), ("qkv_b", "qkv_b"), ("o_w", "o_w"), ("o_b", "o_b"),
+                 ("ffn1_w", "f1_w"), ("ffn1_b", "f1_b"), ("ffn2_w", "f2_w"), ("ffn2_b", "f2_b"),
+                 ("modulation", "mod")]
+        for l in range(L):
+            for cn, pn in names:
+                setattr(self._layers[l], cn, P[pn][l].data_ptr())
+        m.layers = self._layers
+        self.model = m
+        nbytes = ctypes.c_size_t()
+        check(lib.wf_dit_workspace_size(rnd.plan, dim, ffn, channels, freq, ctypes.byref(nbytes)),
+              "wf_dit_workspace_size")
+        self.workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        check(lib.wf_dit_bind(rnd.plan, ctypes.byref(m), _ptr(self.workspace),
+                              _stream_handle(stream)), "wf_dit_bind")
+
+    def round(self, z_new, eps, x0_out=None, chunk_out=None, stream=None):
+        check(lib.wf_dit_round(self.r.plan, _ptr(z_new), _ptr(eps), _ptr(x0_out), _ptr(chunk_out),
+                               _stream_handle(stream)), "wf_dit_round")

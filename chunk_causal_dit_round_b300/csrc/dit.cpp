@@ -1,0 +1,257 @@
+// Host side of the DiT path: the generic linear-layer entry point, the QKV
+// projection with its RoPE + paged-publication epilogue, and one whole
+// wavefront round of the chunk-wise causal DiT forward ("Wave Forcing",
+// Sec. 2 Eq. 1; Sec. 3.1 Eq. 3-5; Sec. 4.1 Eq. 8-9 dependency order; App. A
+// schedules; App. B.3 store pass).
+//
+// On one GPU and one stream the per-layer dependencies of Eq. 8-9 hold by
+// construction: every task's projection P_{s,l} (one batched GEMM over all
+// active tasks) completes before the round's attention C_{s,l} for that
+// layer, and C_{s,l} before P_{s,l+1}.
+
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "wf_plan_impl.h"
+
+namespace {
+
+bool aligned16(const void *q) { return ((uintptr_t)q & 15) == 0; }
+
+double warp_sigma(double nu, double shift) {
+    double s = nu / 1000.0;
+    return shift * s / (1.0 + (shift - 1.0) * s);
+}
+
+GemmParams base_params(wf_plan_s *p, int row_begin, int row_end, int N, int K, const void *bias) {
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.row_begin = row_begin;
+    gp.row_end = row_end;
+    gp.N = N;
+    gp.K = K;
+    gp.bias = static_cast<const __nv_bfloat16 *>(bias);
+    gp.status = static_cast<uint32_t *>(p->scratch);
+    return gp;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wf_linear(wf_plan_t p, const void *a, long long a_rows, int lda, int row_begin, int row_end,
+              const void *w, const void *bias, int N, int K, int epilogue, void *out, int ldo,
+              const float *gate, int gate_ld, int rows_per_group, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (!a || !w || !out) return WF_EINVAL;
+    if (epilogue < WF_EPI_BF16 || epilogue > WF_EPI_GATED_RESIDUAL) return WF_EINVAL;
+    if (K < 64 || K % 64 || N < 32 || N % 32 || lda < K || lda % 8 || ldo < N || ldo % 8)
+        return WF_EINVAL;
+    if (row_begin < 0 || row_end <= row_begin || row_end > a_rows) return WF_ERANGE;
+    if (!aligned16(a) || !aligned16(w) || !aligned16(out) || (bias && !aligned16(bias)))
+        return WF_EINVAL;
+    if (epilogue == WF_EPI_GATED_RESIDUAL &&
+        (!gate || !aligned16(gate) || gate_ld % 4 || gate_ld < N || rows_per_group < 1))
+        return WF_EINVAL;
+    GemmParams gp = base_params(p, row_begin, row_end, N, K, bias);
+    gp.out = out;
+    gp.ldo = ldo;
+    gp.gate = gate;
+    gp.gate_ld = gate_ld;
+    gp.rows_per_group = rows_per_group > 0 ? rows_per_group : 1;
+    return wf_launch_gemm(epilogue, a, a_rows, lda, w, gp, p->num_sms, stream) == cudaSuccess
+               ? WF_OK
+               : WF_ECUDA;
+}
+
+int wf_qkv_proj_rope_publish(wf_plan_t p, int layer, const void *x, const void *w_qkv,
+                             const void *b_qkv, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (p->k < 0) return WF_ENOROUND;
+    if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
+    if (!x || !w_qkv || !aligned16(x) || !aligned16(w_qkv) || (b_qkv && !aligned16(b_qkv)))
+        return WF_EINVAL;
+    if (p->o.dtype != WF_BF16) return WF_EUNSUPPORTED;
+    const int dim = p->H * p->D;
+    if (dim % 64 || p->D % 32) return WF_EUNSUPPORTED;
+    return wf_publish_impl(p, layer, x, w_qkv, b_qkv, nullptr, stream);
+}
+
+int wf_dit_workspace_size(wf_plan_t p, int model_dim, int ffn_dim, int channels, int freq_dim,
+                          size_t *bytes) {
+    if (!p || !bytes) return WF_EINVAL;
+    if (model_dim != p->H * p->D || ffn_dim < 64 || ffn_dim % 64 || channels < 1 ||
+        (4 * channels) % 64 || freq_dim < 2 || freq_dim % 2)
+        return WF_EINVAL;
+    const size_t latent = (size_t)channels * p->g.gt * 4 * p->g.gh * p->g.gw;
+    *bytes = wf_dit_workspace_bytes(p->S, p->NC, model_dim, ffn_dim, channels, freq_dim,
+                                    p->o.layers, latent);
+    return WF_OK;
+}
+
+int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_t stream) {
+    if (!p || !m || !workspace) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (p->o.dtype != WF_BF16 || p->D != 128) return WF_EUNSUPPORTED;
+    if ((uintptr_t)workspace & 255) return WF_EINVAL;
+    size_t need;
+    int rc = wf_dit_workspace_size(p, m->model_dim, m->ffn_dim, m->channels, m->freq_dim, &need);
+    if (rc != WF_OK) return rc;
+    if (!(m->shift > 0.0) || !std::isfinite(m->shift) || !(m->context_noise >= 0.0) ||
+        !(m->context_noise <= 1000.0))
+        return WF_EINVAL;
+    for (int s = 0; s < p->S; ++s)
+        if (!(m->timesteps[s] > 0.0 && m->timesteps[s] <= 1000.0) ||
+            (s > 0 && !(m->timesteps[s] < m->timesteps[s - 1])))
+            return WF_EINVAL;
+    const void *ptrs[] = {m->patch_w, m->t1_w, m->t1_b, m->t2_w, m->t2_b, m->tp_w, m->tp_b,
+                          m->head_w, m->head_mod, m->layers};
+    for (const void *q : ptrs)
+        if (!q) return WF_EINVAL;
+    const int L = p->o.layers;
+    for (int l = 0; l < L; ++l) {
+        const wf_dit_layer &w = m->layers[l];
+        if (!w.qkv_w || !w.o_w || !w.ffn1_w || !w.ffn2_w || !w.modulation) return WF_EINVAL;
+        const void *all[] = {w.qkv_w, w.qkv_b, w.o_w, w.o_b, w.ffn1_w, w.ffn1_b, w.ffn2_w, w.ffn2_b};
+        for (const void *q : all)
+            if (q && !aligned16(q)) return WF_EINVAL;
+    }
+    WfDit &d = p->dit;
+    delete[] d.layers;
+    d.layers = nullptr;
+    p->dit_bound = false;
+    d.dim = m->model_dim;
+    d.ffn = m->ffn_dim;
+    d.C = m->channels;
+    d.freq = m->freq_dim;
+    d.L = L;
+    d.shift = m->shift;
+    d.context_noise = m->context_noise;
+    for (int s = 0; s < p->S; ++s) d.nu[s] = m->timesteps[s];
+    d.nu[p->S] = 0.0;
+    auto B = [](const void *q) { return static_cast<const __nv_bfloat16 *>(q); };
+    d.patch_w = B(m->patch_w); d.patch_b = B(m->patch_b);
+    d.t1_w = B(m->t1_w); d.t1_b = B(m->t1_b);
+    d.t2_w = B(m->t2_w); d.t2_b = B(m->t2_b);
+    d.tp_w = B(m->tp_w); d.tp_b = B(m->tp_b);
+    d.head_w = B(m->head_w); d.head_b = B(m->head_b); d.head_mod = B(m->head_mod);
+    d.layers = new (std::nothrow) WfDitLayerDev[L];
+    if (!d.layers) return WF_ENOMEM;
+    for (int l = 0; l < L; ++l) {
+        const wf_dit_layer &w = m->layers[l];
+        d.layers[l] = {B(w.qkv_w), B(w.qkv_b), B(w.o_w), B(w.o_b), B(w.ffn1_w),
+                       B(w.ffn1_b), B(w.ffn2_w), B(w.ffn2_b), B(w.modulation)};
+    }
+    const size_t latent = (size_t)d.C * p->g.gt * 4 * p->g.gh * p->g.gw;
+    wf_dit_carve(&d, workspace, p->S, p->NC, latent);
+    // model timestep per slot: warped nu_s for stage s, warped context_noise for the store
+    float tm[WF_MAX_TASKS];
+    for (int s = 0; s < p->S; ++s) tm[s] = (float)(1000.0 * warp_sigma(d.nu[s], d.shift));
+    tm[p->S] = (float)(1000.0 * warp_sigma(d.context_noise, d.shift));
+    if (cudaMemcpy(d.tmodel, tm, sizeof(float) * (p->S + 1), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(d.layers_dev, d.layers, sizeof(WfDitLayerDev) * L, cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+        return WF_ECUDA;
+    if (cudaMemsetAsync(d.lat, 0, 2 * (size_t)(p->S + 1) * latent * 4, stream) != cudaSuccess)
+        return WF_ECUDA;
+    if (wf_launch_time_embedding(d, p->S, stream) != cudaSuccess) return WF_ECUDA;
+    p->dit_bound = true;
+    return WF_OK;
+}
+
+int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_out,
+                 float *chunk_out, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (!p->dit_bound) return WF_EUNBOUND;
+    if (p->k < 0) return WF_ENOROUND;
+    const int S = p->S, NC = p->NC, k = p->k;
+    const bool new_chunk = k < p->o.n_chunks;
+    if (new_chunk && (!z_new || ((uintptr_t)z_new & 7))) return WF_EINVAL;
+    if (S > 1 && (!eps || !aligned16(eps))) return WF_EINVAL;
+    if ((x0_out && !aligned16(x0_out)) || (chunk_out && ((uintptr_t)chunk_out & 3)))
+        return WF_EINVAL;
+    WfDit &d = p->dit;
+    int lo, hi;
+    wf_active_range(p, &lo, &hi);
+    const int r0 = lo * NC, r1 = (hi + 1) * NC;
+    const long long rows = (long long)(S + 1) * NC;
+    const size_t latent = d.latent;
+    float *lat_cur = d.lat + (size_t)(k & 1) * (S + 1) * latent;
+    float *lat_next = d.lat + (size_t)((k + 1) & 1) * (S + 1) * latent;
+    const int dim = d.dim, mod_ld = 6 * dim;
+
+    // patch embedding of every active task's input latent
+    const float *src[WF_MAX_TASKS];
+    src[0] = z_new;
+    for (int s = 1; s <= S; ++s) src[s] = lat_cur + (size_t)s * latent;
+    if (wf_launch_patchify(p->g, d.C, src, lo, hi, d.patches, stream) != cudaSuccess) return WF_ECUDA;
+    GemmParams gp = base_params(p, r0, r1, dim, 4 * d.C, d.patch_b);
+    gp.out = d.x;
+    gp.ldo = dim;
+    if (wf_launch_gemm(WF_EPI_F32, d.patches, rows, 4 * d.C, d.patch_w, gp, p->num_sms, stream) !=
+        cudaSuccess)
+        return WF_ECUDA;
+
+    for (int l = 0; l < d.L; ++l) {
+        const WfDitLayerDev &w = d.layers[l];
+        const float *mod = d.modtab + (size_t)l * (S + 1) * mod_ld;
+        // P_{s,l}: x' = LN(x)(1 + scale_a) + shift_a; QKV projection, RoPE, publish
+        if (wf_launch_ln_mod(d.x, d.xa, r0, r1, dim, NC, mod, mod_ld, 0, dim, stream) != cudaSuccess)
+            return WF_ECUDA;
+        int rc = wf_publish_impl(p, l, d.xa, w.qkv_w, w.qkv_b, nullptr, stream);
+        if (rc != WF_OK) return rc;
+        // C_{s,l}: round attention (output over x', which is dead), then the rest of the block
+        rc = wf_round_attention(p, l, d.xa, WF_ATTN_TC, stream);
+        if (rc != WF_OK) return rc;
+        gp = base_params(p, r0, r1, dim, dim, w.o_b);
+        gp.out = d.x;
+        gp.ldo = dim;
+        gp.gate = mod + 2 * dim;
+        gp.gate_ld = mod_ld;
+        gp.rows_per_group = NC;
+        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, d.xa, rows, dim, w.o_w, gp, p->num_sms, stream) !=
+            cudaSuccess)
+            return WF_ECUDA;
+        if (wf_launch_ln_mod(d.x, d.xa, r0, r1, dim, NC, mod, mod_ld, 3 * dim, 4 * dim, stream) !=
+            cudaSuccess)
+            return WF_ECUDA;
+        gp = base_params(p, r0, r1, d.ffn, dim, w.f1_b);
+        gp.out = d.hmid;
+        gp.ldo = d.ffn;
+        if (wf_launch_gemm(WF_EPI_GELU_BF16, d.xa, rows, dim, w.f1_w, gp, p->num_sms, stream) !=
+            cudaSuccess)
+            return WF_ECUDA;
+        gp = base_params(p, r0, r1, dim, d.ffn, w.f2_b);
+        gp.out = d.x;
+        gp.ldo = dim;
+        gp.gate = mod + 5 * dim;
+        gp.gate_ld = mod_ld;
+        gp.rows_per_group = NC;
+        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, d.hmid, rows, d.ffn, w.f2_w, gp, p->num_sms,
+                           stream) != cudaSuccess)
+            return WF_ECUDA;
+    }
+
+    // head and stage transition (Eq. 1) into next round's slot inputs
+    if (wf_launch_ln_mod(d.x, d.xa, r0, r1, dim, NC, d.headtab, 2 * dim, 0, dim, stream) !=
+        cudaSuccess)
+        return WF_ECUDA;
+    gp = base_params(p, r0, r1, 4 * d.C, dim, d.head_b);
+    gp.g = p->g;
+    gp.channels = d.C;
+    for (int s = 0; s <= S; ++s)
+        gp.sigma_next[s] = s < S ? (float)warp_sigma(d.nu[s + 1], d.shift) : 0.f;
+    gp.eps = eps;
+    gp.z_next = lat_next;
+    gp.x0_out = x0_out;
+    gp.chunk_out = chunk_out;
+    if (wf_launch_gemm(WF_EPI_HEAD, d.xa, rows, dim, d.head_w, gp, p->num_sms, stream) != cudaSuccess)
+        return WF_ECUDA;
+    return WF_OK;
+}
+
+}  // extern "C"

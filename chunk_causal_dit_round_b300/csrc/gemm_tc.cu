@@ -1,0 +1,472 @@
+// Linear layers of the DiT block on the 5th-generation tensor cores.
+//
+// out = epilogue(A W^T + b) for A [M, K] bf16 (row-major activations) and
+// W [N, K] bf16 (a linear layer's weight, output-major): the QKV projection
+// whose epilogue applies RoPE and publishes K/V into their page slots
+// ("Wave Forcing", Sec. 4.2: K/V are published right after QKV projection and
+// RoPE; App. B.2 Eq. 13 fixed-slot placement), and the "remaining block" of
+// Sec. 4.1 (output projection and FFN with gated residual adds, GELU), plus
+// the patch embedding and the head whose epilogue performs the stage
+// transition of Sec. 2 Eq. 1.
+//
+// Design (one persistent CTA per SM, 192 threads, no scratch memory):
+//  * tiles of 128 rows x BN columns, visited output-column-fastest so the
+//    CTAs of one wave share a few rows of A and the whole weight matrix stays
+//    in L2; CTA c takes tiles c, c + grid, c + 2 grid, ...;
+//  * warp 0 (one thread): TMA producer of 64-wide K slices of A and W
+//    (128-byte swizzle) into an NST-deep shared-memory ring;
+//  * warp 1 (one thread): tcgen05.mma issuer, M = 128, N = BN, fp32
+//    accumulators in TMEM, double-buffered (2 x BN columns) so the epilogue
+//    of tile i runs under the MMAs of tile i + 1;
+//  * warps 2-5: epilogue, one accumulator row per thread (tcgen05.ld of 32
+//    columns at a time), fused elementwise work, direct global stores.
+// Every wait is bounded (%globaltimer); on a timeout the kernel records it in
+// the plan's status word, drains its own copies and MMAs, frees TMEM and
+// returns.
+
+#include <cuda_bf16.h>
+
+#include "wf_internal.h"
+#include "wf_ptx.cuh"
+
+using namespace wfptx;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                       // one 128-byte swizzle atom of bf16
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t WAIT_NS = 1000000000ull;  // 1 s
+
+template <int BN>
+struct Cfg {
+    static constexpr int NST = BN >= 256 ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
+    static constexpr uint32_t SM_BAR = NST * STAGE;
+    // full[NST], empty[NST], tfull[2], tempty[2], drain
+    static constexpr int B_FULL = 0, B_EMPTY = NST, B_TFULL = 2 * NST, B_TEMPTY = 2 * NST + 2,
+                         B_DRAIN = 2 * NST + 4, NBARS = 2 * NST + 5;
+    static constexpr uint32_t SM_MISC = SM_BAR + ((NBARS * 8 + 63) / 64) * 64;
+    static constexpr uint32_t SM_ALLOC = SM_MISC + 64 + 1024;
+    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+};
+
+struct Roles {
+    uint32_t sbase;
+    volatile int *abort;
+    uint32_t *status, *where;
+    __device__ bool wait(uint32_t bar, uint32_t parity, uint32_t site) const {
+        return mbar_wait(bar, parity, abort, status, where, site, WAIT_NS);
+    }
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+    // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.f + tanhf(u));
+}
+
+// ---- epilogues -----------------------------------------------------------------
+// Each receives one thread's 32 consecutive accumulator columns of one row.
+
+template <int EPI>
+struct Epi;
+
+// out (bf16 or f32) = acc + bias;  GELU variant.
+template <>
+struct Epi<WF_EPI_BF16> {
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + (size_t)row * p.ldo + col;
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    }
+};
+template <>
+struct Epi<WF_EPI_GELU_BF16> {
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+        Epi<WF_EPI_BF16>::apply(p, row, col, v);
+    }
+};
+template <>
+struct Epi<WF_EPI_F32> {
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+        float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)row * p.ldo + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+};
+// out (f32) += gate[group(row)][col] * (acc + bias): the gated residual add of
+// the attention and FFN halves of a block; group = the row's task slot.
+template <>
+struct Epi<WF_EPI_GATED_RESIDUAL> {
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+        const int grp = row / p.rows_per_group;
+        const float4 *g4 = reinterpret_cast<const float4 *>(p.gate + (size_t)grp * p.gate_ld + col);
+        float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)row * p.ldo + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float4 g = __ldg(g4 + q);
+            float4 x = d4[q];
+            x.x = fmaf(g.x, v[4 * q], x.x);
+            x.y = fmaf(g.y, v[4 * q + 1], x.y);
+            x.z = fmaf(g.z, v[4 * q + 2], x.z);
+            x.w = fmaf(g.w, v[4 * q + 3], x.w);
+            d4[q] = x;
+        }
+    }
+};
+
+// QKV projection epilogue: columns [0, dim) are Q, [dim, 2 dim) K, [2 dim,
+// 3 dim) V, head h at columns h*D .. h*D + D - 1 of each part.  RoPE on Q and
+// K at the token's absolute (t, h, w); Q -> qbuf[slot][h][n][:], K/V ->
+// pool[dest page][layer][K|V][h][n][:]; the store of the anchor also keeps
+// its unrotated key on the raw-anchor page (App. B.3).
+template <>
+struct Epi<WF_EPI_QKV_PUBLISH> {
+    __device__ static void store32(__nv_bfloat16 *dst, const float (&v)[32]) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    }
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+        const WfGeom &g = p.g;
+        const int dim = g.H * g.D;
+        const int part = col / dim;                 // 0 Q, 1 K, 2 V
+        const int cc = col - part * dim;
+        const int h = cc / g.D;
+        const int d0 = cc - h * g.D;                // 32 consecutive channels d0 .. d0 + 31
+        const int slot = row / g.NC;
+        const int n = row - slot * g.NC;
+        const int ti = p.slot_task[slot];
+        const size_t plane = (size_t)g.NC * g.D;
+        if (part == 2) {
+            size_t kvp = (((size_t)p.rd.dest[ti] * g.L + p.layer) * 2 + 1) * g.H + h;
+            store32(p.pool + kvp * plane + (size_t)n * g.D + d0, v);
+            return;
+        }
+        if (part == 1 && ti == p.rd.raw_copy_task) {
+            size_t rawp = (((size_t)g.raw_anchor_page * g.L + p.layer) * 2) * g.H + h;
+            store32(p.pool + rawp * plane + (size_t)n * g.D + d0, v);
+        }
+        const int hw = g.gh * g.gw;
+        const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n - (n / g.gw) * g.gw;
+        const int t = g.gt * p.rd.chunk[ti] + f;
+        const float2 *tab = p.rope;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int m = d0 / 2 + i;
+            float2 cs;
+            if (m < g.dt2)
+                cs = __ldg(tab + g.rope_t_off + t * g.dt2 + m);
+            else if (m < g.dt2 + g.dh2)
+                cs = __ldg(tab + g.rope_h_off + hh * g.dh2 + (m - g.dt2));
+            else
+                cs = __ldg(tab + g.rope_w_off + ww * g.dw2 + (m - g.dt2 - g.dh2));
+            const float a = v[2 * i], b = v[2 * i + 1];
+            v[2 * i] = a * cs.x - b * cs.y;
+            v[2 * i + 1] = a * cs.y + b * cs.x;
+        }
+        if (part == 0) {
+            store32(p.qbuf + ((size_t)slot * g.H + h) * plane + (size_t)n * g.D + d0, v);
+        } else {
+            size_t kp = (((size_t)p.rd.dest[ti] * g.L + p.layer) * 2) * g.H + h;
+            store32(p.pool + kp * plane + (size_t)n * g.D + d0, v);
+        }
+    }
+};
+
+// Head epilogue: the 4C outputs of a token are ordered (row offset, column
+// offset, channel) of its 2 x 2 latent patch.  x0 = prediction; for a
+// denoising slot s the next stage's input is Psi(x0, eps) = (1 - sigma') x0 +
+// sigma' eps (Sec. 2 Eq. 1; sigma' = 0 gives x0 itself for the last stage);
+// the store slot's prediction is discarded.
+template <>
+struct Epi<WF_EPI_HEAD> {
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+        const WfGeom &g = p.g;
+        const int slot = row / g.NC;
+        const int n = row - slot * g.NC;
+        const int hw = g.gh * g.gw;
+        const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n - (n / g.gw) * g.gw;
+        const int C = p.channels;
+        const int Hl = 2 * g.gh, Wl = 2 * g.gw;
+        const size_t cstride = (size_t)g.gt * Hl * Wl;
+        const size_t lat = (size_t)C * cstride;
+        const float sg = p.sigma_next[slot];
+        float *x0 = p.x0_out ? p.x0_out + (size_t)slot * lat : nullptr;
+        float *zn = slot < g.S ? p.z_next + (size_t)(slot + 1) * lat : nullptr;
+        const float *eps = (slot < g.S && sg != 0.f) ? p.eps + (size_t)slot * lat : nullptr;
+        float *emit = (slot == g.S - 1) ? p.chunk_out : nullptr;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = col + i;              // feature index (q, r, c)
+            const int qr = j / C, c = j - qr * C;
+            const int q = qr >> 1, r = qr & 1;
+            const size_t at = (size_t)c * cstride + ((size_t)f * Hl + 2 * hh + q) * Wl + 2 * ww + r;
+            const float x = v[i];
+            if (x0) x0[at] = x;
+            if (zn) {
+                const float z = eps ? fmaf(sg, eps[at], (1.f - sg) * x) : x;
+                zn[at] = z;
+                if (emit) emit[at] = z;
+            }
+        }
+    }
+};
+
+// ---- kernel -----------------------------------------------------------------------
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                   const GemmParams p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    Roles r;
+    r.sbase = raw_u32 + pad;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SM_MISC);
+    r.abort = reinterpret_cast<volatile int *>(smem + C::SM_MISC + 16);
+    r.status = p.status;
+    r.where = p.status ? p.status + WF_SCRATCH_WHERE / 4 : nullptr;
+    auto bar = [&](int i) { return r.sbase + C::SM_BAR + 8u * i; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NST; ++i) {
+            mbar_init(bar(C::B_FULL + i), 1);
+            mbar_init(bar(C::B_EMPTY + i), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(C::B_TFULL + b), 1);
+            mbar_init(bar(C::B_TEMPTY + b), 4);     // one arrival per epilogue warp
+        }
+        mbar_init(bar(C::B_DRAIN), 1);
+        mbar_fence_init();
+        *r.abort = 0;
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&ta);
+        tma_prefetch_desc(&tb);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_tiles = p.tiles_m * p.tiles_n;
+    const int kb_n = p.K / BK;
+    uint32_t issued = 0;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer ----
+        uint32_t it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const int m0 = p.row_begin + (tile / p.tiles_n) * BM;
+            const int n0 = (tile % p.tiles_n) * BN;
+            for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                const int st = it % C::NST;
+                if (!r.wait(bar(C::B_EMPTY + st), ((it / C::NST) & 1) ^ 1, 1)) goto done;
+                const uint32_t sa = r.sbase + st * C::STAGE;
+                mbar_arrive_expect_tx(bar(C::B_FULL + st), C::STAGE);
+                tma_load_2d(sa, &ta, bar(C::B_FULL + st), kb * BK, m0);
+                tma_load_2d(sa + C::A_BYTES, &tb, bar(C::B_FULL + st), kb * BK, n0);
+                issued = it + 1;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+        uint32_t it = 0, tl = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+            const int buf = tl & 1;
+            if (!r.wait(bar(C::B_TEMPTY + buf), ((tl >> 1) & 1) ^ 1, 2)) goto done;
+            tc_fence_after();
+            const uint32_t d = tmem + buf * BN;
+            for (int kb = 0; kb < kb_n; ++kb, ++it) {
+                const int st = it % C::NST;
+                if (!r.wait(bar(C::B_FULL + st), (it / C::NST) & 1, 3)) goto done;
+                tc_fence_after();
+                const uint32_t sa = r.sbase + st * C::STAGE;
+                const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_ss(d, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
+                           idesc, (kb | kk) != 0 ? 1u : 0u);
+                mma_commit(bar(C::B_EMPTY + st));
+            }
+            mma_commit(bar(C::B_TFULL + buf));
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue ----
+        const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+        const int row_in = quarter * 32 + lane;
+        uint32_t tl = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+            const int buf = tl & 1;
+            bool ok = r.wait(bar(C::B_TFULL + buf), (tl >> 1) & 1, 4);
+            if (!__all_sync(0xffffffffu, ok)) goto done;
+            tc_fence_after();
+            const int row = p.row_begin + (tile / p.tiles_n) * BM + row_in;
+            const int n0 = (tile % p.tiles_n) * BN;
+            const bool live = row < p.row_end;
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t u[32];
+                tmem_ld32(taddr + c * 32, u);
+                tmem_wait_ld(u);
+                if (c == BN / 32 - 1) {
+                    // the whole accumulator buffer is in registers or consumed:
+                    // hand it back to the MMA issuer before the last stores
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + buf));
+                }
+                const int col = n0 + c * 32;
+                if (!live || col >= p.N) continue;
+                float v[32];
+                if (p.bias) {
+                    const uint4 *b4 = reinterpret_cast<const uint4 *>(p.bias + col);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 bb = __ldg(b4 + q);
+                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&bb);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float2 f = __bfloat1622float2(h2[e]);
+                            v[8 * q + 2 * e] = __uint_as_float(u[8 * q + 2 * e]) + f.x;
+                            v[8 * q + 2 * e + 1] = __uint_as_float(u[8 * q + 2 * e + 1]) + f.y;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
+                }
+                Epi<EPI>::apply(p, row, col, v);
+            }
+        }
+    }
+done:
+    if (*r.abort) {
+        if (warp == 0 && lane == 0) {
+            uint32_t first = issued > (uint32_t)C::NST ? issued - C::NST : 0;
+            for (uint32_t s = first; s < issued; ++s)
+                mbar_wait(bar(C::B_FULL + s % C::NST), (s / C::NST) & 1, nullptr, nullptr, nullptr, 0,
+                          WAIT_NS);
+        }
+        if (warp == 1 && lane == 0) {
+            mma_commit(bar(C::B_DRAIN));
+            mbar_wait(bar(C::B_DRAIN), 0, nullptr, nullptr, nullptr, 0, WAIT_NS);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int BN, int EPI>
+cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int num_sms,
+                   cudaStream_t stream) {
+    using C = Cfg<BN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SM_ALLOC);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int n_tiles = p.tiles_m * p.tiles_n;
+    const int grid = n_tiles < num_sms ? n_tiles : num_sms;
+    gemm_tc_kernel<BN, EPI><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                             const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                             const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                             CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encoder() {
+    static EncodeFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeFn>(f);
+    }
+    return fn;
+}
+
+// 2D bf16 map over a row-major [rows, cols] matrix with row pitch ld
+// elements, box (64 columns, box_rows rows), 128-byte swizzle.
+bool encode_2d(CUtensorMap *m, const void *base, long long rows, long long cols, long long ld,
+               int box_rows) {
+    EncodeFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int wf_gemm_bn_for(int epi) { return epi == WF_EPI_HEAD ? 64 : 256; }
+
+cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, const void *w,
+                           GemmParams p, int num_sms, cudaStream_t stream) {
+    const int bn = wf_gemm_bn_for(epi);
+    if (p.K % BK || p.N % 32 || lda % 8 || p.row_end <= p.row_begin) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, a, a_rows, p.K, lda, BM)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tb, w, p.N, p.K, p.K, bn)) return cudaErrorInvalidValue;
+    p.tiles_m = (p.row_end - p.row_begin + BM - 1) / BM;
+    p.tiles_n = (p.N + bn - 1) / bn;
+    switch (epi) {
+        case WF_EPI_BF16: return launch<256, WF_EPI_BF16>(ta, tb, p, num_sms, stream);
+        case WF_EPI_F32: return launch<256, WF_EPI_F32>(ta, tb, p, num_sms, stream);
+        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16>(ta, tb, p, num_sms, stream);
+        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL>(ta, tb, p, num_sms, stream);
+        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH>(ta, tb, p, num_sms, stream);
+        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD>(ta, tb, p, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}

@@ -6,6 +6,7 @@
 #include <cstddef>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/wf.h"
@@ -70,3 +71,74 @@ cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
 cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int layer,
                                       const WfTmaps &maps, void *out, int num_sms,
                                       cudaStream_t stream, int *wf_err);
+
+// ---- linear layers (gemm_tc.cu) -------------------------------------------
+// Internal epilogue of the QKV projection (RoPE + paged publication) and of
+// the head (unpatchify + stage transition); the public ones are WF_EPI_*.
+#define WF_EPI_QKV_PUBLISH 100
+#define WF_EPI_HEAD        101
+
+struct GemmParams {
+    int row_begin, row_end;      // rows of A / out processed (absolute)
+    int N, K;
+    int tiles_m, tiles_n;        // filled by the launcher
+    const __nv_bfloat16 *bias;   // [N] or null
+    void *out;                   // epilogue destination
+    int ldo;                     // its row pitch, elements
+    const float *gate;           // gated residual: gate[group][col]
+    int gate_ld, rows_per_group;
+    uint32_t *status;            // plan scratch control words (timeouts), or null
+    // QKV publication
+    WfGeom g;
+    WfRoundDev rd;
+    int layer;
+    int slot_task[WF_MAX_TASKS]; // slot -> task index of rd
+    __nv_bfloat16 *qbuf, *pool;
+    const float2 *rope;
+    // head + stage transition
+    int channels;
+    float sigma_next[WF_MAX_TASKS];  // per slot: warped sigma of the next stage (0: identity)
+    const float *eps;            // [S][latent] transition draws, or null
+    float *z_next;               // [S+1][latent] next round's slot inputs
+    float *x0_out;               // [S+1][latent] predictions, or null
+    float *chunk_out;            // [latent] emitted clean chunk, or null
+};
+
+int wf_gemm_bn_for(int epi);
+cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, const void *w,
+                           GemmParams p, int num_sms, cudaStream_t stream);
+
+// ---- DiT block pieces (dit_ops.cu) ------------------------------------------
+struct WfDitLayerDev {
+    const __nv_bfloat16 *qkv_w, *qkv_b, *o_w, *o_b, *f1_w, *f1_b, *f2_w, *f2_b, *mod;
+};
+
+struct WfDit {
+    int dim, ffn, C, freq, L;
+    double shift, context_noise, nu[WF_MAX_STAGES + 1];
+    const __nv_bfloat16 *patch_w, *patch_b, *t1_w, *t1_b, *t2_w, *t2_b, *tp_w, *tp_b, *head_w,
+        *head_b, *head_mod;
+    WfDitLayerDev *layers;       // host array (owned by the plan)
+    // workspace carve-up
+    float *x;                    // [(S+1) N_C][dim] residual stream
+    __nv_bfloat16 *xa;           // [(S+1) N_C][dim] normalised input / attention output
+    __nv_bfloat16 *hmid;         // [(S+1) N_C][ffn]
+    __nv_bfloat16 *patches;      // [(S+1) N_C][4 C]
+    float *lat;                  // [2][S+1][latent] slot inputs, double-buffered by round parity
+    float *modtab;               // [L][S+1][6][dim]
+    float *headtab;              // [S+1][2][dim]
+    float *temb;                 // [S+1][freq + 3 dim + 6 dim] time-embedding work area
+    WfDitLayerDev *layers_dev;   // device copy of the per-layer pointers
+    float *tmodel;               // [S+1] model timestep of each slot
+    size_t latent;               // floats of one latent chunk
+};
+
+size_t wf_dit_workspace_bytes(int S, int NC, int dim, int ffn, int C, int freq, int L, size_t latent);
+void wf_dit_carve(WfDit *d, void *ws, int S, int NC, size_t latent);
+
+cudaError_t wf_launch_ln_mod(const float *x, __nv_bfloat16 *out, int row_begin, int row_end,
+                             int dim, int NC, const float *mod, int mod_ld, int shift_off,
+                             int scale_off, cudaStream_t stream);
+cudaError_t wf_launch_patchify(const WfGeom &g, int C, const float *const *src, int lo, int hi,
+                               __nv_bfloat16 *patches, cudaStream_t stream);
+cudaError_t wf_launch_time_embedding(const WfDit &d, int S, cudaStream_t stream);

@@ -19,47 +19,9 @@
 
 #include "wf_internal.h"
 
-namespace {
+#include "wf_plan_impl.h"
 
-struct CtxEntry {
-    int kind, chunk, j, page, tpos;
-};
-
-struct HostTask {
-    int chunk, stage, dest;
-    int n_ctx;
-    CtxEntry ctx[WF_MAX_CTX];
-};
-
-}  // namespace
-
-struct wf_plan_s {
-    int S, NC, H, D, W;
-    wf_plan_opts o;
-    int R, P;                // ring pages, total pages
-    WfGeom g;
-
-    // round state
-    int k = -1;
-    bool have_prev_store = false;
-    int prev_store_chunk = -1, prev_store_page = -1;
-    bool anchor_stored = false;               // chunk 0 clean and on page 0
-    std::deque<std::pair<int, int>> history;  // (chunk, page), oldest first
-    std::deque<int> free_pages;
-    int n_tasks = 0;
-    HostTask tasks[WF_MAX_TASKS];
-    int anchor_tpos = -1;
-    WfRoundDev rd{};
-    std::vector<int> anchor_rot;              // per layer: tpos the anchor page holds, -1 none
-    std::vector<int> published;               // per layer: round whose publish ran
-
-    // binding
-    bool bound = false;
-    void *pool = nullptr, *qbuf = nullptr, *scratch = nullptr;
-    int device = 0, num_sms = 0;
-    bool tmaps_ok = false;
-    WfTmaps tmaps;
-};
+using namespace wfimpl;
 
 namespace {
 
@@ -152,6 +114,62 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
 }
 
 }  // namespace
+
+// Shared by wf_qkv_rope_publish (Q/K/V given) and the projection path
+// (x and W_qkv given): one launch publishes every active task; the anchor
+// key is re-rotated from its unrotated copy when the window moved.
+int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
+                    const void *qkv, cudaStream_t stream) {
+    WfRoundDev rd = p->rd;
+    int new_rot = p->anchor_rot[layer];
+    bool rerotate = false;
+    if (rd.raw_copy_task >= 0) {
+        new_rot = 0;  // the store of chunk 0 writes the anchor at its own position
+    } else if (p->anchor_tpos >= 0 && p->anchor_rot[layer] != p->anchor_tpos) {
+        rerotate = true;
+        new_rot = p->anchor_tpos;
+    }
+    if (x) {
+        int lo, hi;
+        wf_active_range(p, &lo, &hi);
+        GemmParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        gp.row_begin = lo * p->NC;
+        gp.row_end = (hi + 1) * p->NC;
+        gp.N = 3 * p->H * p->D;
+        gp.K = p->H * p->D;
+        gp.bias = static_cast<const __nv_bfloat16 *>(b_qkv);
+        gp.status = static_cast<uint32_t *>(p->scratch);
+        gp.g = p->g;
+        gp.rd = rd;
+        gp.layer = layer;
+        for (int i = 0; i < WF_MAX_TASKS; ++i) gp.slot_task[i] = -1;
+        for (int i = 0; i < rd.n_tasks; ++i) gp.slot_task[rd.slot[i]] = i;
+        gp.qbuf = static_cast<__nv_bfloat16 *>(p->qbuf);
+        gp.pool = static_cast<__nv_bfloat16 *>(p->pool);
+        gp.rope = reinterpret_cast<const float2 *>(static_cast<const char *>(p->scratch) +
+                                                   WF_SCRATCH_TABLES);
+        if (wf_launch_gemm(WF_EPI_QKV_PUBLISH, x, (long long)(p->S + 1) * p->NC, gp.K, w_qkv, gp,
+                           p->num_sms, stream) != cudaSuccess)
+            return WF_ECUDA;
+        if (rerotate) {
+            WfRoundDev rr = rd;
+            rr.n_tasks = 0;
+            rr.rerotate = 1;
+            if (wf_launch_publish(p->g, rr, layer, p->o.dtype, nullptr, p->qbuf, p->pool, p->scratch,
+                                  stream) != cudaSuccess)
+                return WF_ECUDA;
+        }
+    } else {
+        rd.rerotate = rerotate ? 1 : 0;
+        if (wf_launch_publish(p->g, rd, layer, p->o.dtype, qkv, p->qbuf, p->pool, p->scratch,
+                              stream) != cudaSuccess)
+            return WF_ECUDA;
+    }
+    p->anchor_rot[layer] = new_rot;
+    p->published[layer] = p->k;
+    return WF_OK;
+}
 
 extern "C" {
 
@@ -374,20 +392,7 @@ int wf_qkv_rope_publish(wf_plan_t p, int layer, const void *qkv, cudaStream_t st
     if (p->k < 0) return WF_ENOROUND;
     if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
     if (!qkv || ((uintptr_t)qkv & 15)) return WF_EINVAL;
-    WfRoundDev rd = p->rd;
-    int new_rot = p->anchor_rot[layer];
-    if (rd.raw_copy_task >= 0) {
-        new_rot = 0;  // the store of chunk 0 writes the anchor at its own position
-    } else if (p->anchor_tpos >= 0 && p->anchor_rot[layer] != p->anchor_tpos) {
-        rd.rerotate = 1;
-        new_rot = p->anchor_tpos;
-    }
-    if (wf_launch_publish(p->g, rd, layer, p->o.dtype, qkv, p->qbuf, p->pool, p->scratch,
-                          stream) != cudaSuccess)
-        return WF_ECUDA;
-    p->anchor_rot[layer] = new_rot;
-    p->published[layer] = p->k;
-    return WF_OK;
+    return wf_publish_impl(p, layer, nullptr, nullptr, nullptr, qkv, stream);
 }
 
 int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream_t stream) {

@@ -1,0 +1,70 @@
+// The plan object behind the opaque wf_plan_t handle (host state of one
+// request), shared by the host files of the library.  Not part of the C ABI.
+#pragma once
+
+#include <deque>
+#include <utility>
+#include <vector>
+
+#include "wf_internal.h"
+
+namespace wfimpl {
+
+struct CtxEntry {
+    int kind, chunk, j, page, tpos;
+};
+
+struct HostTask {
+    int chunk, stage, dest;
+    int n_ctx;
+    CtxEntry ctx[WF_MAX_CTX];
+};
+
+}  // namespace wfimpl
+
+struct wf_plan_s {
+    int S, NC, H, D, W;
+    wf_plan_opts o;
+    int R, P;                // ring pages, total pages
+    WfGeom g;
+
+    // round state
+    int k = -1;
+    bool have_prev_store = false;
+    int prev_store_chunk = -1, prev_store_page = -1;
+    bool anchor_stored = false;               // chunk 0 clean and on page 0
+    std::deque<std::pair<int, int>> history;  // (chunk, page), oldest first
+    std::deque<int> free_pages;
+    int n_tasks = 0;
+    wfimpl::HostTask tasks[WF_MAX_TASKS];
+    int anchor_tpos = -1;
+    WfRoundDev rd{};
+    std::vector<int> anchor_rot;              // per layer: tpos the anchor page holds, -1 none
+    std::vector<int> published;               // per layer: round whose publish ran
+
+    // binding
+    bool bound = false;
+    void *pool = nullptr, *qbuf = nullptr, *scratch = nullptr;
+    int device = 0, num_sms = 0;
+    bool tmaps_ok = false;
+    WfTmaps tmaps;
+
+    // DiT model (wf_dit_bind)
+    bool dit_bound = false;
+    WfDit dit{};
+    ~wf_plan_s() { delete[] dit.layers; }
+};
+
+// Active slots of the current round form the contiguous range [lo, hi]
+// (stage s is active iff k - N_chunk < s <= k, the store likewise with s = S).
+inline void wf_active_range(const wf_plan_s *p, int *lo, int *hi) {
+    *lo = p->k - p->o.n_chunks + 1 > 0 ? p->k - p->o.n_chunks + 1 : 0;
+    *hi = p->k < p->S ? p->k : p->S;
+}
+
+// Launch the QKV publication for `layer` of the current round: either the
+// projection GEMM (x != nullptr) or the given Q/K/V; the anchor re-rotation
+// when the window moved.  Returns a WF_* code.
+int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
+                    const void *qkv, cudaStream_t stream);
+

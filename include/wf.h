@@ -77,6 +77,11 @@ typedef struct CUstream_st *cudaStream_t; /* identical to CUDA's own typedef */
 #define WF_ATTN_TC   1    /* tcgen05/TMEM/TMA kernel (bf16, head_dim 128) */
 #define WF_ATTN_SIMT 2    /* CUDA-core kernel (fp32 or bf16, head_dim 32..128, %32) */
 
+#define WF_EPI_BF16           0 /* out bf16 = acc + bias */
+#define WF_EPI_F32            1 /* out f32  = acc + bias */
+#define WF_EPI_GELU_BF16      2 /* out bf16 = GELU_tanh(acc + bias) */
+#define WF_EPI_GATED_RESIDUAL 3 /* out f32 += gate[row / rows_per_group][col] * (acc + bias) */
+
 typedef struct wf_plan_s *wf_plan_t; /* opaque, library-owned host state */
 
 typedef struct wf_plan_opts {
@@ -204,6 +209,117 @@ int wf_round_attention(wf_plan_t plan, int layer, void *out, int kernel, cudaStr
  * and WF_ECUDA (symbol lookup, memset or launch failed). */
 #define WF_NOALLOC_SCRATCH_BYTES 256
 int wf_round_attention_noalloc(wf_plan_t plan, int layer, void *out, cudaStream_t stream);
+
+/* ---- linear layers on the tensor cores -------------------------------------
+ * out = epilogue(A W^T + bias) for rows row_begin .. row_end-1 of A.
+ *   a     bf16 [a_rows][lda] row-major activations (device)
+ *   w     bf16 [N][K] row-major weight of a linear layer, output-major (device)
+ *   bias  bf16 [N] or NULL
+ *   out   WF_EPI_BF16 / WF_EPI_GELU_BF16: bf16 [.][ldo]; WF_EPI_F32 and
+ *         WF_EPI_GATED_RESIDUAL: float [.][ldo] (read-modify-write for the
+ *         latter); row r of out corresponds to row r of a
+ *   gate  WF_EPI_GATED_RESIDUAL only: float rows of gate_ld values, row
+ *         r / rows_per_group gates output row r (one gate vector per task slot
+ *         when rows_per_group = N_C)
+ * These are the dense operators of one DiT block ("Wave Forcing" Sec. 4.1:
+ * attention and "the remaining block" of the standard Wan2.1 transformer,
+ * App. D.2): output projection and FFN with gated residual adds, GELU FFN
+ * hidden layer, patch embedding.  Uses the plan's scratch status word for
+ * bounded-wait timeouts (wf_sync_status) and nothing else of the plan.
+ * Requirements: K % 64 == 0, N % 32 == 0, lda % 8 == 0, ldo % 8 == 0, every
+ * pointer 16-byte aligned.  Errors: WF_EINVAL, WF_ERANGE (row range),
+ * WF_EUNBOUND, WF_ECUDA. */
+int wf_linear(wf_plan_t plan, const void *a, long long a_rows, int lda, int row_begin, int row_end,
+              const void *w, const void *bias, int N, int K, int epilogue, void *out, int ldo,
+              const float *gate, int gate_ld, int rows_per_group, cudaStream_t stream);
+
+/* QKV projection of one layer fused with RoPE and paged publication (Sec.
+ * 4.2: "publishes K/V after QKV projection and RoPE"; App. B.2 Eq. 13 direct
+ * placement into fixed slots).  Same effect as wf_qkv_rope_publish applied
+ * to qkv = x W_qkv^T + b_qkv, without materialising qkv:
+ *   x      bf16 [S+1][N_C][dim] (dim = heads*head_dim), slot-indexed like
+ *          qkv; only the active slots' rows are read
+ *   w_qkv  bf16 [3 dim][dim]: rows 0..dim-1 produce Q, then K, then V; head h
+ *          of each part is rows h*head_dim .. h*head_dim + head_dim - 1
+ *   b_qkv  bf16 [3 dim] or NULL
+ * bf16 plans only, dim % 64 == 0, head_dim % 32 == 0.  Errors: as
+ * wf_qkv_rope_publish, plus WF_EUNSUPPORTED. */
+int wf_qkv_proj_rope_publish(wf_plan_t plan, int layer, const void *x, const void *w_qkv,
+                             const void *b_qkv, cudaStream_t stream);
+
+/* ---- the chunk-wise causal DiT round --------------------------------------
+ * Weights of one transformer block (device pointers, bf16, linear weights
+ * [out][in]; biases may be NULL). */
+typedef struct wf_dit_layer {
+    const void *qkv_w, *qkv_b;     /* [3 dim][dim], [3 dim] */
+    const void *o_w, *o_b;         /* [dim][dim], [dim] */
+    const void *ffn1_w, *ffn1_b;   /* [ffn][dim], [ffn] */
+    const void *ffn2_w, *ffn2_b;   /* [dim][ffn], [dim] */
+    const void *modulation;        /* [6][dim]: shift, scale, gate of attention, then of FFN */
+} wf_dit_layer;
+
+/* A Wan2.1-style DiT without text cross-attention (the pages omit text
+ * conditioning, Sec. 2).  The block, as this library computes it:
+ *   (shift_a, scale_a, gate_a, shift_f, scale_f, gate_f) = modulation + e0(t)
+ *   x' = LN(x)(1 + scale_a) + shift_a   (LayerNorm eps 1e-6, no affine)
+ *   Q,K,V = x' W_qkv^T + b; RoPE on Q, K; x += gate_a (Attn W_o^T + b_o)
+ *   x += gate_f (GELU_tanh((LN(x)(1 + scale_f) + shift_f) W_1^T + b_1) W_2^T + b_2)
+ * with the timestep embedding e(t) = W_t2 SiLU(W_t1 sinusoid(t) + b) + b,
+ * e0 = W_tp SiLU(e) + b_tp; patch embedding of (1,2,2) patches of C
+ * channels (features ordered channel, row offset, column offset); head
+ * (shift, scale) = head_mod + e, y = (LN(x)(1 + scale) + shift) W_h^T + b_h,
+ * 4C outputs per token ordered (row offset, column offset, channel). */
+typedef struct wf_dit_model {
+    int model_dim;                 /* = heads * head_dim of the plan */
+    int ffn_dim;                   /* % 64 == 0 */
+    int channels;                  /* latent channels C, 4C % 64 == 0 (16 for Wan2.1) */
+    int freq_dim;                  /* sinusoidal timestep features (256 for Wan2.1) */
+    double shift;                  /* timestep warp: sigma' = shift s / (1 + (shift-1) s), s = nu/1000 */
+    double context_noise;          /* nu of the store pass (App. B.3), in [0, 1000] */
+    double timesteps[WF_MAX_STAGES];  /* nu_0 > ... > nu_{S-1} in (0, 1000] (App. A) */
+    const void *patch_w, *patch_b; /* [dim][4C], [dim] */
+    const void *t1_w, *t1_b;       /* [dim][freq], [dim] */
+    const void *t2_w, *t2_b;       /* [dim][dim], [dim] */
+    const void *tp_w, *tp_b;       /* [6 dim][dim], [6 dim] */
+    const void *head_w, *head_b;   /* [4C][dim], [4C] */
+    const void *head_mod;          /* [2][dim]: shift, scale */
+    const wf_dit_layer *layers;    /* host array of `layers` (plan option) entries */
+} wf_dit_model;
+
+/* Bytes of the DiT workspace (residual stream, normalised activations, FFN
+ * hidden layer, patches, double-buffered latent slot inputs, modulation
+ * tables).  No CUDA call.  Errors: WF_EINVAL (dims). */
+int wf_dit_workspace_size(wf_plan_t plan, int model_dim, int ffn_dim, int channels, int freq_dim,
+                          size_t *bytes);
+
+/* Attach a model and a caller-owned workspace (256-byte aligned, size from
+ * wf_dit_workspace_size) to a bound bf16 plan with head_dim 128.  The weight
+ * pointers are kept (not copied): they must stay valid while the plan is
+ * used.  Computes the timestep embeddings and modulation tables of every
+ * slot on `stream` (each stage has a fixed timestep) and clears the latent
+ * slot buffers.  Errors: WF_EINVAL, WF_EUNBOUND, WF_EUNSUPPORTED, WF_ENOMEM,
+ * WF_ECUDA. */
+int wf_dit_bind(wf_plan_t plan, const wf_dit_model *model, void *workspace, cudaStream_t stream);
+
+/* The DiT forward of the current round (enter it with wf_round_step) for
+ * every active task, and the stage transition of Sec. 2 Eq. 1:
+ *   Z^(s+1) = Psi_{nu_{s+1}}(G(Z^(s), nu_s | C), eps),  Psi_nu(x, e) = (1 - sigma') x + sigma' e,
+ * Psi_0 = identity.  Slot 0 reads z_new (the fresh noise Z^(0) of chunk k);
+ * slot s in 1..S-1 reads the latent its chunk left in the previous round;
+ * the store slot reads the clean chunk finished in the previous round.
+ *   z_new      float [C][grid_t][2 grid_h][2 grid_w] (device), required while
+ *              chunk k < N_chunk
+ *   eps        float [S][latent]: eps[s] re-noises slot s's prediction (eps[S-1]
+ *              is not read); may be NULL when S == 1
+ *   x0_out     float [S+1][latent] predictions of the active slots, or NULL
+ *   chunk_out  float [latent]: the clean chunk B_{k-S+1} finished this round
+ *              (written when stage S-1 is active), or NULL
+ * All L layers run: per layer one batched QKV projection with RoPE and
+ * paged publication, one round-attention launch, the output projection,
+ * and the FFN; then the head.  Asynchronous on `stream`.  Errors:
+ * WF_EUNBOUND (no wf_bind / wf_dit_bind), WF_ENOROUND, WF_EINVAL, WF_ECUDA. */
+int wf_dit_round(wf_plan_t plan, const float *z_new, const float *eps, float *x0_out,
+                 float *chunk_out, cudaStream_t stream);
 
 /* Read and clear the device status word in scratch (synchronises stream).
  * Returns WF_OK, WF_ETIMEOUT if a kernel's bounded wait gave up, or WF_ECUDA. */

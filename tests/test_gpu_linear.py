@@ -1,0 +1,99 @@
+"""GPU parity of the tensor-core linear layers (wf_linear) against fp64 on
+the same bf16 operands: plain bf16 / f32 outputs, the GELU hidden layer and
+the gated residual add of the DiT block ("Wave Forcing" Sec. 4.1, the
+remaining block of a Wan2.1 transformer layer)."""
+
+import numpy as np
+import pytest
+import torch
+
+import chunk_causal_dit_round_b300 as wf
+import wf_synth
+from oracle import dit
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def plan():
+    r = wf.Round(1, 48, 1, 128, -1, n_chunks=1, grid=(3, 4, 4), dtype=wf.WF_BF16)
+    yield r
+    r.close()
+
+
+def operands(seed, M, N, K, rows_extra=0):
+    a = wf_synth.normal(wf_synth.key_of(seed, 1), (M + rows_extra, K), 1.0, torch.bfloat16)
+    w = wf_synth.normal(wf_synth.key_of(seed, 2), (N, K), 0.05, torch.bfloat16)
+    b = wf_synth.normal(wf_synth.key_of(seed, 3), (N,), 0.5, torch.bfloat16)
+    return a, w, b
+
+
+def ref_linear(a, w, b, r0, r1):
+    return a[r0:r1].double().numpy() @ w.double().numpy().T + b.double().numpy()
+
+
+def tol_f32(K):
+    # fp32 accumulation of K products of O(1) terms: far below bf16 resolution
+    return 1e-4 * np.sqrt(K)
+
+
+# M spans several 128-row tiles with a ragged tail; N several 256-column tiles
+# plus a ragged 32-column remainder; K one and several 64-wide slices.
+SHAPES = [(300, 544, 64), (517, 256, 1536), (129, 800, 320), (1, 32, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_f32_epilogue(plan, M, N, K):
+    a, w, b = operands(1, M, N, K)
+    out = torch.full((M, N), float("nan"), device="cuda")
+    plan.linear(a.cuda(), w.cuda(), b.cuda(), out, wf.WF_EPI_F32)
+    torch.cuda.synchronize()
+    ref = ref_linear(a, w, b, 0, M)
+    err = np.abs(out.cpu().double().numpy() - ref).max()
+    assert err <= tol_f32(K), err
+    assert plan.sync_status() == wf.WF_OK
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_bf16_and_gelu_epilogues(plan, M, N, K):
+    a, w, b = operands(2, M, N, K)
+    ref = ref_linear(a, w, b, 0, M)
+    for epi, fn in ((wf.WF_EPI_BF16, lambda x: x), (wf.WF_EPI_GELU_BF16, dit.gelu_tanh)):
+        out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+        plan.linear(a.cuda(), w.cuda(), b.cuda(), out, epi)
+        torch.cuda.synchronize()
+        got = out.cpu().double().numpy()
+        want = fn(ref)
+        # one bf16 rounding of the result: half an ulp, 2^-9 relative, plus fp32 noise
+        err = np.abs(got - want) / np.maximum(np.abs(want), 1e-2)
+        assert err.max() <= 2 ** -8, (epi, err.max())
+
+
+def test_row_range_and_gated_residual(plan):
+    """Rows outside [row_begin, row_end) are untouched; row r is gated by
+    gate[r // rows_per_group]."""
+    M, N, K, G = 3 * 100, 512, 256, 100
+    a, w, b = operands(3, M, N, K)
+    gate = wf_synth.normal(wf_synth.key_of(3, 9), (3, N), 1.0, torch.float32)
+    x0 = wf_synth.normal(wf_synth.key_of(3, 10), (M, N), 1.0, torch.float32)
+    out = x0.clone().cuda()
+    plan.linear(a.cuda(), w.cuda(), b.cuda(), out, wf.WF_EPI_GATED_RESIDUAL, row_begin=100,
+                row_end=300, gate=gate.cuda(), rows_per_group=G)
+    torch.cuda.synchronize()
+    got = out.cpu().double().numpy()
+    ref = x0.double().numpy().copy()
+    y = ref_linear(a, w, b, 100, 300)
+    g = gate.double().numpy()
+    ref[100:300] += g[np.arange(100, 300) // G] * y
+    assert np.array_equal(got[:100], x0.double().numpy()[:100])
+    assert np.abs(got - ref).max() <= 3 * tol_f32(K)
+
+
+def test_no_bias(plan):
+    M, N, K = 200, 256, 128
+    a, w, _ = operands(4, M, N, K)
+    out = torch.zeros((M, N), device="cuda")
+    plan.linear(a.cuda(), w.cuda(), None, out, wf.WF_EPI_F32)
+    torch.cuda.synchronize()
+    ref = a.double().numpy() @ w.double().numpy().T
+    assert np.abs(out.cpu().double().numpy() - ref).max() <= tol_f32(K)

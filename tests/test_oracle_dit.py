@@ -240,3 +240,44 @@ def test_history_is_read_not_recomputed():
         same = np.allclose(u, v, atol=1e-12)
         # only the stage-0 task (the perturbed chunk itself) may differ
         assert same == (t.stage != 0), (t.stage, same)
+
+
+def test_sharp_model_tolerance_separates_rounding_from_a_mask_mistake():
+    """The GPU parity bars of the sharp DiT test (weights ~ N(0, 0.05)) must
+    admit the spread that bf16 rounding alone causes and reject a planted
+    mistake: queries that also see noisier live chunks (the reverse edges
+    the WF mask removes, Sec. 3.1)."""
+    from gpu_helpers import scaled_errors
+    import oracle.dit as od
+
+    cfg = sch.Cfg(S=2, n_chunks=6, history=1)
+    dims = dit.Dims(dim=256, heads=2, head_dim=128, ffn=512, layers=2, channels=16, freq=256)
+    grid = (3, 8, 10)
+    params = wf_synth.dit_params(12, dims.dim, dims.ffn, dims.layers, dims.channels, dims.freq,
+                                 std=0.05)
+
+    def run(b16):
+        m = dit.Model(cfg, grid, dims, dit.weights_from(params), [1000.0, 500.0], bf16_points=b16)
+        outs = []
+        for k in range(sch.n_rounds(cfg)):
+            z = lat(12, k, -1, dims, grid)
+            outs += m.round(k, z, [lat(12, k - s, s, dims, grid) for s in range(2)])[0]
+        return outs
+
+    def worst(a, b):
+        w = [0.0, 0.0, 0.0]
+        for u, v in zip(a, b):
+            w = [max(p, q) for p, q in zip(w, scaled_errors(u, v))]
+        return w
+
+    ref = run(True)
+    noise = worst(ref, run(False))
+    orig = od.masked_attention
+    try:
+        od.masked_attention = lambda q, k, v, mask: orig(q, k, v, np.ones_like(mask))
+        bad = worst(ref, run(True))
+    finally:
+        od.masked_attention = orig
+    bars = (5e-2, 4e-3, 1e-2)          # SHARP_MAX, SHARP_MEAN, SHARP_REL of tests/test_gpu_dit.py
+    assert all(n <= b / 1.5 for n, b in zip(noise, bars)), noise
+    assert all(e >= 3 * b for e, b in zip(bad, bars)), bad
