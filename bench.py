@@ -37,7 +37,7 @@ UNIT = "TFLOP/s"
 # DRAM bytes (read + write) of one steady attn_tc_kernel launch, from the ncu
 # capture summarised in profiles/attn_tc_kernel_wan13_round.md.  Set to None
 # whenever the kernel changes, until it is captured again.
-ATTN_TC_TRAFFIC_BYTES = None
+ATTN_TC_TRAFFIC_BYTES = 1.259e9
 
 CONFIGS = {
     # name: (S, grid (t,h,w), heads, head_dim, history W)
@@ -81,7 +81,8 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     cfg = DIT_CONFIGS[name]
     steps = args.steps if steps is None else steps
     warmup = args.warmup if warmup is None else warmup
-    S, W, L = cfg["S"], cfg["history"], cfg["layers"]
+    S, W = cfg["S"], cfg["history"]
+    L = getattr(args, "layers", None) or cfg["layers"]
     NC = math.prod(cfg["grid"])
     H, D, dim, ffn = cfg["heads"], cfg["head_dim"], cfg["dim"], cfg["ffn"]
     C = 16
@@ -152,7 +153,8 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     chunks_s = world * steps / (ms * 1e-3)
     peak, src = _sustained_peak()
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
-    res = {"workload": name, "desc": cfg["desc"], "value": round(chunks_s, 3), "unit": "chunks/s",
+    res = {"workload": name, "desc": cfg["desc"], "layers": L, "value": round(chunks_s, 3),
+           "unit": "chunks/s",
            "frames_per_s": round(12 * chunks_s, 2), "round_ms_p50": round(statistics.median(per), 3),
            "rounds": steps, "eta_slot": round(cfg["n_chunks"] / (cfg["n_chunks"] + S), 4),
            "flops_per_round": flops / steps,
@@ -466,6 +468,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="wan13_attn", choices=sorted(CONFIGS) + sorted(DIT_CONFIGS))
     ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="DiT configs: override the block count (smaller profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
