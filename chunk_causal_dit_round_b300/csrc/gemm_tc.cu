@@ -9,7 +9,7 @@
 // the patch embedding and the head whose epilogue performs the stage
 // transition of Sec. 2 Eq. 1.
 //
-// Design (one persistent CTA per SM, 192 threads, no scratch memory):
+// Design (one persistent CTA per SM, 320 threads, no scratch memory):
 //  * tiles of 128 rows x BN columns, visited output-column-fastest so the
 //    CTAs of one wave share a few rows of A and the whole weight matrix stays
 //    in L2; CTA c takes tiles c, c + grid, c + 2 grid, ...;
@@ -18,8 +18,10 @@
 //  * warp 1 (one thread): tcgen05.mma issuer, M = 128, N = BN, fp32
 //    accumulators in TMEM, double-buffered (2 x BN columns) so the epilogue
 //    of tile i runs under the MMAs of tile i + 1;
-//  * warps 2-5: epilogue, one accumulator row per thread (tcgen05.ld of 32
-//    columns at a time), fused elementwise work, direct global stores.
+//  * warps 2-9: epilogue, two warps per TMEM lane quarter (each takes half of
+//    the tile's columns), one accumulator row per thread, tcgen05.ld of 32
+//    columns at a time with the next chunk's load in flight while the
+//    current one is processed; fused elementwise work, direct global stores.
 // Every wait is bounded (%globaltimer); on a timeout the kernel records it in
 // the plan's status word, drains its own copies and MMAs, frees TMEM and
 // returns.
@@ -35,7 +37,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;                       // one 128-byte swizzle atom of bf16
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;           // producer, MMA issuer, 8 epilogue warps
+constexpr int EPI_WARPS = 8;
 constexpr uint64_t WAIT_NS = 1000000000ull;  // 1 s
 
 template <int BN>
@@ -77,9 +80,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __device__ __forceinline__ float gelu_tanh(float x) {
-    // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
-    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.f + tanhf(u));
+    // 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated as
+    // x / (1 + e^(-2u)) since 0.5 (1 + tanh u) = 1 / (1 + e^(-2u)); the
+    // exponent is capped so the divisor stays finite (GELU(x) ~ 0 there).
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    return __fdividef(x, 1.f + __expf(fminf(-2.f * u, 80.f)));
 }
 
 // ---- epilogues -----------------------------------------------------------------
@@ -124,10 +129,18 @@ struct Epi<WF_EPI_GATED_RESIDUAL> {
         const int grp = row / p.rows_per_group;
         const float4 *g4 = reinterpret_cast<const float4 *>(p.gate + (size_t)grp * p.gate_ld + col);
         float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)row * p.ldo + col);
+        // all loads first: the stores below could alias them as far as the
+        // compiler knows, which would serialise eight round trips
+        float4 xs[8], gs[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            float4 g = __ldg(g4 + q);
-            float4 x = d4[q];
+            xs[q] = d4[q];
+            gs[q] = __ldg(g4 + q);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 g = gs[q];
+            float4 x = xs[q];
             x.x = fmaf(g.x, v[4 * q], x.x);
             x.y = fmaf(g.y, v[4 * q + 1], x.y);
             x.z = fmaf(g.z, v[4 * q + 2], x.z);
@@ -264,7 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(C::B_TFULL + b), 1);
-            mbar_init(bar(C::B_TEMPTY + b), 4);     // one arrival per epilogue warp
+            mbar_init(bar(C::B_TEMPTY + b), EPI_WARPS);  // one arrival per epilogue warp
         }
         mbar_init(bar(C::B_DRAIN), 1);
         mbar_fence_init();
@@ -328,7 +341,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp >= 2) {
         // ---- epilogue ----
+        constexpr int NPW = BN / 64;                // 32-column chunks per warp
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 2) >> 2;           // which half of the columns
         const int row_in = quarter * 32 + lane;
         uint32_t tl = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
@@ -337,42 +352,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!__all_sync(0xffffffffu, ok)) goto done;
             tc_fence_after();
             const int row = p.row_begin + (tile / p.tiles_n) * BM + row_in;
-            const int n0 = (tile % p.tiles_n) * BN;
+            const int n0 = (tile % p.tiles_n) * BN + half * (BN / 2);
             const bool live = row < p.row_end;
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t u[32];
-                tmem_ld32(taddr + c * 32, u);
-                tmem_wait_ld(u);
-                if (c == BN / 32 - 1) {
-                    // the whole accumulator buffer is in registers or consumed:
-                    // hand it back to the MMA issuer before the last stores
+            const uint32_t taddr =
+                tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2);
+            uint32_t u[2][32];
+            tmem_ld32(taddr, u[0]);
+            tmem_wait_ld(u[0]);
+#pragma unroll
+            for (int c = 0; c < NPW; ++c) {
+                if (c + 1 < NPW) {
+                    tmem_ld32(taddr + (c + 1) * 32, u[(c + 1) & 1]);
+                } else {
+                    // the accumulator buffer is fully in registers: hand it
+                    // back to the MMA issuer before the last stores
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + buf));
                 }
                 const int col = n0 + c * 32;
-                if (!live || col >= p.N) continue;
-                float v[32];
-                if (p.bias) {
-                    const uint4 *b4 = reinterpret_cast<const uint4 *>(p.bias + col);
+                if (live && col < p.N) {
+                    const uint32_t(&uc)[32] = u[c & 1];
+                    float v[32];
+                    if (p.bias) {
+                        const uint4 *b4 = reinterpret_cast<const uint4 *>(p.bias + col);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 bb = __ldg(b4 + q);
-                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&bb);
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 bb = __ldg(b4 + q);
+                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&bb);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float2 f = __bfloat1622float2(h2[e]);
-                            v[8 * q + 2 * e] = __uint_as_float(u[8 * q + 2 * e]) + f.x;
-                            v[8 * q + 2 * e + 1] = __uint_as_float(u[8 * q + 2 * e + 1]) + f.y;
+                            for (int e = 0; e < 4; ++e) {
+                                float2 f = __bfloat1622float2(h2[e]);
+                                v[8 * q + 2 * e] = __uint_as_float(uc[8 * q + 2 * e]) + f.x;
+                                v[8 * q + 2 * e + 1] = __uint_as_float(uc[8 * q + 2 * e + 1]) + f.y;
+                            }
                         }
-                    }
-                } else {
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(uc[i]);
+                    }
+                    Epi<EPI>::apply(p, row, col, v);
                 }
-                Epi<EPI>::apply(p, row, col, v);
+                if (c + 1 < NPW) tmem_wait_ld(u[(c + 1) & 1]);
             }
         }
     }
