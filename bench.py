@@ -60,6 +60,92 @@ DIT_CONFIGS = {
 }
 
 
+QKV_ATTN_CONFIGS = {
+    "qkv_attn14b": dict(S=4, grid=(3, 30, 52), heads=40, head_dim=128, history=3, dim=5120,
+                        layers=40, n_chunks=64,
+                        desc="14B-scale QKV + attention stack: dim 5120, 40 heads x 128, S=4, "
+                             "4680-token chunks, W=3 + anchor, 40 layers, random-init bf16 "
+                             "weights ~ N(0, 0.02)"),
+}
+
+
+def run_qkv_attn(args, name, rank, world):
+    """Steady rounds of the per-layer P and attention of a 14B-scale model:
+    for each layer, wf_qkv_proj_rope_publish (QKV GEMM 5120 -> 15360 with
+    RoPE + paged publish) and wf_round_attention; the normalised layer input
+    is a synthetic N(0, 1) bf16 activation (the rest of the block is out of
+    this workload)."""
+    import torch
+    import chunk_causal_dit_round_b300 as wf
+
+    cfg = QKV_ATTN_CONFIGS[name]
+    S, W = cfg["S"], cfg["history"]
+    L = getattr(args, "layers", None) or cfg["layers"]
+    NC = math.prod(cfg["grid"])
+    H, D, dim = cfg["heads"], cfg["head_dim"], cfg["dim"]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    k_steady = S + W + 2
+    n_chunks = max(cfg["n_chunks"], k_steady + args.warmup + args.steps + 1)
+    r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16)
+    g = torch.Generator(device=dev)
+    g.manual_seed(777 + rank)
+    ws = [(torch.randn((3 * dim, dim), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+          for _ in range(L)]
+    bs = [(torch.randn((3 * dim,), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+          for _ in range(L)]
+    xs = [torch.randn((S + 1, NC, dim), generator=g, device=dev).to(torch.bfloat16) for _ in range(2)]
+    out = torch.empty((S + 1, NC, dim), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_round(i):
+        info = r.step()
+        for l in range(L):
+            r.publish_proj(l, xs[i % 2], ws[l], bs[l], stream)
+            r.attention(l, out, wf.WF_ATTN_TC, stream)
+        return info
+
+    for i in range(k_steady + args.warmup):
+        one_round(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    flops = 0.0
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        for j in range(args.steps):
+            evs[j][0].record(stream)
+            info = one_round(j)
+            evs[j][1].record(stream)
+            T = info.n_tasks * NC
+            flops += L * (info.attn_flops + 2.0 * T * dim * 3 * dim)
+        torch.cuda.synchronize()
+    st = r.sync_status()
+    if st != wf.WF_OK:
+        raise RuntimeError(f"device status {st}")
+    per = [a.elapsed_time(b) for a, b in evs]
+    ms = sum(per)
+    times = torch.tensor([ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    ms = times.item()
+    peak, src = _sustained_peak()
+    tf = flops / (ms * 1e-3) / 1e12
+    res = {"workload": name, "desc": cfg["desc"], "layers": L,
+           "value": round(world * args.steps / (ms * 1e-3), 3), "unit": "chunks/s",
+           "round_ms_p50": round(statistics.median(per), 3), "rounds": args.steps,
+           "flops_per_round": flops / args.steps,
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                        "peak_source": f"{src} bf16 dense (sustained)"},
+           "gpu_launches_per_round": 3 * L, "clocks": clk.summary()}
+    del r, ws, xs
+    torch.cuda.empty_cache()
+    return res
+
+
 def _sustained_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -466,7 +552,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="wan13_attn", choices=sorted(CONFIGS) + sorted(DIT_CONFIGS))
+    ap.add_argument("--config", default="wan13_attn",
+                    choices=sorted(CONFIGS) + sorted(DIT_CONFIGS) + sorted(QKV_ATTN_CONFIGS))
     ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
@@ -485,8 +572,9 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    if args.config in DIT_CONFIGS:
-        d = run_dit(args, args.config, rank, world)
+    if args.config in DIT_CONFIGS or args.config in QKV_ATTN_CONFIGS:
+        fn = run_dit if args.config in DIT_CONFIGS else run_qkv_attn
+        d = fn(args, args.config, rank, world)
         if rank == 0:
             print(json.dumps(d), flush=True)
         if world > 1:
