@@ -128,3 +128,35 @@ def test_page_table_bit_exact_vs_oracle(cfg):
         assert wf.lib.wf_round_step(h, ctypes.byref(info)) == wf.WF_EDONE
     finally:
         wf.lib.wf_plan_destroy(h)
+
+
+def test_dit_entry_points_validate_before_any_cuda_call():
+    """The DiT and linear-layer entry points reject unbound plans and bad
+    sizes on the host (no CUDA call is reached on these paths)."""
+    rc, h = _plan(4, 4680, 12, 128, 3, n_chunks=64, grid_h=30, grid_w=52, layers=30)
+    assert rc == wf.WF_OK
+    try:
+        n = ctypes.c_size_t()
+        # model_dim must be heads * head_dim; ffn % 64; 4C % 64; freq even
+        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, ctypes.byref(n)) == wf.WF_OK
+        rows = 5 * 4680
+        lat = 16 * 3 * 60 * 104
+        want = (rows * 1536 * 4 + rows * 1536 * 2 + rows * 8960 * 2 + rows * 64 * 2 + 2 * 5 * lat * 4
+                + 30 * 5 * 6 * 1536 * 4 + 5 * 2 * 1536 * 4 + 5 * (256 + 9 * 1536) * 4)
+        assert want <= n.value <= want + 16 * 256 + 30 * 128
+        for bad in ((1535, 8960, 16, 256), (1536, 8961, 16, 256), (1536, 8960, 15, 256),
+                    (1536, 8960, 16, 255)):
+            assert wf.lib.wf_dit_workspace_size(h, *bad, ctypes.byref(n)) == wf.WF_EINVAL
+        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, None) == wf.WF_EINVAL
+        m = wf.wf_dit_model()
+        assert wf.lib.wf_dit_bind(h, ctypes.byref(m), ctypes.c_void_p(256), None) == wf.WF_EUNBOUND
+        assert wf.lib.wf_dit_bind(h, None, ctypes.c_void_p(256), None) == wf.WF_EINVAL
+        assert wf.lib.wf_dit_round(h, None, None, None, None, None) == wf.WF_EUNBOUND
+        p = ctypes.c_void_p(256)
+        assert wf.lib.wf_qkv_proj_rope_publish(h, 0, p, p, None, None) == wf.WF_EUNBOUND
+        assert wf.lib.wf_linear(h, p, 128, 64, 0, 128, p, None, 64, 64, wf.WF_EPI_F32, p, 64,
+                                None, 0, 1, None) == wf.WF_EUNBOUND
+        assert wf.lib.wf_linear(None, p, 128, 64, 0, 128, p, None, 64, 64, wf.WF_EPI_F32, p, 64,
+                                None, 0, 1, None) == wf.WF_EINVAL
+    finally:
+        wf.lib.wf_plan_destroy(h)
