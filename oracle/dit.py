@@ -291,7 +291,7 @@ class Model:
             lab = np.concatenate(lab)
             for i, t in enumerate(tasks):
                 q = proj[i][0]
-                mask = np.broadcast_to(lab[None, :] >= t.stage, (self.nc, lab.shape[0]))
+                mask = np.broadcast_to(sch.sees(cfg, t.stage, lab)[None, :], (self.nc, lab.shape[0]))
                 o = masked_attention(q.transpose(1, 0, 2), K, V, mask).transpose(1, 0, 2)
                 xs[i] = self.finish_layer(xs[i], o, t.stage, layer)
                 if t.stage == cfg.S:

@@ -117,7 +117,7 @@ def round_attention(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw,
         q = task_queries(geom, t, layer, raw, qk_dtype)
         if rows is not None:
             q = q[np.asarray(rows)]
-        mask = np.broadcast_to(lab[None, :] >= t.stage, (q.shape[0], lab.shape[0]))
+        mask = np.broadcast_to(sch.sees(cfg, t.stage, lab)[None, :], (q.shape[0], lab.shape[0]))
         o = masked_attention(q.transpose(1, 0, 2), K, V, mask)
         outs.append(o.transpose(1, 0, 2))
     return outs

@@ -19,6 +19,17 @@ Generation":
 * App. B.8 -- fixed page capacity: anchor, bounded history, live store and at
   most S denoising chunks.
 
+Two comparison graphs the pages define next to WF, on the same pages:
+
+* RF mask (Sec. 3.1, the reverse refinement of Rolling Forcing that Eq. 4
+  removes; Sec. 5.5 "RF's full active-window attention"): a denoising task
+  also reads the noisier live chunks of the window, M_RF(s, j) = 1 for all
+  s, j in A_k.  The store keeps the WF store context (reading: the reverse
+  edges are between denoising slots).
+* Sequential schedule (Sec. 2, NF1C): chunk after chunk, its S denoising
+  forwards and then its store pass, one task per round; round r runs chunk
+  r // (S+1) at stage r % (S+1), attending to anchor, history and itself.
+
 Readings where the pages are silent (each also listed in the design notes):
 
 * W ("history_chunks") counts clean history chunks *excluding* the anchor and
@@ -45,6 +56,9 @@ from dataclasses import dataclass
 ANCHOR_ADJACENT = 0
 ANCHOR_ABSOLUTE = 1
 
+MASK_WF = 0
+MASK_RF = 1
+
 # cleanliness labels j of Eq. 4, extended to the cached entries of Eq. 5
 KIND_ANCHOR = 0
 KIND_HISTORY = 1
@@ -59,6 +73,8 @@ class Cfg:
     history: int           # W, -1 = keep all clean chunks
     use_anchor: bool = True
     anchor_mode: int = ANCHOR_ADJACENT
+    mask: int = MASK_WF
+    sequential: bool = False
 
 
 @dataclass(frozen=True)
@@ -80,19 +96,44 @@ class Task:
 
 
 def n_rounds(cfg: Cfg) -> int:
-    """Algorithm 1 runs rounds k = 0 .. N_chunk + S - 1 (App. B.3)."""
+    """Algorithm 1 runs rounds k = 0 .. N_chunk + S - 1 (App. B.3); the
+    sequential schedule runs N_chunk (S+1) single-task rounds."""
+    if cfg.sequential:
+        return cfg.n_chunks * (cfg.S + 1)
     return cfg.n_chunks + cfg.S
+
+
+def live_tasks(cfg: Cfg, k: int) -> list[tuple[int, int]]:
+    """(chunk, stage) of the denoising tasks of round k, stages ascending:
+    A_k of Sec. 3.1 (after Eq. 3) with chunk k - s, or the one task of a
+    sequential round."""
+    if cfg.sequential:
+        i, s = divmod(k, cfg.S + 1)
+        return [(i, s)] if s < cfg.S else []
+    return [(k - s, s) for s in range(cfg.S) if 0 <= k - s < cfg.n_chunks]
 
 
 def active_stages(cfg: Cfg, k: int) -> list[int]:
     """A_k of Sec. 3.1 (after Eq. 3)."""
-    return [s for s in range(cfg.S) if 0 <= k - s < cfg.n_chunks]
+    return [s for _, s in live_tasks(cfg, k)]
 
 
 def store_chunk(cfg: Cfg, k: int):
     """Chunk refreshed by the store at round k, or None (Sec. 3.1)."""
+    if cfg.sequential:
+        i, s = divmod(k, cfg.S + 1)
+        return i if s == cfg.S else None
     u = k - cfg.S
     return u if 0 <= u < cfg.n_chunks else None
+
+
+def sees(cfg: Cfg, s: int, j: int) -> bool:
+    """Mask of Sec. 3.1 Eq. 4 extended to the labels of cached entries
+    (anchor/history S+1, live store S): WF 1[j >= s]; RF lets a denoising
+    query see every live label of the window as well."""
+    if cfg.mask == MASK_RF and s < cfg.S:
+        return j >= 0                      # every label (elementwise for arrays)
+    return j >= s
 
 
 def ring_size(cfg: Cfg) -> int:
@@ -121,7 +162,10 @@ def raw_anchor_page(cfg: Cfg) -> int:
 
 
 def clean_before(cfg: Cfg, k: int) -> list[int]:
-    """Chunks whose store finished in an earlier round: c + S < k."""
+    """Chunks whose store finished in an earlier round: c + S < k (the
+    store of chunk c runs in round c + S; round c (S+1) + S sequentially)."""
+    if cfg.sequential:
+        return [c for c in range(cfg.n_chunks) if c * (cfg.S + 1) + cfg.S < k]
     return [c for c in range(cfg.n_chunks) if c + cfg.S < k]
 
 
@@ -145,7 +189,7 @@ def anchor_tpos(cfg: Cfg, k: int) -> int:
     u = store_chunk(cfg, k)
     if u is not None and not (cfg.use_anchor and u == 0):
         others.append(u)
-    others += [k - s for s in active_stages(cfg, k)]
+    others += [c for c, _ in live_tasks(cfg, k)]
     if not others:
         return 0
     return max(0, min(others) - 1)
@@ -155,7 +199,7 @@ def round_tasks(cfg: Cfg, k: int) -> list[Task]:
     """The tasks of round k in slot order (stages ascending, then the store),
     each with its ordered context (Eq. 5; store context per App. B.3)."""
     S = cfg.S
-    act = active_stages(cfg, k)
+    live = live_tasks(cfg, k)
     u = store_chunk(cfg, k)
     prefix = []
     if anchor_present(cfg, k):
@@ -166,14 +210,14 @@ def round_tasks(cfg: Cfg, k: int) -> list[Task]:
     if u is not None:
         store_entry = Entry(KIND_STORE, u, S, clean_page(cfg, u), u)
     tasks = []
-    for s in act:
+    for c, s in live:
         ctx = list(prefix)
         if store_entry is not None:
             ctx.append(store_entry)
-        for j in act:
-            if j >= s:
-                ctx.append(Entry(KIND_LIVE, k - j, j, live_page(cfg, j), k - j))
-        tasks.append(Task(k - s, s, live_page(cfg, s), tuple(ctx)))
+        for c2, j in live:
+            if sees(cfg, s, j):
+                ctx.append(Entry(KIND_LIVE, c2, j, live_page(cfg, j), c2))
+        tasks.append(Task(c, s, live_page(cfg, s), tuple(ctx)))
     if u is not None:
         ctx = list(prefix) + [store_entry]
         tasks.append(Task(u, S, clean_page(cfg, u), tuple(ctx)))
@@ -181,7 +225,10 @@ def round_tasks(cfg: Cfg, k: int) -> list[Task]:
 
 
 def slot_occupancy(cfg: Cfg) -> float:
-    """eta_slot = N_chunk / (N_chunk + S) (App. B.4 Eq. 16)."""
+    """eta_slot = N_chunk / (N_chunk + S) (App. B.4 Eq. 16); a sequential
+    schedule keeps one of the S+1 slots busy per round."""
+    if cfg.sequential:
+        return 1.0 / (cfg.S + 1)
     return cfg.n_chunks / (cfg.n_chunks + cfg.S)
 
 

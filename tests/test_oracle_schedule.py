@@ -147,3 +147,91 @@ def test_planted_mistake_is_caught(monkeypatch):
     gold = read_schedule("schedule_s2_n6_full.txt")
     cfg = sch.Cfg(S=2, n_chunks=6, history=-1)
     assert any(_as_tuples(sch.round_tasks(cfg, k)) != v for k, v in gold.items())
+
+
+# ---- comparison graphs: RF mask and the sequential (NF1C) schedule -----------
+
+def _tuples(tasks):
+    return [(t.chunk, t.stage, t.dest_page,
+             tuple((e.kind, e.chunk, e.j, e.page, e.tpos) for e in t.context)) for t in tasks]
+
+
+@pytest.mark.parametrize("S,N,W", [(4, 12, 3), (2, 6, -1), (3, 7, 1)])
+def test_rf_mask_adds_exactly_the_reverse_edges(S, N, W):
+    """RF (Sec. 3.1: the reverse refinement Eq. 4 removes; Sec. 5.5 'full
+    active-window attention'): a denoising task additionally reads the live
+    chunks of noisier stages j < s, i.e. later chunks i' = k - j > i; nothing
+    else changes (pages, store context, prefix)."""
+    wf_cfg = sch.Cfg(S=S, n_chunks=N, history=W)
+    rf_cfg = sch.Cfg(S=S, n_chunks=N, history=W, mask=sch.MASK_RF)
+    for k in range(sch.n_rounds(wf_cfg)):
+        a, b = sch.round_tasks(wf_cfg, k), sch.round_tasks(rf_cfg, k)
+        assert [(t.chunk, t.stage, t.dest_page) for t in a] == [(t.chunk, t.stage, t.dest_page) for t in b]
+        live = [(t.chunk, t.stage) for t in a if t.stage < S]
+        for ta, tb in zip(a, b):
+            if ta.stage == S:
+                assert ta.context == tb.context
+                continue
+            extra = [e for e in tb.context if e not in ta.context]
+            assert all(e in tb.context for e in ta.context)
+            assert sorted((e.chunk, e.j) for e in extra) == sorted((c, s) for c, s in live if s < ta.stage)
+            assert all(e.kind == sch.KIND_LIVE and e.chunk > ta.chunk for e in extra)
+            assert sch.key_count(tb, 7) == sch.key_count(ta, 7) + 7 * len(extra)
+
+
+def test_rf_has_no_sequential_order():
+    """With reverse edges a cleaner task reads a noisier task of the same
+    round and vice versa, so no task-at-a-time order exists (the dependency
+    cycle Wave Parallelism needs removed, Sec. 4.1); WF replays in order."""
+    from oracle.round import Geom, round_attention_replay
+    import numpy as np
+    geom = Geom(1, 2, 2, 1, 8)
+    raw = lambda c, s, l: np.ones((4, 3, 1, 8))
+    k = 3
+    round_attention_replay(sch.Cfg(S=3, n_chunks=6, history=1), geom, k, 0, raw)
+    with pytest.raises(AssertionError):
+        round_attention_replay(sch.Cfg(S=3, n_chunks=6, history=1, mask=sch.MASK_RF), geom, k, 0, raw)
+
+
+def test_sequential_schedule_hand_worked():
+    """NF1C (Sec. 2): chunk after chunk, S denoising forwards then the store,
+    one task per round, each attending to anchor, history and itself.
+    S = 2, N = 3, W = 1: ring of R = 2 pages (1, 2), live pages 3 + s, anchor
+    page 0 (derived by hand from Eq. 5 and App. B.3)."""
+    cfg = sch.Cfg(S=2, n_chunks=3, history=1, sequential=True)
+    A, H, U, L = sch.KIND_ANCHOR, sch.KIND_HISTORY, sch.KIND_STORE, sch.KIND_LIVE
+    want = {
+        0: [(0, 0, 3, ((L, 0, 0, 3, 0),))],
+        1: [(0, 1, 4, ((L, 0, 1, 4, 0),))],
+        2: [(0, 2, 0, ((U, 0, 2, 0, 0),))],
+        3: [(1, 0, 3, ((A, 0, 3, 0, 0), (L, 1, 0, 3, 1)))],
+        4: [(1, 1, 4, ((A, 0, 3, 0, 0), (L, 1, 1, 4, 1)))],
+        5: [(1, 2, 1, ((A, 0, 3, 0, 0), (U, 1, 2, 1, 1)))],
+        6: [(2, 0, 3, ((A, 0, 3, 0, 0), (H, 1, 3, 1, 1), (L, 2, 0, 3, 2)))],
+        7: [(2, 1, 4, ((A, 0, 3, 0, 0), (H, 1, 3, 1, 1), (L, 2, 1, 4, 2)))],
+        8: [(2, 2, 2, ((A, 0, 3, 0, 0), (H, 1, 3, 1, 1), (U, 2, 2, 2, 2)))],
+    }
+    assert sch.n_rounds(cfg) == 9
+    for k, v in want.items():
+        assert _tuples(sch.round_tasks(cfg, k)) == v, k
+
+
+@pytest.mark.parametrize("S,N,W", [(4, 9, 3), (2, 5, -1), (3, 4, 0), (1, 3, 1)])
+def test_sequential_schedule_invariants(S, N, W):
+    cfg = sch.Cfg(S=S, n_chunks=N, history=W, sequential=True)
+    seen = []
+    for k in range(sch.n_rounds(cfg)):
+        tasks = sch.round_tasks(cfg, k)
+        assert len(tasks) == 1                       # one forward per round
+        t = tasks[0]
+        seen.append((t.chunk, t.stage))
+        assert (t.chunk, t.stage) == divmod(k, S + 1)
+        own = [e for e in t.context if e.kind in (sch.KIND_LIVE, sch.KIND_STORE)]
+        assert [(e.chunk, e.j) for e in own] == [(t.chunk, t.stage)]
+        hist = [e.chunk for e in t.context if e.kind == sch.KIND_HISTORY]
+        clean = list(range(1, t.chunk))
+        assert hist == (clean if W < 0 else clean[len(clean) - min(len(clean), W):])
+        assert any(e.kind == sch.KIND_ANCHOR for e in t.context) == (t.chunk > 0)
+    # N = S + 1 forwards per chunk (NF1C), chunks strictly in order
+    assert seen == [(i, s) for i in range(N) for s in range(S + 1)]
+    assert sch.slot_occupancy(cfg) == pytest.approx(1 / (S + 1))
