@@ -57,6 +57,15 @@ DIT_CONFIGS = {
                      layers=30, n_chunks=135, steps=[1000.0, 800.0, 600.0, 400.0, 200.0],
                      desc="long rollout, 5-step (S=5), same 1.3B shapes, 135 chunks, paged K/V "
                           "ring with oldest-chunk eviction, W=3 + anchor"),
+    # comparison graphs on the same model and kernels
+    "dit13_rf": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
+                     layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], mask=1,
+                     desc="as dit13 with Rolling Forcing's full active-window mask (reverse "
+                          "edges to noisier live chunks), one round per chunk"),
+    "dit13_seq": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
+                      layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], sequential=True,
+                      desc="as dit13 run sequentially (NF1C): each chunk's 4 denoising forwards "
+                           "and its store pass, one task per forward"),
 }
 
 
@@ -174,9 +183,13 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     C = 16
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    k_steady = S + W + 2
-    n_chunks = max(cfg["n_chunks"], k_steady + warmup + steps + 1)
-    r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16)
+    seq = cfg.get("sequential", False)
+    per_step = S + 1 if seq else 1          # rounds (forward passes) per completed chunk
+    k_steady = (W + 2) * (S + 1) if seq else S + W + 2
+    n_chunks = max(cfg["n_chunks"], (k_steady // per_step) + warmup + steps + 2)
+    r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16,
+                 mask=cfg.get("mask", 0),
+                 schedule=wf.WF_SCHED_SEQUENTIAL if seq else wf.WF_SCHED_WAVEFRONT)
     g = torch.Generator(device=dev)
     g.manual_seed(4321 + rank)
 
@@ -204,7 +217,7 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
         return info.attn_flops * L + lin + 2.0 * T * (4 * C) * dim * 2
 
     i = 0
-    for _ in range(k_steady + warmup):
+    for _ in range(k_steady + warmup * per_step):
         r.step()
         model.round(zs[i % n_in], epss[i % n_in], None, chunk, stream)
         i += 1
@@ -214,17 +227,25 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     flops = 0.0
+    launches = 0
+    prev_anchor = r.info.anchor_tpos
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
         torch.cuda.synchronize()
         t0.record(stream)
         for j in range(steps):
-            info = r.step()
             evs[j][0].record(stream)
-            model.round(zs[i % n_in], epss[i % n_in], None, chunk, stream)
+            for _ in range(per_step):
+                info = r.step()
+                model.round(zs[i % n_in], epss[i % n_in], None, chunk, stream)
+                flops += round_flops(info)
+                # patchify, patch GEMM, head LN, head GEMM; 7 per layer; plus a
+                # re-rotation launch per layer when the anchor moved
+                moved = info.anchor_tpos >= 0 and info.anchor_tpos != prev_anchor
+                launches += 4 + 7 * L + (L if moved else 0)
+                prev_anchor = info.anchor_tpos
+                i += 1
             evs[j][1].record(stream)
-            flops += round_flops(info)
-            i += 1
         t1.record(stream)
         torch.cuda.synchronize()
     st = r.sync_status()
@@ -240,14 +261,16 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     peak, src = _sustained_peak()
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L, "value": round(chunks_s, 3),
-           "unit": "chunks/s",
-           "frames_per_s": round(12 * chunks_s, 2), "round_ms_p50": round(statistics.median(per), 3),
-           "rounds": steps, "eta_slot": round(cfg["n_chunks"] / (cfg["n_chunks"] + S), 4),
+           "unit": "chunks/s", "forwards_per_chunk_timed": per_step,
+           "frames_per_s": round(12 * chunks_s, 2),
+           "ms_per_chunk_p50": round(statistics.median(per), 3),
+           "chunks_timed": steps,
+           "eta_slot": round(1 / (S + 1) if seq else cfg["n_chunks"] / (cfg["n_chunks"] + S), 4),
            "flops_per_round": flops / steps,
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
                         "peak_source": f"{src} bf16 dense (sustained)"},
-           "gpu_launches_per_round": 4 + 8 * L, "clocks": clk.summary()}
+           "gpu_launches": launches, "clocks": clk.summary()}
     del model, r, P
     torch.cuda.empty_cache()
     return res

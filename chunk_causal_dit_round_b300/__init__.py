@@ -34,6 +34,10 @@ WF_FP32 = 0
 WF_BF16 = 1
 WF_ANCHOR_ADJACENT = 0
 WF_ANCHOR_ABSOLUTE = 1
+WF_MASK_WF = 0
+WF_MASK_RF = 1
+WF_SCHED_WAVEFRONT = 0
+WF_SCHED_SEQUENTIAL = 1
 WF_ATTN_AUTO = 0
 WF_ATTN_TC = 1
 WF_ATTN_SIMT = 2
@@ -57,7 +61,8 @@ class wf_plan_opts(ctypes.Structure):
     _fields_ = [("n_chunks", ctypes.c_int), ("layers", ctypes.c_int), ("grid_t", ctypes.c_int),
                 ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("use_anchor", ctypes.c_int), ("anchor_mode", ctypes.c_int),
-                ("rope_theta", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("mask", ctypes.c_int),
+                ("schedule", ctypes.c_int)]
 
 
 class wf_buffer_sizes(ctypes.Structure):
@@ -162,12 +167,13 @@ class Round:
 
     def __init__(self, S, chunk_tokens, heads, head_dim, history, *, n_chunks, layers=1,
                  grid=(3, 0, 0), dtype=WF_BF16, use_anchor=True,
-                 anchor_mode=WF_ANCHOR_ADJACENT, rope_theta=10000.0, device="cuda",
-                 bind=True):
+                 anchor_mode=WF_ANCHOR_ADJACENT, rope_theta=10000.0, mask=WF_MASK_WF,
+                 schedule=WF_SCHED_WAVEFRONT, device="cuda", bind=True):
         o = default_opts()
         o.n_chunks, o.layers = n_chunks, layers
         o.grid_t, o.grid_h, o.grid_w = grid
         o.dtype, o.use_anchor, o.anchor_mode, o.rope_theta = dtype, int(use_anchor), anchor_mode, rope_theta
+        o.mask, o.schedule = mask, schedule
         self.S, self.NC, self.H, self.D = S, chunk_tokens, heads, head_dim
         self.dtype = dtype
         h = ctypes.c_void_p()

@@ -169,7 +169,8 @@ int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_ou
     if (!p->dit_bound) return WF_EUNBOUND;
     if (p->k < 0) return WF_ENOROUND;
     const int S = p->S, NC = p->NC, k = p->k;
-    const bool new_chunk = k < p->o.n_chunks;
+    bool new_chunk = false;                      // a task at stage 0 reads z_new
+    for (int i = 0; i < p->rd.n_tasks; ++i) new_chunk |= p->rd.slot[i] == 0;
     if (new_chunk && (!z_new || ((uintptr_t)z_new & 7))) return WF_EINVAL;
     if (S > 1 && (!eps || !aligned16(eps))) return WF_EINVAL;
     if ((x0_out && !aligned16(x0_out)) || (chunk_out && ((uintptr_t)chunk_out & 3)))

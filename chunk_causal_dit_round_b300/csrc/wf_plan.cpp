@@ -37,50 +37,66 @@ size_t tables_bytes(const WfGeom &g) {
     return (size_t)(g.t_max * g.dt2 + g.gh * g.dh2 + g.gw * g.dw2) * 8;
 }
 
+// Live (denoising) tasks of the current round: (chunk, stage), stages
+// ascending.  Wavefront: chunk k - s for every s with 0 <= k - s < N
+// (Sec. 3.1 Eq. 3).  Sequential: the single task of round k, if it is not
+// the chunk's store pass.
+int live_tasks(const wf_plan_s *p, int *chunk, int *stage) {
+    int n = 0;
+    if (p->o.schedule == WF_SCHED_SEQUENTIAL) {
+        int i = p->k / (p->S + 1), s = p->k % (p->S + 1);
+        if (s < p->S) { chunk[0] = i; stage[0] = s; n = 1; }
+        return n;
+    }
+    for (int s = 0; s < p->S; ++s) {
+        int c = p->k - s;
+        if (c >= 0 && c < p->o.n_chunks) { chunk[n] = c; stage[n] = s; ++n; }
+    }
+    return n;
+}
+
 // Anchor position of the round (mode ADJACENT): one chunk before the oldest
 // non-anchor chunk present in the round, clamped at 0.
-int adjacent_anchor_pos(const wf_plan_s *p, int store_chunk) {
+int adjacent_anchor_pos(const wf_plan_s *p, int store_chunk, const int *live_chunk, int n_live) {
     int oldest = -1;
     auto take = [&](int c) { if (oldest < 0 || c < oldest) oldest = c; };
     for (auto &h : p->history) take(h.first);
     if (store_chunk >= 0 && !(p->o.use_anchor && store_chunk == 0)) take(store_chunk);
-    for (int s = 0; s < p->S; ++s) {
-        int c = p->k - s;
-        if (c >= 0 && c < p->o.n_chunks) take(c);
-    }
+    for (int a = 0; a < n_live; ++a) take(live_chunk[a]);
     return oldest <= 0 ? 0 : oldest - 1;
 }
 
 void build_round(wf_plan_s *p, int store_chunk, int store_page) {
-    const int S = p->S, k = p->k, N = p->o.n_chunks;
+    const int S = p->S;
+    int lchunk[WF_MAX_STAGES], lstage[WF_MAX_STAGES];
+    const int na = live_tasks(p, lchunk, lstage);
     CtxEntry prefix[WF_MAX_CTX];
     int np = 0;
     bool anchor_in = p->o.use_anchor && p->anchor_stored;
     p->anchor_tpos = -1;
     if (anchor_in) {
-        p->anchor_tpos = p->o.anchor_mode == WF_ANCHOR_ABSOLUTE ? 0 : adjacent_anchor_pos(p, store_chunk);
+        p->anchor_tpos = p->o.anchor_mode == WF_ANCHOR_ABSOLUTE
+                             ? 0 : adjacent_anchor_pos(p, store_chunk, lchunk, na);
         prefix[np++] = {WF_KIND_ANCHOR, 0, S + 1, 0, p->anchor_tpos};
     }
     for (auto &h : p->history) prefix[np++] = {WF_KIND_HISTORY, h.first, S + 1, h.second, h.first};
     if (store_chunk >= 0) prefix[np++] = {WF_KIND_STORE, store_chunk, S, store_page, store_chunk};
 
-    int act[WF_MAX_STAGES];
-    int na = 0;
-    for (int s = 0; s < S; ++s)
-        if (k - s >= 0 && k - s < N) act[na++] = s;
-
     p->n_tasks = 0;
     for (int a = 0; a < na; ++a) {
-        int s = act[a];
+        int s = lstage[a];
         HostTask &t = p->tasks[p->n_tasks++];
-        t.chunk = k - s;
+        t.chunk = lchunk[a];
         t.stage = s;
         t.dest = 1 + p->R + s;
         t.n_ctx = 0;
         for (int e = 0; e < np; ++e) t.ctx[t.n_ctx++] = prefix[e];
-        for (int b = a; b < na; ++b) {
-            int j = act[b];
-            t.ctx[t.n_ctx++] = {WF_KIND_LIVE, k - j, j, 1 + p->R + j, k - j};
+        // Eq. 5: live K/V of stages j >= s in increasing j; the RF mask also
+        // lists the noisier stages j < s
+        for (int b = 0; b < na; ++b) {
+            int j = lstage[b];
+            if (j >= s || p->o.mask == WF_MASK_RF)
+                t.ctx[t.n_ctx++] = {WF_KIND_LIVE, lchunk[b], j, 1 + p->R + j, lchunk[b]};
         }
     }
     if (store_chunk >= 0) {
@@ -202,6 +218,8 @@ void wf_plan_opts_default(wf_plan_opts *o) {
     o->use_anchor = 1;
     o->anchor_mode = WF_ANCHOR_ADJACENT;
     o->rope_theta = 10000.0;
+    o->mask = WF_MASK_WF;
+    o->schedule = WF_SCHED_WAVEFRONT;
 }
 
 int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks,
@@ -219,6 +237,8 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
     if (o.anchor_mode != WF_ANCHOR_ADJACENT && o.anchor_mode != WF_ANCHOR_ABSOLUTE) return WF_EINVAL;
     if (o.use_anchor != 0 && o.use_anchor != 1) return WF_EINVAL;
     if (!(o.rope_theta > 1.0) || !std::isfinite(o.rope_theta)) return WF_EINVAL;
+    if (o.mask != WF_MASK_WF && o.mask != WF_MASK_RF) return WF_EINVAL;
+    if (o.schedule != WF_SCHED_WAVEFRONT && o.schedule != WF_SCHED_SEQUENTIAL) return WF_EINVAL;
     if (o.grid_t < 1) return WF_EINVAL;
     if (o.grid_h == 0 && o.grid_w == 0) {
         if (chunk_tokens % o.grid_t) return WF_EINVAL;
@@ -319,7 +339,8 @@ int wf_bind(wf_plan_t p, void *pool, void *qbuf, void *scratch) {
 int wf_round_step(wf_plan_t p, wf_round_info *info) {
     if (!p) return WF_EINVAL;
     const int S = p->S, N = p->o.n_chunks;
-    if (p->k + 1 >= N + S) return WF_EDONE;
+    const bool seq = p->o.schedule == WF_SCHED_SEQUENTIAL;
+    if (p->k + 1 >= (seq ? N * (S + 1) : N + S)) return WF_EDONE;
     p->k += 1;
     // round boundary: the previous store page becomes history (App. B.3)
     if (p->have_prev_store) {
@@ -334,7 +355,7 @@ int wf_round_step(wf_plan_t p, wf_round_info *info) {
         }
         p->have_prev_store = false;
     }
-    int u = p->k - S;
+    int u = seq ? (p->k % (S + 1) == S ? p->k / (S + 1) : -1) : p->k - S;
     int store_chunk = -1, store_page = -1;
     if (u >= 0 && u < N) {
         store_chunk = u;

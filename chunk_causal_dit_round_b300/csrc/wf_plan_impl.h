@@ -55,11 +55,17 @@ struct wf_plan_s {
     ~wf_plan_s() { delete[] dit.layers; }
 };
 
-// Active slots of the current round form the contiguous range [lo, hi]
-// (stage s is active iff k - N_chunk < s <= k, the store likewise with s = S).
+// Active slots of the current round form the contiguous range [lo, hi]:
+// wavefront stage s is active iff k - N_chunk < s <= k, the store likewise
+// with s = S; a sequential round has one slot.
 inline void wf_active_range(const wf_plan_s *p, int *lo, int *hi) {
-    *lo = p->k - p->o.n_chunks + 1 > 0 ? p->k - p->o.n_chunks + 1 : 0;
-    *hi = p->k < p->S ? p->k : p->S;
+    int a = WF_MAX_TASKS, b = -1;
+    for (int i = 0; i < p->rd.n_tasks; ++i) {
+        if (p->rd.slot[i] < a) a = p->rd.slot[i];
+        if (p->rd.slot[i] > b) b = p->rd.slot[i];
+    }
+    *lo = a;
+    *hi = b;
 }
 
 // Launch the QKV publication for `layer` of the current round: either the

@@ -65,6 +65,14 @@ typedef struct CUstream_st *cudaStream_t; /* identical to CUDA's own typedef */
 #define WF_ANCHOR_ADJACENT 0 /* anchor re-rotated just before the oldest retained chunk */
 #define WF_ANCHOR_ABSOLUTE 1 /* anchor keeps its own position (frames 0..grid_t-1) */
 
+#define WF_MASK_WF 0   /* chunk-wise causal mask M_WF(s, j) = 1[j >= s] (Sec. 3.1 Eq. 4) */
+#define WF_MASK_RF 1   /* Rolling Forcing's full active window: denoising tasks also read
+                          noisier live chunks (the reverse edges Eq. 4 removes) */
+
+#define WF_SCHED_WAVEFRONT  0 /* S+1 staggered tasks per round, one chunk per round (1F1C) */
+#define WF_SCHED_SEQUENTIAL 1 /* one task per round: each chunk's S denoising forwards, then
+                                 its store pass (NF1C, Sec. 2) */
+
 #define WF_KIND_ANCHOR  0
 #define WF_KIND_HISTORY 1
 #define WF_KIND_STORE   2
@@ -93,6 +101,8 @@ typedef struct wf_plan_opts {
     int use_anchor;     /* 1 (default): first clean chunk is a persistent anchor (App. B.3) */
     int anchor_mode;    /* WF_ANCHOR_ADJACENT (default) or WF_ANCHOR_ABSOLUTE */
     double rope_theta;  /* RoPE base, default 10000 */
+    int mask;           /* WF_MASK_WF (default) or WF_MASK_RF */
+    int schedule;       /* WF_SCHED_WAVEFRONT (default) or WF_SCHED_SEQUENTIAL */
 } wf_plan_opts;
 
 typedef struct wf_buffer_sizes {
@@ -106,7 +116,7 @@ typedef struct wf_buffer_sizes {
 } wf_buffer_sizes;
 
 typedef struct wf_round_info {
-    int k;                 /* round just entered, 0 .. N_chunk+S-1 */
+    int k;                 /* round just entered, 0 .. N_chunk+S-1 (sequential: 0 .. N_chunk(S+1)-1) */
     int n_tasks;           /* active tasks, 1 .. S+1 */
     int store_chunk;       /* chunk whose store pass runs (its clean output B_i completes), or -1 */
     int anchor_tpos;       /* temporal chunk position of the anchor's keys this round, or -1 */
@@ -144,8 +154,12 @@ int wf_bind(wf_plan_t plan, void *pool, void *qbuf, void *scratch);
 /* Advance to the next round k (the first call enters k = 0).  Host only:
  * promotes the previous round's store page into history, evicts the oldest
  * history page beyond W, allocates the store page of chunk k - S, and builds
- * the ordered contexts of the round (Algorithm 1, App. B.3).  info may be
- * NULL.  Errors: WF_EDONE after round N_chunk + S - 1 (state unchanged). */
+ * the ordered contexts of the round (Algorithm 1, App. B.3).  With
+ * WF_SCHED_SEQUENTIAL round k runs the single task chunk k / (S+1) at stage
+ * k % (S+1) (stage S = its store pass) over anchor, history and itself.
+ * With WF_MASK_RF each denoising task's context also lists the noisier live
+ * chunks (all live stages in increasing order).  info may be NULL.
+ * Errors: WF_EDONE after the last round (state unchanged). */
 int wf_round_step(wf_plan_t plan, wf_round_info *info);
 
 /* Export the current round's table as int32 rows, one per context entry:

@@ -14,7 +14,8 @@ def make_round(cfg: sch.Cfg, geom: Geom, dtype, layers=1):
     return wf.Round(cfg.S, geom.chunk_tokens, geom.heads, geom.head_dim, cfg.history,
                     n_chunks=cfg.n_chunks, layers=layers, grid=geom.grid, dtype=dtype,
                     use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode,
-                    rope_theta=geom.theta)
+                    rope_theta=geom.theta, mask=cfg.mask,
+                    schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
 
 
 def raw_fn(seed, geom: Geom, tdtype, qk_scale=1.0, v_scale=1.0, heads=None):

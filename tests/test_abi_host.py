@@ -47,6 +47,8 @@ def test_validation_codes():
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, grid_h=5, grid_w=4)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, dtype=7)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, anchor_mode=3)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=6, mask=2)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=6, schedule=2)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=40)[0] == wf.WF_ERANGE      # context > 32 chunks
     assert wf.lib.wf_plan(2, 48, 2, 32, -1, None, None) == wf.WF_EINVAL
     rc, h = _plan(2, 48, 2, 32, -1, n_chunks=6, grid_h=4, grid_w=4)
@@ -96,12 +98,18 @@ def _oracle_rows(cfg, k):
 CFGS = [sch.Cfg(S, N, W, a, m) for S, N, W, a, m in itertools.product(
     [1, 2, 4, 5], [1, 3, 6, 12], [-1, 0, 1, 3], [True, False],
     [sch.ANCHOR_ADJACENT, sch.ANCHOR_ABSOLUTE])] + [sch.Cfg(4, 133, 3), sch.Cfg(5, 135, 3)]
+# the comparison graphs: RF mask (wavefront rounds) and the sequential NF1C schedule
+CFGS += [sch.Cfg(S, N, W, a, mask=sch.MASK_RF) for S, N, W, a in itertools.product(
+    [1, 2, 4], [3, 12], [-1, 1, 3], [True, False])]
+CFGS += [sch.Cfg(S, N, W, a, m, sequential=True) for S, N, W, a, m in itertools.product(
+    [1, 2, 4], [1, 5], [-1, 0, 2], [True, False], [sch.ANCHOR_ADJACENT, sch.ANCHOR_ABSOLUTE])]
 
 
 @pytest.mark.parametrize("cfg", CFGS, ids=str)
 def test_page_table_bit_exact_vs_oracle(cfg):
     rc, h = _plan(cfg.S, 12, 1, 8, cfg.history, n_chunks=cfg.n_chunks, grid_h=2, grid_w=2,
-                  use_anchor=int(cfg.use_anchor), anchor_mode=cfg.anchor_mode)
+                  use_anchor=int(cfg.use_anchor), anchor_mode=cfg.anchor_mode, mask=cfg.mask,
+                  schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
     if 1 + (cfg.history if cfg.history >= 0 else cfg.n_chunks - 1) + 1 + cfg.S > wf.WF_MAX_CTX:
         assert rc == wf.WF_ERANGE
         return

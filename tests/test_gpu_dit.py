@@ -36,7 +36,8 @@ SHARP_MAX, SHARP_MEAN, SHARP_REL = 5e-2, 4e-3, 1e-2
 def new_round(cfg, grid, heads, layers):
     return wf.Round(cfg.S, grid[0] * grid[1] * grid[2], heads, 128, cfg.history,
                     n_chunks=cfg.n_chunks, layers=layers, grid=grid, dtype=wf.WF_BF16,
-                    use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode)
+                    use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode, mask=cfg.mask,
+                    schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
 
 
 # ---- QKV projection + RoPE + publication -------------------------------------------
@@ -137,7 +138,9 @@ GRID = (3, 8, 10)       # 240 tokens per chunk: one full 128-row tile and a ragg
 
 
 @pytest.mark.parametrize("cfg", [sch.Cfg(2, 6, 1), sch.Cfg(3, 5, -1),
-                                 sch.Cfg(2, 5, 2, anchor_mode=sch.ANCHOR_ABSOLUTE)], ids=str)
+                                 sch.Cfg(2, 5, 2, anchor_mode=sch.ANCHOR_ABSOLUTE),
+                                 sch.Cfg(2, 5, 1, mask=sch.MASK_RF),
+                                 sch.Cfg(2, 4, 1, sequential=True)], ids=str)
 def test_dit_request_matches_oracle(cfg):
     steps = [1000.0, 750.0, 500.0, 250.0][:cfg.S] if cfg.S != 2 else [1000.0, 500.0]
     mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=SHARP_STD, seed=12, steps=steps)

@@ -60,7 +60,9 @@ SMALL = Geom(grid_t=3, grid_h=10, grid_w=10, heads=2, head_dim=128)   # 300 toke
 @pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(2, 6, -1),
                                  sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE),
-                                 sch.Cfg(2, 5, 2, use_anchor=False)], ids=str)
+                                 sch.Cfg(2, 5, 2, use_anchor=False),
+                                 sch.Cfg(4, 10, 3, mask=sch.MASK_RF),
+                                 sch.Cfg(3, 4, 1, sequential=True)], ids=str)
 def test_bf16_request_all_rounds(cfg, kernel):
     mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, kernel, seed=7, qk_scale=2.0,
                                  err=scaled_errors)
