@@ -54,7 +54,8 @@ SYMBOLS = ["wf_plan_opts_default", "wf_plan", "wf_plan_buffer_sizes", "wf_bind",
            "wf_round_step", "wf_page_table", "wf_qkv_rope_publish", "wf_round_attention",
            "wf_round_attention_noalloc", "wf_sync_status", "wf_plan_destroy", "wf_strerror",
            "wf_linear", "wf_qkv_proj_rope_publish", "wf_dit_workspace_size", "wf_dit_bind",
-           "wf_dit_round"]
+           "wf_dit_round", "wf_selftest_timeout", "wf_plan_state_size", "wf_plan_export_state",
+           "wf_plan_import_state"]
 
 
 class wf_plan_opts(ctypes.Structure):
@@ -119,6 +120,10 @@ def _load():
         "wf_dit_workspace_size": (I, [P, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_dit_bind": (I, [P, ctypes.POINTER(wf_dit_model), VP, VP]),
         "wf_dit_round": (I, [P, VP, VP, VP, VP, VP]),
+        "wf_selftest_timeout": (I, [P, ctypes.c_uint, VP]),
+        "wf_plan_state_size": (I, [P, ctypes.POINTER(ctypes.c_size_t)]),
+        "wf_plan_export_state": (I, [P, VP, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
+        "wf_plan_import_state": (I, [P, VP, ctypes.c_size_t]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -259,6 +264,23 @@ class Round:
                             _ptr(bias), N, K, epilogue, _ptr(out), out.stride(0), _ptr(gate),
                             gate.stride(0) if gate is not None else 0, rows_per_group,
                             _stream_handle(stream)), "wf_linear")
+
+    def export_state(self) -> bytes:
+        """wf_plan_export_state: the host round state as bytes."""
+        n = ctypes.c_size_t()
+        check(lib.wf_plan_state_size(self.plan, ctypes.byref(n)), "wf_plan_state_size")
+        buf = ctypes.create_string_buffer(n.value)
+        w = ctypes.c_size_t()
+        check(lib.wf_plan_export_state(self.plan, buf, n.value, ctypes.byref(w)),
+              "wf_plan_export_state")
+        return buf.raw[:w.value]
+
+    def import_state(self, state: bytes):
+        check(lib.wf_plan_import_state(self.plan, state, len(state)), "wf_plan_import_state")
+
+    def selftest_timeout(self, limit_us=10000, stream=None):
+        check(lib.wf_selftest_timeout(self.plan, limit_us, _stream_handle(stream)),
+              "wf_selftest_timeout")
 
     def sync_status(self, stream=None):
         return lib.wf_sync_status(self.plan, _stream_handle(stream))

@@ -142,3 +142,6 @@ cudaError_t wf_launch_ln_mod(const float *x, __nv_bfloat16 *out, int row_begin, 
 cudaError_t wf_launch_patchify(const WfGeom &g, int C, const float *const *src, int lo, int hi,
                                __nv_bfloat16 *patches, cudaStream_t stream);
 cudaError_t wf_launch_time_embedding(const WfDit &d, int S, cudaStream_t stream);
+
+// ---- failure-detection self-test (selftest.cu) --------------------------------
+cudaError_t wf_launch_wait_probe(void *scratch, uint64_t limit_ns, cudaStream_t stream);

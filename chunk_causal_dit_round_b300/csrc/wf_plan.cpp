@@ -131,6 +131,15 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
 
 }  // namespace
 
+// Rebuild the current round's contexts from the round state (after a state
+// import): the current round's store is the one recorded for promotion.
+void wf_rebuild_round(wf_plan_s *p) {
+    if (p->have_prev_store)
+        build_round(p, p->prev_store_chunk, p->prev_store_page);
+    else
+        build_round(p, -1, -1);
+}
+
 // Shared by wf_qkv_rope_publish (Q/K/V given) and the projection path
 // (x and W_qkv given): one launch publishes every active task; the anchor
 // key is re-rotated from its unrotated copy when the window moved.
@@ -466,6 +475,104 @@ int wf_sync_status(wf_plan_t p, cudaStream_t stream) {
             return WF_ECUDA;
         return WF_ETIMEOUT;
     }
+    return WF_OK;
+}
+
+int wf_selftest_timeout(wf_plan_t p, unsigned int limit_us, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (limit_us < 1 || limit_us > 2000000) return WF_ERANGE;
+    return wf_launch_wait_probe(p->scratch, (uint64_t)limit_us * 1000ull, stream) == cudaSuccess
+               ? WF_OK
+               : WF_ECUDA;
+}
+
+// ---- checkpoint / resume of the host round state ----------------------------
+// Layout (int32 words): magic, version, S, N_C, H, D, W, n_chunks, layers,
+// use_anchor, anchor_mode, mask, schedule, k, have_prev_store,
+// prev_store_chunk, prev_store_page, anchor_stored, n_history,
+// (chunk, page) x n_history, n_free, page x n_free, anchor_rot[layers],
+// published[layers].
+namespace {
+constexpr int32_t kStateMagic = 0x57465354;  // "WFST"
+constexpr int32_t kStateVersion = 1;
+}  // namespace
+
+int wf_plan_state_size(wf_plan_t p, size_t *bytes) {
+    if (!p || !bytes) return WF_EINVAL;
+    *bytes = sizeof(int32_t) * (19 + 2 * p->history.size() + 1 + p->free_pages.size() +
+                                2 * (size_t)p->o.layers);
+    return WF_OK;
+}
+
+int wf_plan_export_state(wf_plan_t p, void *buf, size_t cap, size_t *written) {
+    if (!p || !buf || !written) return WF_EINVAL;
+    size_t need;
+    wf_plan_state_size(p, &need);
+    if (cap < need) return WF_ENOMEM;
+    std::vector<int32_t> w;
+    w.reserve(need / 4);
+    const int32_t head[] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
+                            p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
+                            p->o.mask, p->o.schedule, p->k, p->have_prev_store ? 1 : 0,
+                            p->prev_store_chunk, p->prev_store_page, p->anchor_stored ? 1 : 0,
+                            (int32_t)p->history.size()};
+    w.insert(w.end(), head, head + 19);
+    for (auto &h : p->history) { w.push_back(h.first); w.push_back(h.second); }
+    w.push_back((int32_t)p->free_pages.size());
+    for (int f : p->free_pages) w.push_back(f);
+    for (int l = 0; l < p->o.layers; ++l) w.push_back(p->anchor_rot[l]);
+    for (int l = 0; l < p->o.layers; ++l) w.push_back(p->published[l]);
+    std::memcpy(buf, w.data(), w.size() * 4);
+    *written = w.size() * 4;
+    return WF_OK;
+}
+
+int wf_plan_import_state(wf_plan_t p, const void *buf, size_t n) {
+    if (!p || !buf || n % 4 || n < 19 * 4) return WF_EINVAL;
+    const int32_t *w = static_cast<const int32_t *>(buf);
+    const size_t nw = n / 4;
+    const int32_t want[] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
+                            p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
+                            p->o.mask, p->o.schedule};
+    for (int i = 0; i < 13; ++i)
+        if (w[i] != want[i]) return WF_EINVAL;
+    const int S = p->S, N = p->o.n_chunks;
+    const bool seq = p->o.schedule == WF_SCHED_SEQUENTIAL;
+    const int k = w[13];
+    if (k < -1 || k >= (seq ? N * (S + 1) : N + S)) return WF_EINVAL;
+    size_t at = 19;
+    const int nh = w[18];
+    if (nh < 0 || nh > p->R || at + 2 * (size_t)nh + 1 > nw) return WF_EINVAL;
+    std::deque<std::pair<int, int>> hist;
+    for (int i = 0; i < nh; ++i, at += 2) {
+        if (w[at] < 0 || w[at] >= N || w[at + 1] < 1 || w[at + 1] > p->R) return WF_EINVAL;
+        hist.emplace_back(w[at], w[at + 1]);
+    }
+    const int nf = w[at++];
+    if (nf < 0 || nf > p->R || at + (size_t)nf + 2 * (size_t)p->o.layers != nw) return WF_EINVAL;
+    std::deque<int> freep;
+    for (int i = 0; i < nf; ++i, ++at) {
+        if (w[at] < 1 || w[at] > p->R) return WF_EINVAL;
+        freep.push_back(w[at]);
+    }
+    std::vector<int> rot(p->o.layers), pub(p->o.layers);
+    for (int l = 0; l < p->o.layers; ++l) rot[l] = w[at++];
+    for (int l = 0; l < p->o.layers; ++l) pub[l] = w[at++];
+    const bool have_prev = w[14] != 0;
+    const int prev_chunk = w[15], prev_page = w[16];
+    if (have_prev && (prev_chunk < 0 || prev_chunk >= N || prev_page < 0 || prev_page > p->R))
+        return WF_EINVAL;
+    p->k = k;
+    p->have_prev_store = have_prev;
+    p->prev_store_chunk = prev_chunk;
+    p->prev_store_page = prev_page;
+    p->anchor_stored = w[17] != 0;
+    p->history = hist;
+    p->free_pages = freep;
+    p->anchor_rot = rot;
+    p->published = pub;
+    if (k >= 0) wf_rebuild_round(p);
     return WF_OK;
 }
 

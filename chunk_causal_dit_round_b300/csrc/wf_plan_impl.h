@@ -68,6 +68,9 @@ inline void wf_active_range(const wf_plan_s *p, int *lo, int *hi) {
     *hi = b;
 }
 
+// Rebuild the current round's task table from the round state.
+void wf_rebuild_round(wf_plan_s *p);
+
 // Launch the QKV publication for `layer` of the current round: either the
 // projection GEMM (x != nullptr) or the given Q/K/V; the anchor re-rotation
 // when the window moved.  Returns a WF_* code.

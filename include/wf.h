@@ -339,6 +339,28 @@ int wf_dit_round(wf_plan_t plan, const float *z_new, const float *eps, float *x0
  * Returns WF_OK, WF_ETIMEOUT if a kernel's bounded wait gave up, or WF_ECUDA. */
 int wf_sync_status(wf_plan_t plan, cudaStream_t stream);
 
+/* Failure-detection self-test.  Launches one CTA that waits, with the same
+ * bounded wait the library's kernels use, on a barrier that nothing ever
+ * completes; after limit_us microseconds the wait gives up, records the
+ * timeout in the plan's status word and the kernel returns, leaving the
+ * context usable.  The following wf_sync_status returns WF_ETIMEOUT (and
+ * clears the word).  Errors: WF_EUNBOUND, WF_ERANGE (limit_us outside
+ * 1 .. 2,000,000), WF_ECUDA. */
+int wf_selftest_timeout(wf_plan_t plan, unsigned int limit_us, cudaStream_t stream);
+
+/* Checkpoint / resume of a request's host round state: round index,
+ * history ring, free pages, anchor state and the per-layer publication and
+ * anchor-rotation records (int32 words, versioned).  Together with the K/V
+ * page pool (caller-owned device memory, which the caller keeps) this lets a
+ * request continue in a new plan of the same shape.  Import checks the shape
+ * words (S, N_C, heads, head_dim, W, n_chunks, layers, anchor, mask,
+ * schedule) and every page and chunk id, then rebuilds the current round's
+ * contexts.  No CUDA call.  Errors: WF_EINVAL (null, foreign or corrupt
+ * state), WF_ENOMEM (cap smaller than wf_plan_state_size). */
+int wf_plan_state_size(wf_plan_t plan, size_t *bytes);
+int wf_plan_export_state(wf_plan_t plan, void *buf, size_t cap, size_t *written);
+int wf_plan_import_state(wf_plan_t plan, const void *buf, size_t n);
+
 void wf_plan_destroy(wf_plan_t plan);
 const char *wf_strerror(int code);
 

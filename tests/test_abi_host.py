@@ -168,3 +168,77 @@ def test_dit_entry_points_validate_before_any_cuda_call():
                                 None, 0, 1, None) == wf.WF_EINVAL
     finally:
         wf.lib.wf_plan_destroy(h)
+
+
+def _round_plan(cfg, **kw):
+    return _plan(cfg.S, 12, 1, 8, cfg.history, n_chunks=cfg.n_chunks, grid_h=2, grid_w=2,
+                 use_anchor=int(cfg.use_anchor), anchor_mode=cfg.anchor_mode, mask=cfg.mask,
+                 schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT,
+                 layers=3, **kw)
+
+
+def _table(h):
+    cap = 512
+    buf = (ctypes.c_int32 * (10 * cap))()
+    n = ctypes.c_int()
+    assert wf.lib.wf_page_table(h, buf, cap, ctypes.byref(n)) == wf.WF_OK
+    return [tuple(buf[10 * i:10 * i + 10]) for i in range(n.value)]
+
+
+def _export(h):
+    n = ctypes.c_size_t()
+    assert wf.lib.wf_plan_state_size(h, ctypes.byref(n)) == wf.WF_OK
+    buf = ctypes.create_string_buffer(n.value)
+    w = ctypes.c_size_t()
+    assert wf.lib.wf_plan_export_state(h, buf, n.value, ctypes.byref(w)) == wf.WF_OK
+    assert w.value == n.value
+    short = ctypes.create_string_buffer(n.value - 4)
+    assert wf.lib.wf_plan_export_state(h, short, n.value - 4, ctypes.byref(w)) == wf.WF_ENOMEM
+    return buf.raw
+
+
+@pytest.mark.parametrize("cfg", [sch.Cfg(4, 14, 3), sch.Cfg(2, 7, -1), sch.Cfg(3, 9, 1, mask=sch.MASK_RF),
+                                 sch.Cfg(2, 4, 1, sequential=True)], ids=str)
+def test_state_export_import_resumes_the_request(cfg):
+    """A request checkpointed at every round and resumed in a fresh plan
+    follows the uninterrupted plan's schedule bit for bit to the end."""
+    for cut in range(-1, sch.n_rounds(cfg)):
+        rc, a = _round_plan(cfg)
+        assert rc == wf.WF_OK
+        for _ in range(cut + 1):
+            assert wf.lib.wf_round_step(a, None) == wf.WF_OK
+        state = _export(a)
+        rc, b = _round_plan(cfg)
+        assert wf.lib.wf_plan_import_state(b, state, len(state)) == wf.WF_OK
+        if cut >= 0:
+            assert _table(b) == _table(a)
+        while True:
+            ra, rb = wf.lib.wf_round_step(a, None), wf.lib.wf_round_step(b, None)
+            assert ra == rb
+            if ra == wf.WF_EDONE:
+                break
+            assert _table(a) == _table(b)
+        wf.lib.wf_plan_destroy(a)
+        wf.lib.wf_plan_destroy(b)
+
+
+def test_state_import_rejects_foreign_or_corrupt_state():
+    cfg = sch.Cfg(4, 14, 3)
+    rc, a = _round_plan(cfg)
+    for _ in range(9):
+        wf.lib.wf_round_step(a, None)
+    state = bytearray(_export(a))
+    rc, other = _plan(4, 12, 1, 8, 2, n_chunks=14, grid_h=2, grid_w=2, layers=3)   # W differs
+    assert wf.lib.wf_plan_import_state(other, bytes(state), len(state)) == wf.WF_EINVAL
+    rc, b = _round_plan(cfg)
+    assert wf.lib.wf_plan_import_state(b, bytes(state[:-4]), len(state) - 4) == wf.WF_EINVAL
+    bad = bytearray(state)
+    bad[19 * 4:19 * 4 + 4] = (999).to_bytes(4, "little", signed=True)   # history chunk id
+    assert wf.lib.wf_plan_import_state(b, bytes(bad), len(bad)) == wf.WF_EINVAL
+    bad = bytearray(state)
+    bad[0] ^= 1                                                       # magic
+    assert wf.lib.wf_plan_import_state(b, bytes(bad), len(bad)) == wf.WF_EINVAL
+    assert wf.lib.wf_plan_import_state(b, None, 0) == wf.WF_EINVAL
+    assert wf.lib.wf_selftest_timeout(b, 1000, None) == wf.WF_EUNBOUND
+    for h in (a, other, b):
+        wf.lib.wf_plan_destroy(h)
