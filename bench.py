@@ -135,11 +135,7 @@ def run_qkv_attn(args, name, rank, world):
     if st != wf.WF_OK:
         raise RuntimeError(f"device status {st}")
     per = [a.elapsed_time(b) for a, b in evs]
-    ms = sum(per)
-    times = torch.tensor([ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    ms = times.item()
+    ms, = max_over_ranks([sum(per)], world, dev)
     peak, src = _sustained_peak()
     tf = flops / (ms * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L,
@@ -153,6 +149,17 @@ def run_qkv_attn(args, name, rank, world):
     del r, ws, xs
     torch.cuda.empty_cache()
     return res
+
+
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of per-rank timings over all replicas (one
+    process per GPU, independent replicas; the slowest rank sets the
+    whole-job time).  With world == 1 the values come back unchanged."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
 
 
 def _sustained_peak():
@@ -251,12 +258,8 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     st = r.sync_status()
     if st != wf.WF_OK:
         raise RuntimeError(f"device status {st}")
-    ms = t0.elapsed_time(t1)
     per = sorted(a.elapsed_time(b) for a, b in evs)
-    times = torch.tensor([ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    ms = times.item()
+    ms, = max_over_ranks([t0.elapsed_time(t1)], world, dev)
     chunks_s = world * steps / (ms * 1e-3)
     peak, src = _sustained_peak()
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
@@ -440,10 +443,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
-    times = torch.tensor([ms, e2e_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    ms, e2e_ms = times.tolist()
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
     peak_tf, hbm, peak_src = _peaks()
     attn_avg = statistics.mean(attn_ms)
     per_launch = flops / args.steps
