@@ -52,7 +52,10 @@ struct Cfg {
     static constexpr int B_FULL = 0, B_EMPTY = NST, B_TFULL = 2 * NST, B_TEMPTY = 2 * NST + 2,
                          B_DRAIN = 2 * NST + 4, NBARS = 2 * NST + 5;
     static constexpr uint32_t SM_MISC = SM_BAR + ((NBARS * 8 + 63) / 64) * 64;
-    static constexpr uint32_t SM_ALLOC = SM_MISC + 64 + 1024;
+    // per epilogue warp: a 32 x 32 fp32 staging tile (transposes the residual
+    // read-modify-write into coalesced row segments)
+    static constexpr uint32_t SM_STAGE = SM_MISC + 64;
+    static constexpr uint32_t SM_ALLOC = SM_STAGE + 8 * 4096 + 1024;
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
 };
 
@@ -250,6 +253,48 @@ struct Epi<WF_EPI_HEAD> {
     }
 };
 
+// Gated residual add from a staged 32 x 32 block (row r at stg[r * 32],
+// 16-byte units swizzled by r & 7): lane l takes column pair l & 15 of rows
+// 2i + (l >> 4), i = 0..15, in four batches whose loads of x and the gates
+// are all issued before their stores.  row0 is the block's first row, col0
+// its first column.
+__device__ __forceinline__ void residual_staged(const GemmParams &p, const float *stg, int lane,
+                                                int row0, int col0) {
+    const int cp = lane & 15, rp = lane >> 4;
+    const int col = col0 + 2 * cp;
+    float2 b = make_float2(0.f, 0.f);
+    if (p.bias) b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p.bias + col));
+    const int rpg = p.rows_per_group;
+    const int g_lo = row0 / rpg, g_bnd = (g_lo + 1) * rpg;
+    float *out = static_cast<float *>(p.out);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {          // four batches of 4 row pairs
+        float2 xv[4], gv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = row0 + 2 * (4 * h + i) + rp;
+            if (row < p.row_end) {
+                const int grp = rpg >= 32 ? g_lo + (row >= g_bnd ? 1 : 0) : row / rpg;
+                xv[i] = *reinterpret_cast<const float2 *>(out + (size_t)row * p.ldo + col);
+                gv[i] = __ldg(reinterpret_cast<const float2 *>(p.gate + (size_t)grp * p.gate_ld + col));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 2 * (4 * h + i) + rp;
+            const int row = row0 + r;
+            const float2 a = *reinterpret_cast<const float2 *>(stg + r * 32 +
+                                                               (((cp >> 1) ^ (r & 7)) * 4) + (cp & 1) * 2);
+            if (row < p.row_end) {
+                float2 x = xv[i];
+                x.x = fmaf(gv[i].x, a.x + b.x, x.x);
+                x.y = fmaf(gv[i].y, a.y + b.y, x.y);
+                *reinterpret_cast<float2 *>(out + (size_t)row * p.ldo + col) = x;
+            }
+        }
+    }
+}
+
 // ---- kernel -----------------------------------------------------------------------
 
 template <int BN, int EPI>
@@ -371,7 +416,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + buf));
                 }
                 const int col = n0 + c * 32;
-                if (live && col < p.N) {
+                if constexpr (EPI == WF_EPI_GATED_RESIDUAL) {
+                    // Stage the 32 x 32 block through shared memory so that the
+                    // fp32 read-modify-write of x covers two full 128-byte row
+                    // segments per warp instruction instead of 32 rows.
+                    if (col < p.N) {
+                        const uint32_t(&uc)[32] = u[c & 1];
+                        float *stg = reinterpret_cast<float *>(smem + C::SM_STAGE) + (warp - 2) * 1024;
+                        float4 *srow = reinterpret_cast<float4 *>(stg + lane * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            srow[q ^ (lane & 7)] =
+                                make_float4(__uint_as_float(uc[4 * q]), __uint_as_float(uc[4 * q + 1]),
+                                            __uint_as_float(uc[4 * q + 2]), __uint_as_float(uc[4 * q + 3]));
+                        __syncwarp();
+                        residual_staged(p, stg, lane, row - lane, col);
+                        __syncwarp();
+                    }
+                } else if (live && col < p.N) {
                     const uint32_t(&uc)[32] = u[c & 1];
                     float v[32];
                     if (p.bias) {
