@@ -193,7 +193,7 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     seq = cfg.get("sequential", False)
     per_step = S + 1 if seq else 1          # rounds (forward passes) per completed chunk
     k_steady = (W + 2) * (S + 1) if seq else S + W + 2
-    n_chunks = max(cfg["n_chunks"], (k_steady // per_step) + warmup + steps + 2)
+    n_chunks = max(cfg["n_chunks"], (k_steady // per_step) + warmup + steps + 4)
     r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16,
                  mask=cfg.get("mask", 0),
                  schedule=wf.WF_SCHED_SEQUENTIAL if seq else wf.WF_SCHED_WAVEFRONT)
@@ -259,12 +259,38 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     if st != wf.WF_OK:
         raise RuntimeError(f"device status {st}")
     per = sorted(a.elapsed_time(b) for a, b in evs)
-    ms, = max_over_ranks([t0.elapsed_time(t1)], world, dev)
+
+    # end to end through the public API with host buffers: each chunk's fresh
+    # noise and transition draws go up from pinned memory, the finished clean
+    # chunk comes back
+    h_z = torch.empty(latent, dtype=torch.float32).pin_memory()
+    h_eps = torch.empty((S, latent), dtype=torch.float32).pin_memory()
+    h_z.copy_(zs[0].cpu())
+    h_eps.copy_(epss[0].cpu())
+    h_out = torch.empty(latent, dtype=torch.float32).pin_memory()
+    d_z, d_eps = torch.empty_like(zs[0]), torch.empty_like(epss[0])
+    e2e_steps = 2
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for _ in range(per_step):
+            d_z.copy_(h_z, non_blocking=True)
+            d_eps.copy_(h_eps, non_blocking=True)
+            r.step()
+            model.round(d_z, d_eps, None, chunk, stream)
+        h_out.copy_(chunk, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms, e2e_ms = max_over_ranks([t0.elapsed_time(t1), e0.elapsed_time(e1)], world, dev)
     chunks_s = world * steps / (ms * 1e-3)
     peak, src = _sustained_peak()
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L, "value": round(chunks_s, 3),
            "unit": "chunks/s", "forwards_per_chunk_timed": per_step,
+           "e2e": {"value": round(world * e2e_steps / (e2e_ms * 1e-3), 3), "unit": "chunks/s",
+                   "h2d_bytes_per_step": per_step * (h_z.numel() + h_eps.numel()) * 4,
+                   "d2h_bytes_per_step": h_out.numel() * 4, "steps": e2e_steps},
            "frames_per_s": round(12 * chunks_s, 2),
            "ms_per_chunk_p50": round(statistics.median(per), 3),
            "chunks_timed": steps,
@@ -424,21 +450,48 @@ def run_ours(args, rank, world):
         raise RuntimeError(f"device status {st}")
 
     # ---- timed: end to end through the C ABI with host buffers ------------
+    # Every round's Q/K/V go up from pinned host memory and its output comes
+    # back.  Two device buffers each way and two copy streams: round i+1's
+    # upload and round i-1's readback overlap round i's kernels.
     host_in = torch.empty_like(qkvs[0], device="cpu").pin_memory()
     host_in.copy_(qkvs[0].cpu())
-    host_out = torch.empty(out.shape, dtype=out.dtype, device="cpu").pin_memory()
-    dev_in = torch.empty_like(qkvs[0])
+    host_out = [torch.empty(out.shape, dtype=out.dtype, device="cpu").pin_memory() for _ in range(2)]
+    dev_in = [torch.empty_like(qkvs[0]) for _ in range(2)]
+    dev_out = [r.new_out() for _ in range(2)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_flops = 0.0
     torch.cuda.synchronize()
     e0.record(stream)
+    up.wait_stream(stream)
+    down.wait_stream(stream)
+    with torch.cuda.stream(up):
+        dev_in[0].copy_(host_in, non_blocking=True)
+        h2d_done[0].record(up)
     for i in range(e2e_steps):
-        dev_in.copy_(host_in, non_blocking=True)
+        b = i % 2
+        if i + 1 < e2e_steps:
+            nb = (i + 1) % 2
+            with torch.cuda.stream(up):
+                if i >= 1:
+                    up.wait_event(comp_done[nb])          # round i-1 has read dev_in[nb]
+                dev_in[nb].copy_(host_in, non_blocking=True)
+                h2d_done[nb].record(up)
+        stream.wait_event(h2d_done[b])
+        if i >= 2:
+            stream.wait_event(d2h_done[b])                # round i-2's output is home
         info = r.step()
-        r.publish(0, dev_in, stream)
-        r.attention(0, out, wf.WF_ATTN_AUTO, stream)
-        host_out.copy_(out, non_blocking=True)
+        r.publish(0, dev_in[b], stream)
+        r.attention(0, dev_out[b], wf.WF_ATTN_AUTO, stream)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(comp_done[b])
+            host_out[b].copy_(dev_out[b], non_blocking=True)
+            d2h_done[b].record(down)
         e2e_flops += info.attn_flops
+    stream.wait_stream(down)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -469,7 +522,7 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "e2e": {"value": round(world * e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
-                "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
+                "d2h_bytes_per_step": host_out[0].numel() * host_out[0].element_size(),
                 "ms_per_step": round(e2e_ms / max(1, e2e_steps), 4), "steps": e2e_steps},
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel",
@@ -580,7 +633,7 @@ def main():
     ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
