@@ -23,6 +23,11 @@ the chunk's own position; the anchor's key is its unrotated store key rotated
 at the anchor's position for this round (App. B.3).  Raw per-task Q/K/V come
 from a caller-supplied function ``raw(chunk, stage, layer) -> [N_C, 3, H, D]``.
 
+``qk_dtype=Fp8(...)`` models 8-bit attention (the pages' SageAttention
+backend, App. B.1 / Sec. 5, with the FP8 K/V pages of App. C.6): Q, K and V
+are stored as e4m3 after scaling (saturating at +-448); the anchor's key is
+re-rotated from its stored 8-bit unrotated copy once the window has moved.
+
 ``qk_dtype="bf16"`` models the pages' BF16 execution (App. B.1: BF16/FA3
 reference backend; App. B.2: K/V pages hold the published tensors): Q and K
 enter attention as bf16 values after RoPE, so the fp64 rotation is rounded
@@ -41,14 +46,41 @@ from .attention import masked_attention
 from .rope import rope_chunk
 
 
+@dataclass(frozen=True)
+class Fp8:
+    """e4m3 storage of Q, K (scaled by qk_scale) and V (scaled by v_scale)."""
+    qk_scale: float = 1.0
+    v_scale: float = 1.0
+
+
+def e4m3(x, scale=1.0):
+    """Round fp64 values to OCP FP8 e4m3 after multiplying by scale (round
+    to nearest even, saturating at +-448 as a satfinite conversion does),
+    returned divided by scale again."""
+    import torch
+    y = np.clip(np.asarray(x, np.float64) * scale, -448.0, 448.0)
+    q = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).double().numpy()
+    return q / scale
+
+
 def round_to(x: np.ndarray, qk_dtype):
     """Round fp64 values to the attention input dtype (None: unchanged)."""
     if qk_dtype is None:
         return x
+    if isinstance(qk_dtype, Fp8):
+        return e4m3(x, qk_dtype.qk_scale)
     if qk_dtype != "bf16":
         raise ValueError(qk_dtype)
     import torch
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+def round_v(v: np.ndarray, qk_dtype):
+    """V as attention reads it: e4m3 for Fp8 storage, else unchanged (the
+    raw values are already in the storage dtype)."""
+    if isinstance(qk_dtype, Fp8):
+        return e4m3(v, qk_dtype.v_scale)
+    return v
 
 
 @dataclass(frozen=True)
@@ -73,8 +105,12 @@ def entry_kv(cfg: sch.Cfg, geom: Geom, e: sch.Entry, layer: int, raw, qk_dtype=N
     """K (RoPE applied at e.tpos) and V of one context entry: [N_C, H, D] each."""
     producer_stage = e.j if e.kind == sch.KIND_LIVE else cfg.S
     x = np.asarray(raw(e.chunk, producer_stage, layer), dtype=np.float64)
-    k = rope_chunk(x[:, 1], e.tpos, geom.grid, geom.theta)
-    return round_to(k, qk_dtype), x[:, 2]
+    k_in = x[:, 1]
+    if isinstance(qk_dtype, Fp8) and e.kind == sch.KIND_ANCHOR and e.tpos != e.chunk:
+        # re-rotated from the stored 8-bit unrotated copy (App. B.3)
+        k_in = e4m3(k_in, qk_dtype.qk_scale)
+    k = rope_chunk(k_in, e.tpos, geom.grid, geom.theta)
+    return round_to(k, qk_dtype), round_v(x[:, 2], qk_dtype)
 
 
 def task_queries(geom: Geom, t: sch.Task, layer: int, raw, qk_dtype=None) -> np.ndarray:

@@ -169,3 +169,47 @@ def test_bf16_rounding_of_attention_inputs():
     y = np.random.default_rng(0).standard_normal(1000)
     r = round_to(y, "bf16")
     assert np.all(np.abs(r - y) <= 2.0 ** -8 * np.abs(y))
+
+
+# ---- 8-bit (e4m3) storage -------------------------------------------------------
+
+def test_e4m3_rounding_matches_the_format_definition():
+    """OCP FP8 e4m3 (4 exponent bits, bias 7, 3 mantissa bits, no infinity,
+    max 448): spacing 1/8 on [1, 2), round to nearest even, subnormals in
+    steps of 2^-9, saturation at 448 (satfinite)."""
+    from oracle.round import e4m3
+    cases = {1.0625: 1.0,            # halfway 1 .. 1.125 -> even (1.000b)
+             1.1875: 1.25,           # halfway 1.125 .. 1.25 -> even (1.010b)
+             1.1: 1.125, -3.3: -3.25, 448.0: 448.0, 500.0: 448.0, -1e4: -448.0,
+             2.0 ** -6: 2.0 ** -6,   # smallest normal
+             2.0 ** -9: 2.0 ** -9,   # smallest subnormal
+             2.0 ** -10: 0.0,        # halfway 0 .. 2^-9 -> even (0)
+             3 * 2.0 ** -10: 2 * 2.0 ** -9, 0.0: 0.0}
+    for x, want in cases.items():
+        assert e4m3(np.array([x]))[0] == want, x
+    # the scale multiplies before and divides after the rounding
+    assert e4m3(np.array([0.3]), 8.0)[0] == 2.5 / 8.0
+
+
+def test_fp8_fingerprint_is_exact():
+    """With Q = 0 and V one-hot in {0, 1} (exact in e4m3) the 8-bit round
+    still yields O = 1/|context| per visible entry (up to fp64 rounding): the mask and
+    page bookkeeping are unaffected by the storage precision."""
+    from oracle.round import Fp8, round_attention
+    cfg = sch.Cfg(3, 7, 2)
+    geom = Geom(1, 2, 3, 1, 16)
+    n = geom.chunk_tokens
+
+    def raw(c, s, l):
+        x = np.zeros((n, 3, 1, 16))
+        x[:, 1] = np.random.default_rng(100 * c + s).normal(size=(n, 1, 16))
+        x[:, 2, :, c] = 1.0
+        return x
+
+    k = 6
+    outs = round_attention(cfg, geom, k, 0, raw, qk_dtype=Fp8(4.0, 1.0))
+    for t, o in zip(sch.round_tasks(cfg, k), outs):
+        want = np.zeros(16)
+        for e in t.context:
+            want[e.chunk] += 1.0 / len(t.context)
+        assert np.allclose(o[:, 0, :], np.broadcast_to(want, (n, 16)), rtol=0, atol=1e-14)
