@@ -32,6 +32,7 @@ WF_EORDER = -10
 
 WF_FP32 = 0
 WF_BF16 = 1
+WF_FP8 = 2
 WF_ANCHOR_ADJACENT = 0
 WF_ANCHOR_ABSOLUTE = 1
 WF_MASK_WF = 0
@@ -63,7 +64,8 @@ class wf_plan_opts(ctypes.Structure):
                 ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("use_anchor", ctypes.c_int), ("anchor_mode", ctypes.c_int),
                 ("rope_theta", ctypes.c_double), ("mask", ctypes.c_int),
-                ("schedule", ctypes.c_int)]
+                ("schedule", ctypes.c_int), ("fp8_qk_scale", ctypes.c_double),
+                ("fp8_v_scale", ctypes.c_double)]
 
 
 class wf_buffer_sizes(ctypes.Structure):
@@ -173,12 +175,13 @@ class Round:
     def __init__(self, S, chunk_tokens, heads, head_dim, history, *, n_chunks, layers=1,
                  grid=(3, 0, 0), dtype=WF_BF16, use_anchor=True,
                  anchor_mode=WF_ANCHOR_ADJACENT, rope_theta=10000.0, mask=WF_MASK_WF,
-                 schedule=WF_SCHED_WAVEFRONT, device="cuda", bind=True):
+                 schedule=WF_SCHED_WAVEFRONT, fp8_scales=(1.0, 1.0), device="cuda", bind=True):
         o = default_opts()
         o.n_chunks, o.layers = n_chunks, layers
         o.grid_t, o.grid_h, o.grid_w = grid
         o.dtype, o.use_anchor, o.anchor_mode, o.rope_theta = dtype, int(use_anchor), anchor_mode, rope_theta
         o.mask, o.schedule = mask, schedule
+        o.fp8_qk_scale, o.fp8_v_scale = fp8_scales
         self.S, self.NC, self.H, self.D = S, chunk_tokens, heads, head_dim
         self.dtype = dtype
         h = ctypes.c_void_p()
@@ -193,15 +196,27 @@ class Round:
 
     @property
     def torch_dtype(self):
+        """Element type of the Q/K/V input and the attention output."""
         import torch
-        return torch.bfloat16 if self.dtype == WF_BF16 else torch.float32
+        return torch.float32 if self.dtype == WF_FP32 else torch.bfloat16
+
+    @property
+    def page_dtype(self):
+        """Element type of the query workspace and the K/V pages."""
+        import torch
+        return torch.float8_e4m3fn if self.dtype == WF_FP8 else self.torch_dtype
 
     def bind(self, device="cuda"):
         import torch
-        es = 2 if self.dtype == WF_BF16 else 4
+        es = {WF_FP32: 4, WF_BF16: 2, WF_FP8: 1}[self.dtype]
         s = self.sizes
-        self.pool = torch.zeros(s.pool // es, dtype=self.torch_dtype, device=device)
-        self.qbuf = torch.zeros(s.qbuf // es, dtype=self.torch_dtype, device=device)
+        self.pool = torch.zeros(s.pool // es, dtype=torch.uint8 if es == 1 else self.torch_dtype,
+                                device=device)
+        self.qbuf = torch.zeros(s.qbuf // es, dtype=torch.uint8 if es == 1 else self.torch_dtype,
+                                device=device)
+        if es == 1:
+            self.pool = self.pool.view(self.page_dtype)
+            self.qbuf = self.qbuf.view(self.page_dtype)
         self.scratch = torch.zeros(s.scratch, dtype=torch.uint8, device=device)
         check(lib.wf_bind(self.plan, ctypes.c_void_p(self.pool.data_ptr()),
                           ctypes.c_void_p(self.qbuf.data_ptr()),
@@ -288,7 +303,8 @@ class Round:
     def pool_view(self):
         """The pool as [P][L][2][H][N_C][D]."""
         s = self.sizes
-        L = s.pool // (s.n_pages * 2 * self.H * self.NC * self.D * (2 if self.dtype == WF_BF16 else 4))
+        es = {WF_FP32: 4, WF_BF16: 2, WF_FP8: 1}[self.dtype]
+        L = s.pool // (s.n_pages * 2 * self.H * self.NC * self.D * es)
         return self.pool.view(s.n_pages, L, 2, self.H, self.NC, self.D)
 
     def close(self):

@@ -32,6 +32,7 @@
 // returns.
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include <mutex>
 
@@ -46,14 +47,20 @@ constexpr int BM = 128;             // query rows per tile
 constexpr int BN = 128;             // keys per tile
 constexpr int HD = 128;             // head dim
 constexpr int NST = 4;              // K/V ring stages
-constexpr uint32_t TILE_BYTES = BM * HD * 2;
-constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
 constexpr int NUM_THREADS = 384;
 
-constexpr uint32_t SM_Q0 = 0;
-constexpr uint32_t SM_Q1 = TILE_BYTES;
-constexpr uint32_t SM_KV = 2 * TILE_BYTES;
-constexpr uint32_t SM_BAR = SM_KV + NST * TILE_BYTES;
+// Shared-memory layout of one CTA.  bf16: a 128 x 128 tile is two 64-column
+// halves of 128-byte rows (16 KB each); e4m3: one block of 128-byte rows.
+template <bool F8>
+struct Lay {
+    static constexpr uint32_t TILE = BM * HD * (F8 ? 1 : 2);
+    static constexpr uint32_t HALF = F8 ? TILE : TILE / 2;  // one 128-byte-wide column block
+    static constexpr uint32_t Q0 = 0;
+    static constexpr uint32_t Q1 = TILE;
+    static constexpr uint32_t KV = 2 * TILE;
+    static constexpr uint32_t BAR = KV + NST * TILE;
+};
+
 constexpr int B_QFULL = 0;
 constexpr int B_KVFULL = 1;
 constexpr int B_KVEMPTY = B_KVFULL + NST;
@@ -62,9 +69,12 @@ constexpr int B_PFULL = B_SFULL + 2;
 constexpr int B_ODONE = B_PFULL + 2;
 constexpr int B_DRAIN = B_ODONE + 2;
 constexpr int NBARS = B_DRAIN + 1;
-constexpr uint32_t SM_MISC = SM_BAR + ((NBARS * 8 + 63) / 64) * 64;
-constexpr uint32_t SM_TOTAL = SM_MISC + 64;
-constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;  // alignment slack
+
+template <bool F8>
+struct LayMisc {
+    static constexpr uint32_t MISC = Lay<F8>::BAR + ((NBARS * 8 + 63) / 64) * 64;
+    static constexpr uint32_t ALLOC = MISC + 64 + 1024;   // + alignment slack
+};
 
 constexpr uint64_t WAIT_NS = 1000000000ull;  // 1 s
 
@@ -83,7 +93,8 @@ struct TcParams {
     int n_units;
     int qpairs;           // pairs of query tiles per (task, head)
     int tpc;              // key tiles per chunk
-    float sl2;            // log2(e) / sqrt(D)
+    float sl2;            // log2(e) / sqrt(D) (/ qk_scale^2 for e4m3 Q and K)
+    float o_scale;        // 1 (bf16) or 1 / v_scale (e4m3 V)
     __nv_bfloat16 *out;
     uint32_t *ctl;        // scratch control words
 };
@@ -91,11 +102,12 @@ struct TcParams {
 __device__ __forceinline__ int kseq(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int vseq(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
+template <bool F8>
 struct Ctx {
     uint32_t sbase;
     volatile int *abort;
     uint32_t *status, *where;
-    __device__ uint32_t bar(int i) const { return sbase + SM_BAR + 8u * i; }
+    __device__ uint32_t bar(int i) const { return sbase + Lay<F8>::BAR + 8u * i; }
     __device__ bool wait(int b, uint32_t parity, uint32_t site) const {
         return mbar_wait(bar(b), parity, abort, status, where, site, WAIT_NS);
     }
@@ -112,15 +124,18 @@ __device__ __forceinline__ void decode_unit(int u, const WfRoundDev &rd, const T
 }
 
 // ---- producer ----------------------------------------------------------------
-__device__ void producer(const Ctx &c, const CUtensorMap *tq, const CUtensorMap *tkv,
+template <bool F8>
+__device__ void producer(const Ctx<F8> &c, const CUtensorMap *tq, const CUtensorMap *tkv,
                          const WfGeom &g, const WfRoundDev &rd, const TcParams &p, int ti, int h,
                          int qp, int n, uint32_t seq, uint32_t *issued) {
+    using L = Lay<F8>;
     const int plane_q = rd.slot[ti] * g.H + h;
-    mbar_arrive_expect_tx(c.bar(B_QFULL), 2 * TILE_BYTES);
-    tma_load_3d(c.sbase + SM_Q0, tq, c.bar(B_QFULL), 0, (2 * qp) * BM, plane_q);
-    tma_load_3d(c.sbase + SM_Q0 + HALF_BYTES, tq, c.bar(B_QFULL), 64, (2 * qp) * BM, plane_q);
-    tma_load_3d(c.sbase + SM_Q1, tq, c.bar(B_QFULL), 0, (2 * qp + 1) * BM, plane_q);
-    tma_load_3d(c.sbase + SM_Q1 + HALF_BYTES, tq, c.bar(B_QFULL), 64, (2 * qp + 1) * BM, plane_q);
+    mbar_arrive_expect_tx(c.bar(B_QFULL), 2 * L::TILE);
+    for (int x = 0; x < 2; ++x) {
+        const uint32_t dst = c.sbase + (x ? L::Q1 : L::Q0);
+        tma_load_3d(dst, tq, c.bar(B_QFULL), 0, (2 * qp + x) * BM, plane_q);
+        if (!F8) tma_load_3d(dst + L::HALF, tq, c.bar(B_QFULL), 64, (2 * qp + x) * BM, plane_q);
+    }
     for (int i = 0; i < 2 * n; ++i) {
         int j;
         int isv;
@@ -139,38 +154,85 @@ __device__ void producer(const Ctx &c, const CUtensorMap *tq, const CUtensorMap 
         int ci = j / p.tpc;
         int t = j - ci * p.tpc;
         int plane = ((rd.page[ti][ci] * g.L + p.layer) * 2 + isv) * g.H + h;
-        uint32_t dst = c.sbase + SM_KV + st * TILE_BYTES;
-        mbar_arrive_expect_tx(c.bar(B_KVFULL + st), TILE_BYTES);
+        uint32_t dst = c.sbase + L::KV + st * L::TILE;
+        mbar_arrive_expect_tx(c.bar(B_KVFULL + st), L::TILE);
         tma_load_3d(dst, tkv, c.bar(B_KVFULL + st), 0, t * BN, plane);
-        tma_load_3d(dst + HALF_BYTES, tkv, c.bar(B_KVFULL + st), 64, t * BN, plane);
+        if (!F8) tma_load_3d(dst + L::HALF, tkv, c.bar(B_KVFULL + st), 64, t * BN, plane);
         *issued = s + 1;
     }
 }
 
 // ---- MMA issuer ----------------------------------------------------------------
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0 in
+// bits 7-9 and 10-12), fp32 accumulator (bits 4-5 = 1), B major-ness in bit 16,
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// S = Q K^T: K = 16 per instruction for bf16 (two 64-column halves), 32 for
+// e4m3 (one 128-byte block); the descriptor start advances 32 bytes a step.
+template <bool F8>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+    if constexpr (F8) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN, false);
 #pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
-        uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-        mma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-               idesc, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < HD / 32; ++kk)
+            mma_ss_f8(d_tmem, sdesc_sw128(q_addr + kk * 32, 16, 1024),
+                      sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    } else {
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+            uint32_t off = (kk >> 2) * Lay<false>::HALF + (kk & 3) * 32;
+            mma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                   idesc, kk > 0 ? 1u : 0u);
+        }
     }
 }
+// O += P V: P from TMEM (bf16: 2 keys per column, e4m3: 4), V the MN-major B
+// operand (keys along K, rows of 128 bytes; 8-row groups 1 KB apart).
+template <bool F8>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
                                          bool acc) {
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, HD, true);
+    if constexpr (F8) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM, HD, true);
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-        mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, HALF_BYTES, 1024), idesc,
-               (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BN / 32; ++kk)
+            mma_ts_f8(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 4096, Lay<true>::HALF, 1024),
+                      idesc, (acc || kk > 0) ? 1u : 0u);
+    } else {
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, HD, true);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, Lay<false>::HALF, 1024),
+                   idesc, (acc || kk > 0) ? 1u : 0u);
     }
 }
 
-__device__ void mma_issuer(const Ctx &c, uint32_t tmem, int n, uint32_t seq, uint32_t it_base,
+template <bool F8>
+__device__ void mma_issuer(const Ctx<F8> &c, uint32_t tmem, int n, uint32_t seq, uint32_t it_base,
                            uint32_t unit_iter) {
     const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-    const uint32_t q0 = c.sbase + SM_Q0, q1 = c.sbase + SM_Q1;
+    using L = Lay<F8>;
+    const uint32_t q0 = c.sbase + L::Q0, q1 = c.sbase + L::Q1;
     if (!c.wait(B_QFULL, unit_iter & 1, 2)) return;
     tc_fence_after();
     for (int j = 0; j < n; ++j) {
@@ -178,11 +240,11 @@ __device__ void mma_issuer(const Ctx &c, uint32_t tmem, int n, uint32_t seq, uin
         int kst = ks % NST;
         if (!c.wait(B_KVFULL + kst, (ks / NST) & 1, 3)) return;
         tc_fence_after();
-        uint32_t ka = c.sbase + SM_KV + kst * TILE_BYTES;
+        uint32_t ka = c.sbase + L::KV + kst * L::TILE;
         if (j == 0) {
-            issue_qk(tS0, q0, ka);
+            issue_qk<F8>(tS0, q0, ka);
             mma_commit(c.bar(B_SFULL + 0));
-            issue_qk(tS1, q1, ka);
+            issue_qk<F8>(tS1, q1, ka);
             mma_commit(c.bar(B_SFULL + 1));
             mma_commit(c.bar(B_KVEMPTY + kst));
             continue;
@@ -190,33 +252,33 @@ __device__ void mma_issuer(const Ctx &c, uint32_t tmem, int n, uint32_t seq, uin
         uint32_t vs = seq + vseq(j - 1, n);
         int vst = vs % NST;
         if (!c.wait(B_KVFULL + vst, (vs / NST) & 1, 4)) return;
-        uint32_t va = c.sbase + SM_KV + vst * TILE_BYTES;
+        uint32_t va = c.sbase + L::KV + vst * L::TILE;
         uint32_t par = (it_base + j - 1) & 1;
         if (!c.wait(B_PFULL + 0, par, 5)) return;
         tc_fence_after();
-        issue_pv(tO0, tS0, va, j - 1 > 0);
-        issue_qk(tS0, q0, ka);
+        issue_pv<F8>(tO0, tS0, va, j - 1 > 0);
+        issue_qk<F8>(tS0, q0, ka);
         mma_commit(c.bar(B_SFULL + 0));
         if (!c.wait(B_PFULL + 1, par, 6)) return;
         tc_fence_after();
-        issue_pv(tO1, tS1, va, j - 1 > 0);
+        issue_pv<F8>(tO1, tS1, va, j - 1 > 0);
         mma_commit(c.bar(B_KVEMPTY + vst));
-        issue_qk(tS1, q1, ka);
+        issue_qk<F8>(tS1, q1, ka);
         mma_commit(c.bar(B_SFULL + 1));
         mma_commit(c.bar(B_KVEMPTY + kst));
     }
     uint32_t vs = seq + vseq(n - 1, n);
     int vst = vs % NST;
     if (!c.wait(B_KVFULL + vst, (vs / NST) & 1, 7)) return;
-    uint32_t va = c.sbase + SM_KV + vst * TILE_BYTES;
+    uint32_t va = c.sbase + L::KV + vst * L::TILE;
     uint32_t par = (it_base + n - 1) & 1;
     if (!c.wait(B_PFULL + 0, par, 8)) return;
     tc_fence_after();
-    issue_pv(tO0, tS0, va, n - 1 > 0);
+    issue_pv<F8>(tO0, tS0, va, n - 1 > 0);
     mma_commit(c.bar(B_ODONE + 0));
     if (!c.wait(B_PFULL + 1, par, 9)) return;
     tc_fence_after();
-    issue_pv(tO1, tS1, va, n - 1 > 0);
+    issue_pv<F8>(tO1, tS1, va, n - 1 > 0);
     mma_commit(c.bar(B_ODONE + 1));
     mma_commit(c.bar(B_KVEMPTY + vst));
 }
@@ -226,8 +288,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+// Two floats to e4m3 (round to nearest even, saturating): lo in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
 
-__device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const WfRoundDev &rd,
+template <bool F8>
+__device__ void softmax_tile(const Ctx<F8> &c, uint32_t tmem, const WfGeom &g, const WfRoundDev &rd,
                              const TcParams &p, int X, int ti, int h, int qp, int n,
                              uint32_t it_base, uint32_t unit_iter) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -283,6 +350,7 @@ __device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t negm2 = f2_pack(-m_run, -m_run);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // P for the PV MMA: bf16 pairs (64 TMEM columns) or e4m3 quads (32)
         uint32_t pk[2][32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -294,7 +362,13 @@ __device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const
                 f2_unpack(x, a0, a1);
                 const float p0 = ex2(a0), p1 = ex2(a1);
                 acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                pk[q >> 1][(q & 1) * 16 + i] = pack_bf16(p0, p1);
+                if constexpr (F8) {
+                    const uint32_t h = pack_e4m3x2(p0, p1);
+                    uint32_t &w = pk[0][q * 8 + (i >> 1)];
+                    w = (i & 1) ? (w | (h << 16)) : h;
+                } else {
+                    pk[q >> 1][(q & 1) * 16 + i] = pack_bf16(p0, p1);
+                }
             }
         }
         float s0, s1, s2, s3;
@@ -314,7 +388,7 @@ __device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const
             }
         }
         tmem_st32(tS + 0, pk[0]);
-        tmem_st32(tS + 32, pk[1]);
+        if (!F8) tmem_st32(tS + 32, pk[1]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(c.bar(B_PFULL + X));
@@ -324,7 +398,7 @@ __device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const
     if (!__all_sync(0xffffffffu, ok)) return;
     tc_fence_after();
     const int qrow = (2 * qp + X) * BM + row;
-    const float inv = 1.f / l_run;
+    const float inv = p.o_scale / l_run;
     __nv_bfloat16 *dst = p.out + (((size_t)rd.slot[ti] * g.NC + qrow) * g.H + h) * HD;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -346,6 +420,7 @@ __device__ void softmax_tile(const Ctx &c, uint32_t tmem, const WfGeom &g, const
     }
 }
 
+template <bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
                    const WfGeom g, const WfRoundDev rd, const TcParams p) {
@@ -353,11 +428,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
-    Ctx c;
+    constexpr uint32_t MISC = LayMisc<F8>::MISC;
+    Ctx<F8> c;
     c.sbase = raw_u32 + pad;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM_MISC);
-    int *unit_slot = reinterpret_cast<int *>(smem + SM_MISC + 8);
-    c.abort = reinterpret_cast<volatile int *>(smem + SM_MISC + 16);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC);
+    int *unit_slot = reinterpret_cast<int *>(smem + MISC + 8);
+    c.abort = reinterpret_cast<volatile int *>(smem + MISC + 16);
     c.status = p.ctl + WF_SCRATCH_STATUS / 4;
     c.where = p.ctl + WF_SCRATCH_WHERE / 4;
     uint32_t *work = p.ctl + WF_SCRATCH_WORK / 4;
@@ -414,7 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int ti, h, qp;
             decode_unit(u, rd, p, g.H, ti, h, qp);
             const int n = rd.n_ctx[ti] * p.tpc;
-            softmax_tile(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
+            softmax_tile<F8>(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
             u = next_unit(n);
         }
     } else {
@@ -424,9 +500,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_unit(u, rd, p, g.H, ti, h, qp);
             const int n = rd.n_ctx[ti] * p.tpc;
             if (warp == 8 && lane == 0)
-                producer(c, &tq, &tkv, g, rd, p, ti, h, qp, n, seq, &issued);
+                producer<F8>(c, &tq, &tkv, g, rd, p, ti, h, qp, n, seq, &issued);
             else if (warp == 9 && lane == 0)
-                mma_issuer(c, tmem, n, seq, it_base, unit_iter);
+                mma_issuer<F8>(c, tmem, n, seq, it_base, unit_iter);
             u = next_unit(n);
         }
     }
@@ -464,19 +540,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // Opt in to the shared-memory size and refuse to launch unless the kernel was
 // compiled to exactly the register count the setmaxnreg split assumes.
+template <bool F8>
 cudaError_t prepare_kernel() {
+    static bool done = false;
+    if (done) return cudaSuccess;
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<F8>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SM_ALLOC);
+    e = cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LayMisc<F8>::ALLOC);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
+// Parameters and launch of one round's attention (ctl: the control words).
+cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const WfTmaps &maps,
+                      void *out, uint32_t *ctl, int num_sms, cudaStream_t stream) {
+    const bool f8 = g.dtype == WF_FP8;
+    cudaError_t e = f8 ? prepare_kernel<true>() : prepare_kernel<false>();
+    if (e != cudaSuccess) return e;
+    TcParams p;
+    p.layer = layer;
+    p.tpc = (g.NC + BN - 1) / BN;
+    p.qpairs = ((g.NC + BM - 1) / BM + 1) / 2;
+    p.n_units = rd.n_tasks * g.H * p.qpairs;
+    p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
+    p.o_scale = 1.f;
+    if (f8) {
+        p.sl2 /= g.qk_scale * g.qk_scale;
+        p.o_scale = 1.f / g.v_scale;
+    }
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ctl = ctl;
+    int grid = p.n_units < num_sms ? p.n_units : num_sms;
+    if (f8)
+        attn_tc_kernel<true><<<grid, NUM_THREADS, LayMisc<true>::ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
+    else
+        attn_tc_kernel<false><<<grid, NUM_THREADS, LayMisc<false>::ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 bool wf_attn_tc_supported(const WfGeom &g, int dtype) {
-    return dtype == WF_BF16 && g.D == HD;
+    return (dtype == WF_BF16 || dtype == WF_FP8) && g.D == HD;
 }
 
 cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out) {
@@ -494,16 +602,21 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
             return cudaErrorUnknown;
         encode = reinterpret_cast<EncodeFn>(fn);
     }
-    const cuuint32_t box[3] = {64, 128, 1};
+    // bf16: 64-element (128-byte) boxes, two per 128-wide tile; e4m3: one
+    // 128-element (128-byte) box
+    const bool f8 = g.dtype == WF_FP8;
+    const cuuint64_t es = f8 ? 1 : 2;
+    const CUtensorMapDataType ty = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint32_t box[3] = {f8 ? 128u : 64u, 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)g.NC * HD * 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)HD * es, (cuuint64_t)g.NC * HD * es};
     cuuint64_t dq[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)(g.S + 1) * g.H};
-    if (encode(&out->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qbuf, dq, strides, box, estr,
+    if (encode(&out->q, ty, 3, qbuf, dq, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     cuuint64_t dk[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)g.P * g.L * 2 * g.H};
-    if (encode(&out->kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool, dk, strides, box, estr,
+    if (encode(&out->kv, ty, 3, pool, dk, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -514,23 +627,7 @@ cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
                               cudaStream_t stream) {
     if (rd.n_tasks < 1) return cudaSuccess;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = prepare_kernel();
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    TcParams p;
-    p.layer = layer;
-    p.tpc = (g.NC + BN - 1) / BN;
-    p.qpairs = ((g.NC + BM - 1) / BM + 1) / 2;
-    p.n_units = rd.n_tasks * g.H * p.qpairs;
-    p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.ctl = static_cast<uint32_t *>(scratch);
-    int grid = p.n_units < num_sms ? p.n_units : num_sms;
-    attn_tc_kernel<<<grid, NUM_THREADS, SM_ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
-    return cudaGetLastError();
+    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(scratch), num_sms, stream);
 }
 
 // ---- launch without caller scratch ------------------------------------------
@@ -581,21 +678,5 @@ cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int
     if (rd.n_tasks < 1) return cudaSuccess;
     e = cudaMemsetAsync(ctl, 0, need, stream);
     if (e != cudaSuccess) return e;
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = prepare_kernel();
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    TcParams p;
-    p.layer = layer;
-    p.tpc = (g.NC + BN - 1) / BN;
-    p.qpairs = ((g.NC + BM - 1) / BM + 1) / 2;
-    p.n_units = rd.n_tasks * g.H * p.qpairs;
-    p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.ctl = static_cast<uint32_t *>(ctl);
-    int grid = p.n_units < num_sms ? p.n_units : num_sms;
-    attn_tc_kernel<<<grid, NUM_THREADS, SM_ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
-    return cudaGetLastError();
+    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(ctl), num_sms, stream);
 }

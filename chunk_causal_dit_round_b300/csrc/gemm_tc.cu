@@ -124,34 +124,8 @@ struct Epi<WF_EPI_F32> {
         for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
 };
-// out (f32) += gate[group(row)][col] * (acc + bias): the gated residual add of
-// the attention and FFN halves of a block; group = the row's task slot.
-template <>
-struct Epi<WF_EPI_GATED_RESIDUAL> {
-    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
-        const int grp = row / p.rows_per_group;
-        const float4 *g4 = reinterpret_cast<const float4 *>(p.gate + (size_t)grp * p.gate_ld + col);
-        float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)row * p.ldo + col);
-        // all loads first: the stores below could alias them as far as the
-        // compiler knows, which would serialise eight round trips
-        float4 xs[8], gs[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            xs[q] = d4[q];
-            gs[q] = __ldg(g4 + q);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 g = gs[q];
-            float4 x = xs[q];
-            x.x = fmaf(g.x, v[4 * q], x.x);
-            x.y = fmaf(g.y, v[4 * q + 1], x.y);
-            x.z = fmaf(g.z, v[4 * q + 2], x.z);
-            x.w = fmaf(g.w, v[4 * q + 3], x.w);
-            d4[q] = x;
-        }
-    }
-};
+// The gated residual add x += gate[group(row)][col] * (acc + bias) of the
+// attention and FFN halves of a block runs through residual_staged below.
 
 // QKV projection epilogue: columns [0, dim) are Q, [dim, 2 dim) K, [2 dim,
 // 3 dim) V, head h at columns h*D .. h*D + D - 1 of each part.  RoPE on Q and

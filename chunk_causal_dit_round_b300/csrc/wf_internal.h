@@ -22,6 +22,8 @@ struct WfGeom {
     int dt2, dh2, dw2;         // rotary pairs of the t / h / w parts
     int t_max;                 // rows of the temporal table (absolute frames)
     int rope_t_off, rope_h_off, rope_w_off;  // float2 offsets of the tables in scratch
+    int dtype;                 // WF_FP32 / WF_BF16 / WF_FP8 (storage of Q and the K/V pages)
+    float qk_scale, v_scale;   // e4m3 storage: Q, K (resp. V) multiplied by these before rounding
 };
 
 // One round as the kernels see it (host-built in wf_round_step).

@@ -25,7 +25,10 @@ using namespace wfimpl;
 
 namespace {
 
+// bytes of one element of the Q/K/V input and attention output, and of the
+// query workspace and page pool
 size_t elem_size(int dtype) { return dtype == WF_FP32 ? 4 : 2; }
+size_t page_elem_size(int dtype) { return dtype == WF_FP32 ? 4 : (dtype == WF_FP8 ? 1 : 2); }
 
 bool mul_ok(size_t a, size_t b, size_t *out) {
     if (a != 0 && b > SIZE_MAX / a) return false;
@@ -229,6 +232,8 @@ void wf_plan_opts_default(wf_plan_opts *o) {
     o->rope_theta = 10000.0;
     o->mask = WF_MASK_WF;
     o->schedule = WF_SCHED_WAVEFRONT;
+    o->fp8_qk_scale = 1.0;
+    o->fp8_v_scale = 1.0;
 }
 
 int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks,
@@ -242,7 +247,11 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
     if (head_dim > 256) return WF_ERANGE;
     if (history_chunks < -1) return WF_EINVAL;
     if (o.n_chunks < 1 || o.layers < 1) return WF_ERANGE;
-    if (o.dtype != WF_FP32 && o.dtype != WF_BF16) return WF_EINVAL;
+    if (o.dtype != WF_FP32 && o.dtype != WF_BF16 && o.dtype != WF_FP8) return WF_EINVAL;
+    if (o.dtype == WF_FP8 &&
+        (!(o.fp8_qk_scale > 0.0) || !std::isfinite(o.fp8_qk_scale) || !(o.fp8_v_scale > 0.0) ||
+         !std::isfinite(o.fp8_v_scale)))
+        return WF_EINVAL;
     if (o.anchor_mode != WF_ANCHOR_ADJACENT && o.anchor_mode != WF_ANCHOR_ABSOLUTE) return WF_EINVAL;
     if (o.use_anchor != 0 && o.use_anchor != 1) return WF_EINVAL;
     if (!(o.rope_theta > 1.0) || !std::isfinite(o.rope_theta)) return WF_EINVAL;
@@ -274,6 +283,9 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
     g.S = S; g.NC = chunk_tokens; g.H = heads; g.D = head_dim; g.L = o.layers;
     g.gt = o.grid_t; g.gh = o.grid_h; g.gw = o.grid_w;
     g.P = P; g.raw_anchor_page = 1 + R + S;
+    g.dtype = o.dtype;
+    g.qk_scale = (float)o.fp8_qk_scale;
+    g.v_scale = (float)o.fp8_v_scale;
     int q6 = head_dim / 6;
     g.dt2 = (head_dim - 4 * q6) / 2; g.dh2 = q6; g.dw2 = q6;
     g.t_max = o.grid_t * o.n_chunks;
@@ -289,15 +301,16 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
 
 int wf_plan_buffer_sizes(wf_plan_t p, wf_buffer_sizes *out) {
     if (!p || !out) return WF_EINVAL;
-    size_t es = elem_size(p->o.dtype);
-    size_t tok = (size_t)p->NC * p->H * p->D * es;  // one slot, one of Q/K/V
+    const size_t elems = (size_t)p->NC * p->H * p->D;  // one slot, one of Q/K/V
+    size_t tok = elems * elem_size(p->o.dtype);
+    size_t ptok = elems * page_elem_size(p->o.dtype);
     size_t slots = (size_t)p->S + 1;
     size_t a, b;
     std::memset(out, 0, sizeof(*out));
     if (!mul_ok(tok, slots * 3, &out->qkv)) return WF_ERANGE;
-    out->qbuf = tok * slots;
+    out->qbuf = ptok * slots;
     out->out = tok * slots;
-    if (!mul_ok(tok, (size_t)p->P * p->o.layers, &a) || !mul_ok(a, 2, &b)) return WF_ERANGE;
+    if (!mul_ok(ptok, (size_t)p->P * p->o.layers, &a) || !mul_ok(a, 2, &b)) return WF_ERANGE;
     out->pool = b;
     out->scratch = WF_SCRATCH_TABLES + tables_bytes(p->g);
     out->n_pages = p->P;
@@ -434,7 +447,7 @@ int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream
     if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
     if (p->published[layer] != p->k) return WF_EORDER;
     bool tc_ok = p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype);
-    bool simt_ok = p->D % 32 == 0 && p->D <= 128;
+    bool simt_ok = p->D % 32 == 0 && p->D <= 128 && p->o.dtype != WF_FP8;
     if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
     cudaError_t e;
     if (kernel == WF_ATTN_TC) {

@@ -23,7 +23,8 @@
  *    the task at denoising stage s, slot S the store task.  Slots of inactive
  *    stages (pipeline fill/drain) are neither read nor written.
  *  - Element type of every activation buffer is the plan's dtype
- *    (WF_BF16: bfloat16, WF_FP32: float).
+ *    (WF_BF16: bfloat16, WF_FP32: float); with WF_FP8 the query workspace
+ *    and the page pool hold e4m3 bytes while qkv and out are bfloat16.
  *
  * Layouts (row-major, innermost last; N_C = chunk_tokens, H = heads,
  * D = head_dim, L = layers, P = n_pages from wf_plan_buffer_sizes):
@@ -61,6 +62,11 @@ typedef struct CUstream_st *cudaStream_t; /* identical to CUDA's own typedef */
 
 #define WF_FP32 0
 #define WF_BF16 1
+#define WF_FP8  2  /* 8-bit attention: Q and the K/V pages stored as OCP FP8 e4m3 (1 byte;
+                      Q and K multiplied by fp8_qk_scale, V by fp8_v_scale before rounding,
+                      saturating at +-448); Q/K/V input and attention output stay bf16;
+                      tensor-core attention only (the pages' 8-bit SageAttention backend
+                      and FP8 K/V payload, Sec. 5 and App. C.6) */
 
 #define WF_ANCHOR_ADJACENT 0 /* anchor re-rotated just before the oldest retained chunk */
 #define WF_ANCHOR_ABSOLUTE 1 /* anchor keeps its own position (frames 0..grid_t-1) */
@@ -103,6 +109,8 @@ typedef struct wf_plan_opts {
     double rope_theta;  /* RoPE base, default 10000 */
     int mask;           /* WF_MASK_WF (default) or WF_MASK_RF */
     int schedule;       /* WF_SCHED_WAVEFRONT (default) or WF_SCHED_SEQUENTIAL */
+    double fp8_qk_scale;  /* WF_FP8: scale of Q and K before e4m3 rounding (default 1) */
+    double fp8_v_scale;   /* WF_FP8: scale of V before e4m3 rounding (default 1) */
 } wf_plan_opts;
 
 typedef struct wf_buffer_sizes {

@@ -10,8 +10,8 @@ from oracle import schedule as sch
 from oracle.round import Geom
 
 
-def make_round(cfg: sch.Cfg, geom: Geom, dtype, layers=1):
-    return wf.Round(cfg.S, geom.chunk_tokens, geom.heads, geom.head_dim, cfg.history,
+def make_round(cfg: sch.Cfg, geom: Geom, dtype, layers=1, fp8_scales=(1.0, 1.0)):
+    return wf.Round(cfg.S, geom.chunk_tokens, geom.heads, geom.head_dim, cfg.history, fp8_scales=fp8_scales,
                     n_chunks=cfg.n_chunks, layers=layers, grid=geom.grid, dtype=dtype,
                     use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode,
                     rope_theta=geom.theta, mask=cfg.mask,

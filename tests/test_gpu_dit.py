@@ -212,3 +212,46 @@ def test_wan13_linears_sampled_rows():
         del a, w, out
     assert r.sync_status() == wf.WF_OK
     r.close()
+
+
+def test_wan13_qkv_publish_sampled_rows():
+    """The fused QKV projection + RoPE + paged publication at the Wan2.1-1.3B
+    shape (dim 1536 -> 4608, 5 tasks of 4680 tokens) in a steady round,
+    checked on sampled tokens of every task against the fp64 oracle."""
+    cfg = sch.Cfg(4, 14, 3)
+    grid, H = (3, 30, 52), 12
+    NC, dim = 4680, 1536
+    r = new_round(cfg, grid, H, 1)
+    w = wf_synth.normal(wf_synth.key_of(41, 1), (3 * dim, dim), 0.02, torch.bfloat16)
+    b = wf_synth.normal(wf_synth.key_of(41, 2), (3 * dim,), 0.02, torch.bfloat16)
+    W, Bv = w.double().numpy(), b.double().numpy()
+    wd, bd = w.cuda(), b.cuda()
+    rows = np.array([0, 1, 127, 128, 2500, 4607, 4608, 4679])
+    k_check = cfg.S + cfg.history + 2
+    xs = {}
+    for k in range(k_check + 1):
+        info = r.step()
+        x = torch.empty((cfg.S + 1, NC, dim), dtype=torch.bfloat16)
+        for i in range(info.n_tasks):
+            c, s_ = info.task_chunk[i], info.task_stage[i]
+            xs[(c, s_)] = wf_synth.normal(wf_synth.key_of(41, 3, c, s_), (NC, dim), 1.0, torch.bfloat16)
+            x[s_] = xs[(c, s_)]
+        r.publish_proj(0, x.cuda(), wd, bd)
+    torch.cuda.synchronize()
+    assert r.sync_status() == wf.WF_OK
+    P = r.pool_view()
+    qb = r.qbuf.view(cfg.S + 1, H, NC, 128)
+    t_idx = torch.from_numpy(rows).cuda()
+    for t in sch.round_tasks(cfg, k_check):
+        y = xs[(t.chunk, t.stage)][rows].double().numpy() @ W.T + Bv
+        q, kk, v = (y[:, i * dim:(i + 1) * dim].reshape(len(rows), H, 128) for i in range(3))
+        # RoPE of the sampled tokens at their (t, h, w) positions
+        pos = [p[rows] for p in orope.chunk_positions(t.chunk, *grid)]
+        ang = orope.pair_angles(128, 1e4, *pos)
+        qr, kr = orope.rotate(q, ang), orope.rotate(kk, ang)
+        got_q = qb[t.stage][:, t_idx].transpose(0, 1).double().cpu().numpy()
+        got_k = P[t.dest_page, 0, 0][:, t_idx].transpose(0, 1).double().cpu().numpy()
+        got_v = P[t.dest_page, 0, 1][:, t_idx].transpose(0, 1).double().cpu().numpy()
+        for g, ref in ((got_q, qr), (got_k, kr), (got_v, v)):
+            assert np.all(np.abs(g - ref) <= 2 ** -7 * np.abs(ref) + 1e-3), t.stage
+    r.close()

@@ -209,3 +209,31 @@ def test_bf16_extreme_scores(kernel):
     mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, kernel, seed=9, qk_scale=8.0,
                                  err=scaled_errors)
     assert np.isfinite(mx) and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
+
+
+def test_14b_shape_sampled_rows():
+    """14B-scale attention layer (40 heads x 128, S = 4, 4680-token chunks,
+    W = 3) in a steady round with anchor re-rotation, TC kernel, against the
+    oracle on sampled query rows of 3 heads (first, middle, last)."""
+    cfg = sch.Cfg(4, 12, 3)
+    geom = Geom(3, 30, 52, 40, 128)
+    heads = [0, 19, 39]
+    s = 1.0 / np.sqrt(128)
+    r = make_round(cfg, geom, wf.WF_BF16)
+    raw, traw = raw_fn(23, geom, torch.bfloat16, qk_scale=4 * s, v_scale=1.0, heads=heads)
+    out = r.new_out()
+    k_check = cfg.S + cfg.history + 2
+    for k in range(k_check + 1):
+        info = r.step()
+        r.publish(0, fill_qkv(r, info, traw, 0))
+    r.attention(0, out, wf.WF_ATTN_TC)
+    torch.cuda.synchronize()
+    assert r.sync_status() == wf.WF_OK
+    rows = [0, 127, 128, 2345, 4607, 4608, 4679]
+    geom_h = Geom(3, 30, 52, len(heads), 128)
+    ref = round_attention(cfg, geom_h, k_check, 0, raw, rows=rows, qk_dtype="bf16")
+    for t, o in zip(sch.round_tasks(cfg, k_check), ref):
+        g = out[t.stage][rows][:, heads].float().cpu().numpy()
+        mx, mean, rel = errors(g, o)
+        assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (t.stage, mx, mean, rel)
+    r.close()
