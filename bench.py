@@ -44,6 +44,9 @@ CONFIGS = {
     "wan13_attn": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3,
                        desc="Wan2.1-1.3B attention layer, S=4 (5 tasks/round), 4680-token chunks, "
                             "12x128 heads, W=3 + anchor, bf16"),
+    "wan13_attn_fp8": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, fp8=(8.0, 8.0),
+                           desc="the same round with 8-bit attention: Q and K/V pages in e4m3 "
+                                "(x8 scales), P in e4m3, bf16 Q/K/V input and output"),
 }
 
 
@@ -57,6 +60,10 @@ DIT_CONFIGS = {
                      layers=30, n_chunks=135, steps=[1000.0, 800.0, 600.0, 400.0, 200.0],
                      desc="long rollout, 5-step (S=5), same 1.3B shapes, 135 chunks, paged K/V "
                           "ring with oldest-chunk eviction, W=3 + anchor"),
+    "dit13_fp8": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
+                      layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], fp8=(4.0, 4.0),
+                      desc="as dit13 with 8-bit attention: e4m3 Q and K/V pages (x4 scales), "
+                           "e4m3 P; linear layers bf16"),
     # comparison graphs on the same model and kernels
     "dit13_rf": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
                      layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], mask=1,
@@ -194,8 +201,9 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     per_step = S + 1 if seq else 1          # rounds (forward passes) per completed chunk
     k_steady = (W + 2) * (S + 1) if seq else S + W + 2
     n_chunks = max(cfg["n_chunks"], (k_steady // per_step) + warmup + steps + 4)
-    r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16,
-                 mask=cfg.get("mask", 0),
+    r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"],
+                 dtype=wf.WF_FP8 if cfg.get("fp8") else wf.WF_BF16,
+                 fp8_scales=cfg.get("fp8") or (1.0, 1.0), mask=cfg.get("mask", 0),
                  schedule=wf.WF_SCHED_SEQUENTIAL if seq else wf.WF_SCHED_WAVEFRONT)
     g = torch.Generator(device=dev)
     g.manual_seed(4321 + rank)
@@ -218,9 +226,12 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     chunk = torch.empty(latent, device=dev)
     stream = torch.cuda.current_stream()
 
+    attn_total = [0.0]
+
     def round_flops(info):
         T = info.n_tasks * NC
         lin = 2.0 * T * (3 * dim * dim + dim * dim + 2 * dim * ffn) * L
+        attn_total[0] += info.attn_flops * L
         return info.attn_flops * L + lin + 2.0 * T * (4 * C) * dim * 2
 
     i = 0
@@ -285,6 +296,13 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     ms, e2e_ms = max_over_ranks([t0.elapsed_time(t1), e0.elapsed_time(e1)], world, dev)
     chunks_s = world * steps / (ms * 1e-3)
     peak, src = _sustained_peak()
+    peak_kind = "bf16 dense (sustained)"
+    if cfg.get("fp8"):
+        # attention runs on the e4m3 pipe (2 x bf16 nominal), the linears on
+        # bf16: the bound is the time both would take at their own peaks
+        fa = attn_total[0]                       # attention FLOPs of the timed rounds
+        t_min = fa / (2 * peak) + (flops - fa) / peak
+        peak, peak_kind = flops / t_min, "attention at 2 x and linears at 1 x measured bf16 (sustained)"
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L, "value": round(chunks_s, 3),
            "unit": "chunks/s", "forwards_per_chunk_timed": per_step,
@@ -296,9 +314,9 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
            "chunks_timed": steps,
            "eta_slot": round(1 / (S + 1) if seq else cfg["n_chunks"] / (cfg["n_chunks"] + S), 4),
            "flops_per_round": flops / steps,
-           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak, 1),
                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
-                        "peak_source": f"{src} bf16 dense (sustained)"},
+                        "peak_source": f"{src} {peak_kind}"},
            "gpu_launches": launches, "clocks": clk.summary()}
     del model, r, P
     torch.cuda.empty_cache()
@@ -374,10 +392,10 @@ class ClockSampler:
 
 
 def steady_plan(wf, cfg, n_chunks):
-    import torch
-    r = wf.Round(cfg["S"], math.prod(cfg["grid"]), cfg["heads"], cfg["head_dim"], cfg["history"],
-                 n_chunks=n_chunks, layers=1, grid=cfg["grid"], dtype=wf.WF_BF16)
-    return r
+    fp8 = cfg.get("fp8")
+    return wf.Round(cfg["S"], math.prod(cfg["grid"]), cfg["heads"], cfg["head_dim"], cfg["history"],
+                    n_chunks=n_chunks, layers=1, grid=cfg["grid"],
+                    dtype=wf.WF_FP8 if fp8 else wf.WF_BF16, fp8_scales=fp8 or (1.0, 1.0))
 
 
 def run_ours(args, rank, world):
@@ -498,6 +516,11 @@ def run_ours(args, rank, world):
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
     peak_tf, hbm, peak_src = _peaks()
+    fp8 = bool(cfg.get("fp8"))
+    peak_kind = "bf16 dense (burst)"
+    if fp8:
+        # e4m3 tensor peak: the measured bf16 peak times the nominal 4.5 / 2.25 ratio
+        peak_tf, peak_kind = 2.0 * peak_tf, "e4m3 dense (burst) = 2 x measured bf16"
     attn_avg = statistics.mean(attn_ms)
     per_launch = flops / args.steps
     achieved = per_launch / (attn_avg * 1e-3) / 1e12
@@ -513,7 +536,7 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1)/sqrt(128) Q/K/V, device-resident ring of 3 rounds)",
         "config": {"workload": args.config, "desc": cfg["desc"], "S": S, "chunk_tokens": NC,
                    "heads": H, "head_dim": D, "history_chunks": W, "n_chunks": n_chunks,
@@ -528,9 +551,10 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel",
                      "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4),
-                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "peak_source": f"{peak_src} {peak_kind}",
                      "avg_launch_ms": round(attn_avg, 4),
-                     "flops_per_launch": per_launch, "traffic": ATTN_TC_TRAFFIC_BYTES},
+                     "flops_per_launch": per_launch,
+                     "traffic": None if fp8 else ATTN_TC_TRAFFIC_BYTES},
         "clocks": clocks,
     }
     return res

@@ -74,7 +74,7 @@ int wf_qkv_proj_rope_publish(wf_plan_t p, int layer, const void *x, const void *
     if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
     if (!x || !w_qkv || !aligned16(x) || !aligned16(w_qkv) || (b_qkv && !aligned16(b_qkv)))
         return WF_EINVAL;
-    if (p->o.dtype != WF_BF16) return WF_EUNSUPPORTED;
+    if (p->o.dtype != WF_BF16 && p->o.dtype != WF_FP8) return WF_EUNSUPPORTED;
     const int dim = p->H * p->D;
     if (dim % 64 || p->D % 32) return WF_EUNSUPPORTED;
     return wf_publish_impl(p, layer, x, w_qkv, b_qkv, nullptr, stream);
@@ -95,7 +95,7 @@ int wf_dit_workspace_size(wf_plan_t p, int model_dim, int ffn_dim, int channels,
 int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_t stream) {
     if (!p || !m || !workspace) return WF_EINVAL;
     if (!p->bound) return WF_EUNBOUND;
-    if (p->o.dtype != WF_BF16 || p->D != 128) return WF_EUNSUPPORTED;
+    if ((p->o.dtype != WF_BF16 && p->o.dtype != WF_FP8) || p->D != 128) return WF_EUNSUPPORTED;
     if ((uintptr_t)workspace & 255) return WF_EINVAL;
     size_t need;
     int rc = wf_dit_workspace_size(p, m->model_dim, m->ffn_dim, m->channels, m->freq_dim, &need);

@@ -27,6 +27,7 @@
 // returns.
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "wf_internal.h"
 #include "wf_ptx.cuh"
@@ -131,7 +132,8 @@ struct Epi<WF_EPI_F32> {
 // 3 dim) V, head h at columns h*D .. h*D + D - 1 of each part.  RoPE on Q and
 // K at the token's absolute (t, h, w); Q -> qbuf[slot][h][n][:], K/V ->
 // pool[dest page][layer][K|V][h][n][:]; the store of the anchor also keeps
-// its unrotated key on the raw-anchor page (App. B.3).
+// its unrotated key on the raw-anchor page (App. B.3).  WF_FP8 plans store
+// e4m3 (Q and K times qk_scale, V times v_scale) instead of bf16.
 template <>
 struct Epi<WF_EPI_QKV_PUBLISH> {
     __device__ static void store32(__nv_bfloat16 *dst, const float (&v)[32]) {
@@ -140,6 +142,34 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
         for (int q = 0; q < 4; ++q)
             d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
                                pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    }
+    // e4m3 pages (WF_FP8 plans): 32 values times scale, rounded, 32 bytes
+    __device__ static void store32_e4m3(uint8_t *dst, const float (&v)[32], float scale) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * scale, v[4 * i + 1] * scale),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * scale, v[4 * i + 3] * scale),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            w[i] = lo | (hi << 16);
+        }
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    // one row of one head's 32 channels into a page plane or the query workspace
+    __device__ static void put(const GemmParams &p, size_t off, const float (&v)[32], float scale) {
+        if (p.g.dtype == WF_FP8)
+            store32_e4m3(reinterpret_cast<uint8_t *>(p.pool) + off, v, scale);
+        else
+            store32(p.pool + off, v);
+    }
+    __device__ static void putq(const GemmParams &p, size_t off, const float (&v)[32], float scale) {
+        if (p.g.dtype == WF_FP8)
+            store32_e4m3(reinterpret_cast<uint8_t *>(p.qbuf) + off, v, scale);
+        else
+            store32(p.qbuf + off, v);
     }
     __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
         const WfGeom &g = p.g;
@@ -154,12 +184,12 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
         const size_t plane = (size_t)g.NC * g.D;
         if (part == 2) {
             size_t kvp = (((size_t)p.rd.dest[ti] * g.L + p.layer) * 2 + 1) * g.H + h;
-            store32(p.pool + kvp * plane + (size_t)n * g.D + d0, v);
+            put(p, kvp * plane + (size_t)n * g.D + d0, v, g.v_scale);
             return;
         }
         if (part == 1 && ti == p.rd.raw_copy_task) {
             size_t rawp = (((size_t)g.raw_anchor_page * g.L + p.layer) * 2) * g.H + h;
-            store32(p.pool + rawp * plane + (size_t)n * g.D + d0, v);
+            put(p, rawp * plane + (size_t)n * g.D + d0, v, g.qk_scale);
         }
         const int hw = g.gh * g.gw;
         const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n - (n / g.gw) * g.gw;
@@ -180,10 +210,10 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
             v[2 * i + 1] = a * cs.y + b * cs.x;
         }
         if (part == 0) {
-            store32(p.qbuf + ((size_t)slot * g.H + h) * plane + (size_t)n * g.D + d0, v);
+            putq(p, ((size_t)slot * g.H + h) * plane + (size_t)n * g.D + d0, v, g.qk_scale);
         } else {
             size_t kp = (((size_t)p.rd.dest[ti] * g.L + p.layer) * 2) * g.H + h;
-            store32(p.pool + kp * plane + (size_t)n * g.D + d0, v);
+            put(p, kp * plane + (size_t)n * g.D + d0, v, g.qk_scale);
         }
     }
 };

@@ -264,8 +264,8 @@ int wf_linear(wf_plan_t plan, const void *a, long long a_rows, int lda, int row_
  *   w_qkv  bf16 [3 dim][dim]: rows 0..dim-1 produce Q, then K, then V; head h
  *          of each part is rows h*head_dim .. h*head_dim + head_dim - 1
  *   b_qkv  bf16 [3 dim] or NULL
- * bf16 plans only, dim % 64 == 0, head_dim % 32 == 0.  Errors: as
- * wf_qkv_rope_publish, plus WF_EUNSUPPORTED. */
+ * bf16 or WF_FP8 plans (e4m3 pages), dim % 64 == 0, head_dim % 32 == 0.
+ * Errors: as wf_qkv_rope_publish, plus WF_EUNSUPPORTED. */
 int wf_qkv_proj_rope_publish(wf_plan_t plan, int layer, const void *x, const void *w_qkv,
                              const void *b_qkv, cudaStream_t stream);
 
@@ -315,7 +315,8 @@ int wf_dit_workspace_size(wf_plan_t plan, int model_dim, int ffn_dim, int channe
                           size_t *bytes);
 
 /* Attach a model and a caller-owned workspace (256-byte aligned, size from
- * wf_dit_workspace_size) to a bound bf16 plan with head_dim 128.  The weight
+ * wf_dit_workspace_size) to a bound bf16 or WF_FP8 plan with head_dim 128
+ * (WF_FP8: attention in e4m3, every other tensor as in the bf16 plan).  The weight
  * pointers are kept (not copied): they must stay valid while the plan is
  * used.  Computes the timestep embeddings and modulation tables of every
  * slot on `stream` (each stage has a fixed timestep) and clears the latent

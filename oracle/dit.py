@@ -41,6 +41,10 @@ in the design notes:
   matching; Psi_0 = identity as Eq. 1 requires);
 * the store pass uses context_noise = 0 (App. B.3 leaves the value open).
 
+``kv_fp8=(qk_scale, v_scale)`` stores the RoPE'd Q and K and V (and the
+anchor's unrotated key) as e4m3 after scaling instead of bf16 (8-bit
+attention, the pages' SageAttention backend and FP8 K/V payload).
+
 ``bf16=True`` rounds to bfloat16 where a BF16 execution (App. B.1) stores a
 tensor: the latent patches, every linear layer's input (normalised
 activations, attention output, FFN hidden), the RoPE-applied Q/K and V that
@@ -191,12 +195,13 @@ class Model:
     k; state (latent slot inputs, K/V of stored chunks) carries over."""
 
     def __init__(self, cfg: sch.Cfg, grid, dims: Dims, w: Weights, timesteps,
-                 shift=5.0, context_noise=0.0, theta=10000.0, bf16_points=True):
+                 shift=5.0, context_noise=0.0, theta=10000.0, bf16_points=True, kv_fp8=None):
         assert len(timesteps) == cfg.S
         self.cfg, self.grid, self.d, self.w = cfg, tuple(grid), dims, w
         self.nu = list(timesteps) + [0.0]          # nu_0 > ... > nu_{S-1} > nu_S = 0
         self.shift, self.theta = shift, theta
         self.rb = bf16 if bf16_points else (lambda x: np.asarray(x, np.float64))
+        self.kv_fp8 = kv_fp8
         # model timestep of each slot: stage s -> warped nu_s; the store -> context_noise
         self.slot_t = [1000.0 * warp_sigma(nu, shift) for nu in timesteps]
         self.slot_t.append(1000.0 * warp_sigma(context_noise, shift))
@@ -217,6 +222,10 @@ class Model:
         y = xa @ w.qkv_w[layer].T + w.qkv_b[layer]
         q, k, v = (y[:, i * d.dim:(i + 1) * d.dim].reshape(-1, d.heads, d.head_dim) for i in range(3))
         ang = self.angles(chunk)
+        if self.kv_fp8 is not None:
+            from .round import e4m3
+            sqk, sv = self.kv_fp8
+            return (e4m3(rotate(q, ang), sqk), e4m3(rotate(k, ang), sqk), e4m3(v, sv), e4m3(k, sqk))
         return self.rb(rotate(q, ang)), self.rb(rotate(k, ang)), self.rb(v), self.rb(k)
 
     def angles(self, tpos):
@@ -241,9 +250,14 @@ class Model:
 
     def cached_kv(self, e: sch.Entry, layer):
         k_rot, v, k_raw = self.cache[e.chunk][layer]
-        if e.kind == sch.KIND_ANCHOR:
-            # the anchor's key is re-rotated from its unrotated copy (App. B.3)
-            return self.rb(rotate(k_raw, self.angles(e.tpos))), v
+        if e.kind == sch.KIND_ANCHOR and e.tpos != e.chunk:
+            # once the window has moved, the anchor's key is re-rotated from
+            # its stored unrotated copy (App. B.3)
+            k = rotate(k_raw, self.angles(e.tpos))
+            if self.kv_fp8 is not None:
+                from .round import e4m3
+                return e4m3(k, self.kv_fp8[0]), v
+            return self.rb(k), v
         return k_rot, v
 
     # -- inputs of a round ---------------------------------------------------------

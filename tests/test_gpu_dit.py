@@ -33,9 +33,10 @@ SHARP_STD = 0.05
 SHARP_MAX, SHARP_MEAN, SHARP_REL = 5e-2, 4e-3, 1e-2
 
 
-def new_round(cfg, grid, heads, layers):
+def new_round(cfg, grid, heads, layers, fp8=None):
     return wf.Round(cfg.S, grid[0] * grid[1] * grid[2], heads, 128, cfg.history,
-                    n_chunks=cfg.n_chunks, layers=layers, grid=grid, dtype=wf.WF_BF16,
+                    n_chunks=cfg.n_chunks, layers=layers, grid=grid,
+                    dtype=wf.WF_FP8 if fp8 else wf.WF_BF16, fp8_scales=fp8 or (1.0, 1.0),
                     use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode, mask=cfg.mask,
                     schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
 
@@ -95,11 +96,12 @@ def test_qkv_projection_publish_matches_oracle():
 
 # ---- whole rounds ---------------------------------------------------------------------
 
-def run_request(cfg, grid, heads, dims, std, seed, steps):
+def run_request(cfg, grid, heads, dims, std, seed, steps, fp8=None):
     params = wf_synth.dit_params(seed, dims.dim, dims.ffn, dims.layers, dims.channels, dims.freq,
                                  std=std)
-    oracle = dit.Model(cfg, grid, dims, dit.weights_from(params), steps, bf16_points=True)
-    r = new_round(cfg, grid, heads, dims.layers)
+    oracle = dit.Model(cfg, grid, dims, dit.weights_from(params), steps, bf16_points=True,
+                       kv_fp8=fp8)
+    r = new_round(cfg, grid, heads, dims.layers, fp8)
     model = wf.Dit(r, params, ffn=dims.ffn, channels=dims.channels, freq=dims.freq,
                    timesteps=steps)
     C, F, Hl, Wl = dims.channels, grid[0], 2 * grid[1], 2 * grid[2]
@@ -254,4 +256,63 @@ def test_wan13_qkv_publish_sampled_rows():
         got_v = P[t.dest_page, 0, 1][:, t_idx].transpose(0, 1).double().cpu().numpy()
         for g, ref in ((got_q, qr), (got_k, kr), (got_v, v)):
             assert np.all(np.abs(g - ref) <= 2 ** -7 * np.abs(ref) + 1e-3), t.stage
+    r.close()
+
+
+
+# ---- 8-bit attention inside the DiT round ------------------------------------------
+
+FP8_REL, FP8_MEAN = 4e-2, 1.5e-2     # the e4m3 bars of tests/test_gpu_fp8.py
+
+
+def test_dit_request_fp8_attention():
+    """A WF_FP8 plan runs the same DiT round with e4m3 Q/K/V pages (written by
+    the QKV epilogue) and e4m3 attention; checked against the oracle with
+    the same e4m3 storage."""
+    cfg = sch.Cfg(4, 6, 3)
+    mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=0.02, seed=13,
+                                steps=[1000.0, 750.0, 500.0, 250.0], fp8=(4.0, 4.0))
+    assert np.isfinite(mx) and mean <= FP8_MEAN and rel <= FP8_REL, (mx, mean, rel)
+
+
+def test_qkv_projection_publish_fp8():
+    """The QKV epilogue's e4m3 pages: V, K and Q (after RoPE) within one e4m3
+    step of the oracle (fp32 vs fp64 before the rounding), the anchor's
+    unrotated key likewise."""
+    cfg = sch.Cfg(3, 7, 2)
+    grid, H = (3, 10, 10), 2
+    NC, dim = 300, 256
+    scales = (4.0, 2.0)
+    r = new_round(cfg, grid, H, 1, fp8=scales)
+    w = wf_synth.normal(wf_synth.key_of(33, 1), (3 * dim, dim), 0.05, torch.bfloat16)
+    b = wf_synth.normal(wf_synth.key_of(33, 2), (3 * dim,), 0.5, torch.bfloat16)
+    W, Bv = w.double().numpy(), b.double().numpy()
+    P = r.pool_view()
+    ys = {}
+
+    def x_of(c, s):
+        return wf_synth.normal(wf_synth.key_of(33, 3, c, s), (NC, dim), 1.0, torch.bfloat16)
+
+    def close(got, ref, scale):
+        g = got.float().cpu().double().numpy() / scale
+        return np.all(np.abs(g - ref) <= 2 ** -3 * np.abs(ref) + 2 ** -9 / scale)
+
+    for k in range(sch.n_rounds(cfg)):
+        info = r.step()
+        x = torch.zeros((cfg.S + 1, NC, dim), dtype=torch.bfloat16)
+        for i in range(info.n_tasks):
+            x[info.task_stage[i]] = x_of(info.task_chunk[i], info.task_stage[i])
+        r.publish_proj(0, x.cuda(), w.cuda(), b.cuda())
+        torch.cuda.synchronize()
+        qb = r.qbuf.view(cfg.S + 1, H, NC, 128)
+        for t in sch.round_tasks(cfg, k):
+            y = x_of(t.chunk, t.stage).double().numpy() @ W.T + Bv
+            q, kk, v = (y[:, i * dim:(i + 1) * dim].reshape(NC, H, 128) for i in range(3))
+            ys[(t.chunk, t.stage)] = kk
+            assert close(P[t.dest_page, 0, 1].transpose(0, 1), v, scales[1]), (k, t.stage)
+            assert close(P[t.dest_page, 0, 0].transpose(0, 1), orope.rope_chunk(kk, t.chunk, grid, 1e4), scales[0])
+            assert close(qb[t.stage].transpose(0, 1), orope.rope_chunk(q, t.chunk, grid, 1e4), scales[0])
+        if sch.anchor_present(cfg, k):
+            assert close(P[sch.raw_anchor_page(cfg), 0, 0].transpose(0, 1), ys[(0, cfg.S)], scales[0])
+    assert r.sync_status() == wf.WF_OK
     r.close()
