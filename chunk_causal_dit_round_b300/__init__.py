@@ -56,7 +56,7 @@ SYMBOLS = ["wf_plan_opts_default", "wf_plan", "wf_plan_buffer_sizes", "wf_bind",
            "wf_round_attention_noalloc", "wf_sync_status", "wf_plan_destroy", "wf_strerror",
            "wf_linear", "wf_qkv_proj_rope_publish", "wf_dit_workspace_size", "wf_dit_bind",
            "wf_dit_round", "wf_selftest_timeout", "wf_plan_state_size", "wf_plan_export_state",
-           "wf_plan_import_state"]
+           "wf_plan_import_state", "wf_quantize_weight_e4m3", "wf_linear_e4m3"]
 
 
 class wf_plan_opts(ctypes.Structure):
@@ -123,6 +123,9 @@ def _load():
         "wf_dit_bind": (I, [P, ctypes.POINTER(wf_dit_model), VP, VP]),
         "wf_dit_round": (I, [P, VP, VP, VP, VP, VP]),
         "wf_selftest_timeout": (I, [P, ctypes.c_uint, VP]),
+        "wf_quantize_weight_e4m3": (I, [P, VP, I, I, VP, VP, VP]),
+        "wf_linear_e4m3": (I, [P, VP, ctypes.c_longlong, I, I, I, VP, VP, VP, I, I, I, VP, I, VP, I, I,
+                               VP]),
         "wf_plan_state_size": (I, [P, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_plan_export_state": (I, [P, VP, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_plan_import_state": (I, [P, VP, ctypes.c_size_t]),
@@ -296,6 +299,26 @@ class Round:
     def selftest_timeout(self, limit_us=10000, stream=None):
         check(lib.wf_selftest_timeout(self.plan, limit_us, _stream_handle(stream)),
               "wf_selftest_timeout")
+
+    def quantize_weight_e4m3(self, w, stream=None):
+        """wf_quantize_weight_e4m3 on a bf16 [N, K] tensor -> (w8 uint8 [N, K], scale float [N])."""
+        import torch
+        N, K = w.shape
+        w8 = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+        sc = torch.empty(N, dtype=torch.float32, device=w.device)
+        check(lib.wf_quantize_weight_e4m3(self.plan, _ptr(w), N, K, _ptr(w8), _ptr(sc),
+                                          _stream_handle(stream)), "wf_quantize_weight_e4m3")
+        return w8, sc
+
+    def linear_e4m3(self, a8, w8, wscale, bias, out, epilogue, row_begin=0, row_end=None,
+                    gate=None, rows_per_group=1, stream=None):
+        rows, K = a8.shape
+        N = w8.shape[0]
+        row_end = rows if row_end is None else row_end
+        check(lib.wf_linear_e4m3(self.plan, _ptr(a8), rows, a8.stride(0), row_begin, row_end,
+                                 _ptr(w8), _ptr(wscale), _ptr(bias), N, K, epilogue, _ptr(out),
+                                 out.stride(0), _ptr(gate), gate.stride(0) if gate is not None else 0,
+                                 rows_per_group, _stream_handle(stream)), "wf_linear_e4m3")
 
     def sync_status(self, stream=None):
         return lib.wf_sync_status(self.plan, _stream_handle(stream))

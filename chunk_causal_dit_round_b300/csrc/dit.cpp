@@ -66,6 +66,43 @@ int wf_linear(wf_plan_t p, const void *a, long long a_rows, int lda, int row_beg
                : WF_ECUDA;
 }
 
+int wf_quantize_weight_e4m3(wf_plan_t p, const void *w, int N, int K, void *w8, float *scale,
+                            cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (!w || !w8 || !scale || N < 1 || K < 2 || K % 2) return WF_EINVAL;
+    return wf_launch_quant_rows(w, N, K, w8, scale, stream) == cudaSuccess ? WF_OK : WF_ECUDA;
+}
+
+int wf_linear_e4m3(wf_plan_t p, const void *a8, long long a_rows, int lda, int row_begin,
+                   int row_end, const void *w8, const float *wscale, const void *bias, int N, int K,
+                   int epilogue, void *out, int ldo, const float *gate, int gate_ld,
+                   int rows_per_group, cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (!a8 || !w8 || !wscale || !out) return WF_EINVAL;
+    if (epilogue < WF_EPI_BF16 || epilogue > WF_EPI_GATED_RESIDUAL) return WF_EINVAL;
+    if (K < 128 || K % 128 || N < 32 || N % 32 || lda < K || lda % 16 || ldo < N || ldo % 8)
+        return WF_EINVAL;
+    if (row_begin < 0 || row_end <= row_begin || row_end > a_rows) return WF_ERANGE;
+    if (!aligned16(a8) || !aligned16(w8) || !aligned16(wscale) || !aligned16(out) ||
+        (bias && !aligned16(bias)))
+        return WF_EINVAL;
+    if (epilogue == WF_EPI_GATED_RESIDUAL &&
+        (!gate || !aligned16(gate) || gate_ld % 4 || gate_ld < N || rows_per_group < 1))
+        return WF_EINVAL;
+    GemmParams gp = base_params(p, row_begin, row_end, N, K, bias);
+    gp.wscale = wscale;
+    gp.out = out;
+    gp.ldo = ldo;
+    gp.gate = gate;
+    gp.gate_ld = gate_ld;
+    gp.rows_per_group = rows_per_group;
+    return wf_launch_gemm(epilogue, a8, a_rows, lda, w8, gp, p->num_sms, stream, true) == cudaSuccess
+               ? WF_OK
+               : WF_ECUDA;
+}
+
 int wf_qkv_proj_rope_publish(wf_plan_t p, int layer, const void *x, const void *w_qkv,
                              const void *b_qkv, cudaStream_t stream) {
     if (!p) return WF_EINVAL;

@@ -91,6 +91,19 @@ __device__ __forceinline__ float gelu_tanh(float x) {
     return __fdividef(x, 1.f + __expf(fminf(-2.f * u, 80.f)));
 }
 
+// e4m3 operands: accumulator column j times the weight row's scale ws[j]
+__device__ __forceinline__ void scale_cols(uint32_t (&u)[32], const float *ws) {
+    const float4 *w4 = reinterpret_cast<const float4 *>(ws);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 w = __ldg(w4 + q);
+        u[4 * q] = __float_as_uint(__uint_as_float(u[4 * q]) * w.x);
+        u[4 * q + 1] = __float_as_uint(__uint_as_float(u[4 * q + 1]) * w.y);
+        u[4 * q + 2] = __float_as_uint(__uint_as_float(u[4 * q + 2]) * w.z);
+        u[4 * q + 3] = __float_as_uint(__uint_as_float(u[4 * q + 3]) * w.w);
+    }
+}
+
 // ---- epilogues -----------------------------------------------------------------
 // Each receives one thread's 32 consecutive accumulator columns of one row.
 
@@ -115,6 +128,24 @@ struct Epi<WF_EPI_GELU_BF16> {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
         Epi<WF_EPI_BF16>::apply(p, row, col, v);
+    }
+};
+// FFN hidden layer for an e4m3 FFN2: GELU, then e4m3 bytes (unit scale)
+template <>
+struct Epi<WF_EPI_GELU_E4M3> {
+    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(gelu_tanh(v[4 * i]), gelu_tanh(v[4 * i + 1])), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(gelu_tanh(v[4 * i + 2]), gelu_tanh(v[4 * i + 3])), __NV_SATFINITE, __NV_E4M3);
+            w[i] = lo | (hi << 16);
+        }
+        uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)row * p.ldo + col);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
 };
 template <>
@@ -301,7 +332,7 @@ __device__ __forceinline__ void residual_staged(const GemmParams &p, const float
 
 // ---- kernel -----------------------------------------------------------------------
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                    const GemmParams p) {
@@ -346,7 +377,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int n_tiles = p.tiles_m * p.tiles_n;
-    const int kb_n = p.K / BK;
+    // K elements per 128-byte stage row: 64 bf16 or 128 e4m3
+    constexpr int KE = F8 ? 2 * BK : BK;
+    const int kb_n = p.K / KE;
     uint32_t issued = 0;
 
     if (warp == 0 && lane == 0) {
@@ -360,14 +393,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!r.wait(bar(C::B_EMPTY + st), ((it / C::NST) & 1) ^ 1, 1)) goto done;
                 const uint32_t sa = r.sbase + st * C::STAGE;
                 mbar_arrive_expect_tx(bar(C::B_FULL + st), C::STAGE);
-                tma_load_2d(sa, &ta, bar(C::B_FULL + st), kb * BK, m0);
-                tma_load_2d(sa + C::A_BYTES, &tb, bar(C::B_FULL + st), kb * BK, n0);
+                tma_load_2d(sa, &ta, bar(C::B_FULL + st), kb * KE, m0);
+                tma_load_2d(sa + C::A_BYTES, &tb, bar(C::B_FULL + st), kb * KE, n0);
                 issued = it + 1;
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN, false) : idesc_bf16_f32(BM, BN, false);
         uint32_t it = 0, tl = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
             const int buf = tl & 1;
@@ -382,8 +415,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_ss(d, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
-                           idesc, (kb | kk) != 0 ? 1u : 0u);
+                    if constexpr (F8)
+                        mma_ss_f8(d, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
+                                  idesc, (kb | kk) != 0 ? 1u : 0u);
+                    else
+                        mma_ss(d, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024),
+                               idesc, (kb | kk) != 0 ? 1u : 0u);
                 mma_commit(bar(C::B_EMPTY + st));
             }
             mma_commit(bar(C::B_TFULL + buf));
@@ -425,7 +462,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // fp32 read-modify-write of x covers two full 128-byte row
                     // segments per warp instruction instead of 32 rows.
                     if (col < p.N) {
-                        const uint32_t(&uc)[32] = u[c & 1];
+                        uint32_t(&uc)[32] = u[c & 1];
+                        if (F8) scale_cols(uc, p.wscale + col);
                         float *stg = reinterpret_cast<float *>(smem + C::SM_STAGE) + (warp - 2) * 1024;
                         float4 *srow = reinterpret_cast<float4 *>(stg + lane * 32);
 #pragma unroll
@@ -438,7 +476,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                     }
                 } else if (live && col < p.N) {
-                    const uint32_t(&uc)[32] = u[c & 1];
+                    uint32_t(&uc)[32] = u[c & 1];
+                    if (F8) scale_cols(uc, p.wscale + col);
                     float v[32];
                     if (p.bias) {
                         const uint4 *b4 = reinterpret_cast<const uint4 *>(p.bias + col);
@@ -482,20 +521,20 @@ done:
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool F8>
 cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int num_sms,
                    cudaStream_t stream) {
     using C = Cfg<BN>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SM_ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int n_tiles = p.tiles_m * p.tiles_n;
     const int grid = n_tiles < num_sms ? n_tiles : num_sms;
-    gemm_tc_kernel<BN, EPI><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, p);
+    gemm_tc_kernel<BN, EPI, F8><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
@@ -521,16 +560,17 @@ EncodeFn encoder() {
 // 2D bf16 map over a row-major [rows, cols] matrix with row pitch ld
 // elements, box (64 columns, box_rows rows), 128-byte swizzle.
 bool encode_2d(CUtensorMap *m, const void *base, long long rows, long long cols, long long ld,
-               int box_rows) {
+               int box_rows, bool f8) {
     EncodeFn enc = encoder();
     if (!enc) return false;
+    const int es = f8 ? 1 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -539,21 +579,69 @@ bool encode_2d(CUtensorMap *m, const void *base, long long rows, long long cols,
 int wf_gemm_bn_for(int epi) { return epi == WF_EPI_HEAD ? 64 : 256; }
 
 cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, const void *w,
-                           GemmParams p, int num_sms, cudaStream_t stream) {
+                           GemmParams p, int num_sms, cudaStream_t stream, bool f8) {
     const int bn = wf_gemm_bn_for(epi);
-    if (p.K % BK || p.N % 32 || lda % 8 || p.row_end <= p.row_begin) return cudaErrorInvalidValue;
+    const int ke = f8 ? 2 * BK : BK;
+    if (p.K % ke || p.N % 32 || lda % (f8 ? 16 : 8) || p.row_end <= p.row_begin)
+        return cudaErrorInvalidValue;
+    if (f8 && !p.wscale) return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
-    if (!encode_2d(&ta, a, a_rows, p.K, lda, BM)) return cudaErrorInvalidValue;
-    if (!encode_2d(&tb, w, p.N, p.K, p.K, bn)) return cudaErrorInvalidValue;
+    if (!encode_2d(&ta, a, a_rows, p.K, lda, BM, f8)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tb, w, p.N, p.K, p.K, bn, f8)) return cudaErrorInvalidValue;
     p.tiles_m = (p.row_end - p.row_begin + BM - 1) / BM;
     p.tiles_n = (p.N + bn - 1) / bn;
+    if (f8) {
+        switch (epi) {
+            case WF_EPI_BF16: return launch<256, WF_EPI_BF16, true>(ta, tb, p, num_sms, stream);
+            case WF_EPI_F32: return launch<256, WF_EPI_F32, true>(ta, tb, p, num_sms, stream);
+            case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, true>(ta, tb, p, num_sms, stream);
+            case WF_EPI_GELU_E4M3: return launch<256, WF_EPI_GELU_E4M3, true>(ta, tb, p, num_sms, stream);
+            case WF_EPI_GATED_RESIDUAL:
+                return launch<256, WF_EPI_GATED_RESIDUAL, true>(ta, tb, p, num_sms, stream);
+            case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, true>(ta, tb, p, num_sms, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (epi) {
-        case WF_EPI_BF16: return launch<256, WF_EPI_BF16>(ta, tb, p, num_sms, stream);
-        case WF_EPI_F32: return launch<256, WF_EPI_F32>(ta, tb, p, num_sms, stream);
-        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16>(ta, tb, p, num_sms, stream);
-        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL>(ta, tb, p, num_sms, stream);
-        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH>(ta, tb, p, num_sms, stream);
-        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD>(ta, tb, p, num_sms, stream);
+        case WF_EPI_BF16: return launch<256, WF_EPI_BF16, false>(ta, tb, p, num_sms, stream);
+        case WF_EPI_F32: return launch<256, WF_EPI_F32, false>(ta, tb, p, num_sms, stream);
+        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, false>(ta, tb, p, num_sms, stream);
+        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL, false>(ta, tb, p, num_sms, stream);
+        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, false>(ta, tb, p, num_sms, stream);
+        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD, false>(ta, tb, p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// ---- weight quantisation: one warp per output row ------------------------------------
+namespace {
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16 *__restrict__ w, int N,
+                                                         int K, uint8_t *__restrict__ w8,
+                                                         float *__restrict__ scale) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const __nv_bfloat16 *wr = w + (size_t)row * K;
+    float amax = 0.f;
+    for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(__bfloat162float(wr[k])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (lane == 0) scale[row] = sc;
+    uint8_t *dst = w8 + (size_t)row * K;
+    for (int k = 2 * lane; k < K; k += 64) {
+        const float a = __fdiv_rn(__bfloat162float(wr[k]), sc);
+        const float b = __fdiv_rn(__bfloat162float(wr[k + 1]), sc);
+        *reinterpret_cast<uint16_t *>(dst + k) =
+            (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    }
+}
+}  // namespace
+
+cudaError_t wf_launch_quant_rows(const void *w, int N, int K, void *w8, float *scale,
+                                 cudaStream_t stream) {
+    if (K % 2) return cudaErrorInvalidValue;
+    quant_rows_kernel<<<(N * 32 + 255) / 256, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(w), N, K, static_cast<uint8_t *>(w8), scale);
+    return cudaGetLastError();
 }

@@ -79,12 +79,14 @@ cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int
 // the head (unpatchify + stage transition); the public ones are WF_EPI_*.
 #define WF_EPI_QKV_PUBLISH 100
 #define WF_EPI_HEAD        101
+#define WF_EPI_GELU_E4M3   102   // GELU, e4m3 bytes out (the input of an e4m3 FFN2)
 
 struct GemmParams {
     int row_begin, row_end;      // rows of A / out processed (absolute)
     int N, K;
     int tiles_m, tiles_n;        // filled by the launcher
     const __nv_bfloat16 *bias;   // [N] or null
+    const float *wscale;         // e4m3 operands: per output column (weight row) scale
     void *out;                   // epilogue destination
     int ldo;                     // its row pitch, elements
     const float *gate;           // gated residual: gate[group][col]
@@ -108,7 +110,11 @@ struct GemmParams {
 
 int wf_gemm_bn_for(int epi);
 cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, const void *w,
-                           GemmParams p, int num_sms, cudaStream_t stream);
+                           GemmParams p, int num_sms, cudaStream_t stream, bool f8 = false);
+// Per-row e4m3 quantisation of a bf16 weight [N][K]: scale[n] = max|w_n| / 448
+// (1 for an all-zero row), w8[n][k] = e4m3(w[n][k] / scale[n]).
+cudaError_t wf_launch_quant_rows(const void *w, int N, int K, void *w8, float *scale,
+                                 cudaStream_t stream);
 
 // ---- DiT block pieces (dit_ops.cu) ------------------------------------------
 struct WfDitLayerDev {

@@ -255,6 +255,24 @@ int wf_linear(wf_plan_t plan, const void *a, long long a_rows, int lda, int row_
               const void *w, const void *bias, int N, int K, int epilogue, void *out, int ldo,
               const float *gate, int gate_ld, int rows_per_group, cudaStream_t stream);
 
+/* 8-bit linear layers (the pages' W8A8 backend, Sec. 5; the pages give no
+ * recipe, so: OCP e4m3 weights with one scale per output channel, e4m3
+ * activations with unit scale, fp32 accumulation).
+ *
+ * wf_quantize_weight_e4m3: w bf16 [N][K] -> w8 e4m3 [N][K] and scale float
+ *   [N]: scale[n] = max_k |w[n][k]| / 448 (1 for an all-zero row),
+ *   w8[n][k] = e4m3(w[n][k] / scale[n]) (round to nearest even, saturating).
+ * wf_linear_e4m3: as wf_linear with a8 e4m3 [a_rows][lda] and w8 e4m3
+ *   [N][K]; out = epilogue(scale[n] * (a8 w8^T) + bias).  K % 128 == 0,
+ *   lda % 16 == 0.
+ * Errors: as wf_linear. */
+int wf_quantize_weight_e4m3(wf_plan_t plan, const void *w, int N, int K, void *w8, float *scale,
+                            cudaStream_t stream);
+int wf_linear_e4m3(wf_plan_t plan, const void *a8, long long a_rows, int lda, int row_begin,
+                   int row_end, const void *w8, const float *wscale, const void *bias, int N, int K,
+                   int epilogue, void *out, int ldo, const float *gate, int gate_ld,
+                   int rows_per_group, cudaStream_t stream);
+
 /* QKV projection of one layer fused with RoPE and paged publication (Sec.
  * 4.2: "publishes K/V after QKV projection and RoPE"; App. B.2 Eq. 13 direct
  * placement into fixed slots).  Same effect as wf_qkv_rope_publish applied

@@ -97,3 +97,51 @@ def test_no_bias(plan):
     torch.cuda.synchronize()
     ref = a.double().numpy() @ w.double().numpy().T
     assert np.abs(out.cpu().double().numpy() - ref).max() <= tol_f32(K)
+
+
+# ---- 8-bit linear layers ----------------------------------------------------------
+
+def e4m3_bytes_np(x32):
+    """float32 values -> e4m3 bytes (round to nearest even, saturating)."""
+    t = torch.from_numpy(np.clip(x32, -448.0, 448.0).astype(np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def test_weight_quantisation_bit_exact(plan):
+    N, K = 300, 384
+    w = wf_synth.normal(wf_synth.key_of(8, 1), (N, K), 0.02, torch.bfloat16)
+    w[7].zero_()                                     # an all-zero row keeps scale 1
+    w8, sc = plan.quantize_weight_e4m3(w.cuda())
+    torch.cuda.synchronize()
+    wf32 = w.float().numpy()
+    amax = np.abs(wf32).max(axis=1)
+    want_sc = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0))
+    assert np.array_equal(sc.cpu().numpy(), want_sc)
+    q = (wf32 / want_sc[:, None]).astype(np.float32)      # IEEE fp32 division, as the kernel
+    assert np.array_equal(w8.cpu().numpy(), e4m3_bytes_np(q))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 544, 128), (517, 256, 1536), (129, 800, 384)])
+def test_e4m3_linear_epilogues(plan, M, N, K):
+    a = wf_synth.normal(wf_synth.key_of(9, 1), (M, K), 1.0, torch.float32)
+    a8 = a.to(torch.float8_e4m3fn)
+    w = wf_synth.normal(wf_synth.key_of(9, 2), (N, K), 0.05, torch.bfloat16)
+    b = wf_synth.normal(wf_synth.key_of(9, 3), (N,), 0.5, torch.bfloat16)
+    w8, sc = plan.quantize_weight_e4m3(w.cuda())
+    deq_w = w8.cpu().view(torch.float8_e4m3fn).double().numpy() * sc.cpu().double().numpy()[:, None]
+    ref = a8.double().numpy() @ deq_w.T + b.double().numpy()
+    a8d = a8.view(torch.uint8).cuda()
+    out = torch.zeros((M, N), device="cuda")
+    plan.linear_e4m3(a8d, w8, sc, b.cuda(), out, wf.WF_EPI_F32)
+    torch.cuda.synchronize()
+    err = np.abs(out.cpu().double().numpy() - ref).max()
+    assert err <= 1e-4 * np.sqrt(K) * max(1.0, np.abs(ref).max()), err
+    gate = wf_synth.normal(wf_synth.key_of(9, 4), ((M + 199) // 200, N), 1.0, torch.float32)
+    x0 = wf_synth.normal(wf_synth.key_of(9, 5), (M, N), 1.0, torch.float32)
+    x = x0.clone().cuda()
+    plan.linear_e4m3(a8d, w8, sc, b.cuda(), x, wf.WF_EPI_GATED_RESIDUAL, gate=gate.cuda(),
+                     rows_per_group=200)
+    torch.cuda.synchronize()
+    want = x0.double().numpy() + gate.double().numpy()[np.arange(M) // 200] * ref
+    assert np.abs(x.cpu().double().numpy() - want).max() <= 3e-4 * np.sqrt(K) * max(1.0, np.abs(ref).max())
+    assert plan.sync_status() == wf.WF_OK
