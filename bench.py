@@ -64,6 +64,11 @@ DIT_CONFIGS = {
                       layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], fp8=(4.0, 4.0),
                       desc="as dit13 with 8-bit attention: e4m3 Q and K/V pages (x4 scales), "
                            "e4m3 P; linear layers bf16"),
+    "dit13_w8a8": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
+                       layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], fp8=(4.0, 4.0),
+                       linear_fp8=True,
+                       desc="as dit13 with 8-bit attention and 8-bit linear layers (e4m3 weights "
+                            "per output channel, e4m3 activations); patch embedding and head bf16"),
     # comparison graphs on the same model and kernels
     "dit13_rf": dict(S=4, grid=(3, 30, 52), heads=12, head_dim=128, history=3, dim=1536, ffn=8960,
                      layers=30, n_chunks=64, steps=[1000.0, 750.0, 500.0, 250.0], mask=1,
@@ -218,7 +223,8 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
                     ("o_b", (dim,)), ("f1_w", (ffn, dim)), ("f1_b", (ffn,)), ("f2_w", (dim, ffn)),
                     ("f2_b", (dim,)), ("mod", (6, dim))):
         P[k_] = [rnd(*shp) for _ in range(L)]
-    model = wf.Dit(r, P, ffn=ffn, channels=C, freq=256, timesteps=cfg["steps"])
+    model = wf.Dit(r, P, ffn=ffn, channels=C, freq=256, timesteps=cfg["steps"],
+                   linear_fp8=cfg.get("linear_fp8", False))
     latent = C * cfg["grid"][0] * 4 * cfg["grid"][1] * cfg["grid"][2]
     n_in = 3
     zs = [torch.randn(latent, generator=g, device=dev) for _ in range(n_in)]
@@ -298,11 +304,14 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     peak, src = _sustained_peak()
     peak_kind = "bf16 dense (sustained)"
     if cfg.get("fp8"):
-        # attention runs on the e4m3 pipe (2 x bf16 nominal), the linears on
-        # bf16: the bound is the time both would take at their own peaks
+        # attention (and with e4m3 linears the linear layers) run on the e4m3
+        # pipe, 2 x bf16 nominal: the bound is the time each part would take
+        # at its own peak
         fa = attn_total[0]                       # attention FLOPs of the timed rounds
-        t_min = fa / (2 * peak) + (flops - fa) / peak
-        peak, peak_kind = flops / t_min, "attention at 2 x and linears at 1 x measured bf16 (sustained)"
+        lin_x = 2.0 if cfg.get("linear_fp8") else 1.0
+        t_min = fa / (2 * peak) + (flops - fa) / (lin_x * peak)
+        peak_kind = (f"attention at 2 x and linears at {lin_x:g} x measured bf16 (sustained)")
+        peak = flops / t_min
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L, "value": round(chunks_s, 3),
            "unit": "chunks/s", "forwards_per_chunk_timed": per_step,

@@ -95,7 +95,7 @@ class wf_dit_model(ctypes.Structure):
                 ("context_noise", ctypes.c_double), ("timesteps", ctypes.c_double * WF_MAX_STAGES)] + \
         [(n, ctypes.c_void_p) for n in ("patch_w", "patch_b", "t1_w", "t1_b", "t2_w", "t2_b", "tp_w",
                                         "tp_b", "head_w", "head_b", "head_mod")] + \
-        [("layers", ctypes.POINTER(wf_dit_layer))]
+        [("layers", ctypes.POINTER(wf_dit_layer)), ("linear_fp8", ctypes.c_int)]
 
 
 def _load():
@@ -119,7 +119,7 @@ def _load():
         "wf_strerror": (ctypes.c_char_p, [I]),
         "wf_linear": (I, [P, VP, ctypes.c_longlong, I, I, I, VP, VP, I, I, I, VP, I, VP, I, I, VP]),
         "wf_qkv_proj_rope_publish": (I, [P, I, VP, VP, VP, VP]),
-        "wf_dit_workspace_size": (I, [P, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
+        "wf_dit_workspace_size": (I, [P, I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_dit_bind": (I, [P, ctypes.POINTER(wf_dit_model), VP, VP]),
         "wf_dit_round": (I, [P, VP, VP, VP, VP, VP]),
         "wf_selftest_timeout": (I, [P, ctypes.c_uint, VP]),
@@ -348,7 +348,7 @@ class Dit:
     launching wf_dit_round for the round the plan is in."""
 
     def __init__(self, rnd: Round, params: dict, *, ffn, channels=16, freq=256, timesteps,
-                 shift=5.0, context_noise=0.0, stream=None):
+                 shift=5.0, context_noise=0.0, linear_fp8=False, stream=None):
         import torch
         self.r = rnd
         dev = rnd.pool.device
@@ -373,10 +373,11 @@ class Dit:
             for cn, pn in names:
                 setattr(self._layers[l], cn, P[pn][l].data_ptr())
         m.layers = self._layers
+        m.linear_fp8 = int(linear_fp8)
         self.model = m
         nbytes = ctypes.c_size_t()
-        check(lib.wf_dit_workspace_size(rnd.plan, dim, ffn, channels, freq, ctypes.byref(nbytes)),
-              "wf_dit_workspace_size")
+        check(lib.wf_dit_workspace_size(rnd.plan, dim, ffn, channels, freq, int(linear_fp8),
+                                         ctypes.byref(nbytes)), "wf_dit_workspace_size")
         self.workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
         check(lib.wf_dit_bind(rnd.plan, ctypes.byref(m), _ptr(self.workspace),
                               _stream_handle(stream)), "wf_dit_bind")

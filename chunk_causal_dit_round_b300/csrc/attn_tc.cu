@@ -95,7 +95,8 @@ struct TcParams {
     int tpc;              // key tiles per chunk
     float sl2;            // log2(e) / sqrt(D) (/ qk_scale^2 for e4m3 Q and K)
     float o_scale;        // 1 (bf16) or 1 / v_scale (e4m3 V)
-    __nv_bfloat16 *out;
+    __nv_bfloat16 *out;   // [slot][N_C][H][D] bf16, or e4m3 bytes when out_e4m3
+    int out_e4m3;         // O as e4m3 (unit scale): the input of an e4m3 output projection
     uint32_t *ctl;        // scratch control words
 };
 
@@ -375,22 +376,34 @@ __device__ void softmax_tile(const Ctx<F8> &c, uint32_t tmem, const WfGeom &g, c
     tc_fence_after();
     const int qrow = (2 * qp + X) * BM + row;
     const float inv = p.o_scale / l_run;
-    __nv_bfloat16 *dst = p.out + (((size_t)rd.slot[ti] * g.NC + qrow) * g.H + h) * HD;
+    const size_t o_off = (((size_t)rd.slot[ti] * g.NC + qrow) * g.H + h) * HD;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t o[32];
         tmem_ld32(tO + q * 32, o);
         tmem_wait_ld(o);
         if (qrow < g.NC) {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
+            if (p.out_e4m3) {
+                uint32_t w[8];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                uint4 w;
-                w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                d4[v] = w;
+                for (int v = 0; v < 8; ++v)
+                    w[v] = pack_e4m3x2(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv) |
+                           (pack_e4m3x2(__uint_as_float(o[4 * v + 2]) * inv,
+                                        __uint_as_float(o[4 * v + 3]) * inv) << 16);
+                uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) + o_off + q * 32);
+                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(p.out + o_off + q * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                    d4[v] = w;
+                }
             }
         }
     }
@@ -532,7 +545,7 @@ cudaError_t prepare_kernel() {
 
 // Parameters and launch of one round's attention (ctl: the control words).
 cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const WfTmaps &maps,
-                      void *out, uint32_t *ctl, int num_sms, cudaStream_t stream) {
+                      void *out, uint32_t *ctl, int num_sms, cudaStream_t stream, int out_e4m3 = 0) {
     const bool f8 = g.dtype == WF_FP8;
     cudaError_t e = f8 ? prepare_kernel<true>() : prepare_kernel<false>();
     if (e != cudaSuccess) return e;
@@ -548,6 +561,7 @@ cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const Wf
         p.o_scale = 1.f / g.v_scale;
     }
     p.out = static_cast<__nv_bfloat16 *>(out);
+    p.out_e4m3 = out_e4m3;
     p.ctl = ctl;
     int grid = p.n_units < num_sms ? p.n_units : num_sms;
     if (f8)
@@ -601,9 +615,10 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
 
 cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, int out_e4m3) {
     if (rd.n_tasks < 1) return cudaSuccess;
-    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(scratch), num_sms, stream);
+    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(scratch), num_sms, stream,
+                     out_e4m3);
 }
 
 // ---- launch without caller scratch ------------------------------------------

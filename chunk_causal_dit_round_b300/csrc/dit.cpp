@@ -118,14 +118,16 @@ int wf_qkv_proj_rope_publish(wf_plan_t p, int layer, const void *x, const void *
 }
 
 int wf_dit_workspace_size(wf_plan_t p, int model_dim, int ffn_dim, int channels, int freq_dim,
-                          size_t *bytes) {
+                          int linear_fp8, size_t *bytes) {
     if (!p || !bytes) return WF_EINVAL;
     if (model_dim != p->H * p->D || ffn_dim < 64 || ffn_dim % 64 || channels < 1 ||
-        (4 * channels) % 64 || freq_dim < 2 || freq_dim % 2)
+        (4 * channels) % 64 || freq_dim < 2 || freq_dim % 2 || (linear_fp8 != 0 && linear_fp8 != 1))
         return WF_EINVAL;
+    // e4m3 linear layers take K in 128-element steps
+    if (linear_fp8 && (model_dim % 128 || ffn_dim % 128)) return WF_EINVAL;
     const size_t latent = (size_t)channels * p->g.gt * 4 * p->g.gh * p->g.gw;
     *bytes = wf_dit_workspace_bytes(p->S, p->NC, model_dim, ffn_dim, channels, freq_dim,
-                                    p->o.layers, latent);
+                                    p->o.layers, latent, linear_fp8);
     return WF_OK;
 }
 
@@ -135,7 +137,8 @@ int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_
     if ((p->o.dtype != WF_BF16 && p->o.dtype != WF_FP8) || p->D != 128) return WF_EUNSUPPORTED;
     if ((uintptr_t)workspace & 255) return WF_EINVAL;
     size_t need;
-    int rc = wf_dit_workspace_size(p, m->model_dim, m->ffn_dim, m->channels, m->freq_dim, &need);
+    int rc = wf_dit_workspace_size(p, m->model_dim, m->ffn_dim, m->channels, m->freq_dim,
+                                   m->linear_fp8, &need);
     if (rc != WF_OK) return rc;
     if (!(m->shift > 0.0) || !std::isfinite(m->shift) || !(m->context_noise >= 0.0) ||
         !(m->context_noise <= 1000.0))
@@ -165,6 +168,7 @@ int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_
     d.C = m->channels;
     d.freq = m->freq_dim;
     d.L = L;
+    d.linear_fp8 = m->linear_fp8;
     d.shift = m->shift;
     d.context_noise = m->context_noise;
     for (int s = 0; s < p->S; ++s) d.nu[s] = m->timesteps[s];
@@ -180,7 +184,8 @@ int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_
     for (int l = 0; l < L; ++l) {
         const wf_dit_layer &w = m->layers[l];
         d.layers[l] = {B(w.qkv_w), B(w.qkv_b), B(w.o_w), B(w.o_b), B(w.ffn1_w),
-                       B(w.ffn1_b), B(w.ffn2_w), B(w.ffn2_b), B(w.modulation)};
+                       B(w.ffn1_b), B(w.ffn2_w), B(w.ffn2_b), B(w.modulation),
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     }
     const size_t latent = (size_t)d.C * p->g.gt * 4 * p->g.gh * p->g.gw;
     wf_dit_carve(&d, workspace, p->S, p->NC, latent);
@@ -195,6 +200,17 @@ int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_
     if (cudaMemsetAsync(d.lat, 0, 2 * (size_t)(p->S + 1) * latent * 4, stream) != cudaSuccess)
         return WF_ECUDA;
     if (wf_launch_time_embedding(d, p->S, stream) != cudaSuccess) return WF_ECUDA;
+    if (d.linear_fp8) {
+        const int dm = d.dim, f = d.ffn;
+        for (int l = 0; l < L; ++l) {
+            const WfDitLayerDev &w = d.layers[l];
+            if (wf_launch_quant_rows(w.qkv_w, 3 * dm, dm, w.qkv_w8, w.qkv_s, stream) != cudaSuccess ||
+                wf_launch_quant_rows(w.o_w, dm, dm, w.o_w8, w.o_s, stream) != cudaSuccess ||
+                wf_launch_quant_rows(w.f1_w, f, dm, w.f1_w8, w.f1_s, stream) != cudaSuccess ||
+                wf_launch_quant_rows(w.f2_w, dm, f, w.f2_w8, w.f2_s, stream) != cudaSuccess)
+                return WF_ECUDA;
+        }
+    }
     p->dit_bound = true;
     return WF_OK;
 }
@@ -234,16 +250,20 @@ int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_ou
         cudaSuccess)
         return WF_ECUDA;
 
+    const bool f8 = d.linear_fp8 != 0;
     for (int l = 0; l < d.L; ++l) {
         const WfDitLayerDev &w = d.layers[l];
         const float *mod = d.modtab + (size_t)l * (S + 1) * mod_ld;
+        // activations of the linear layers: bf16, or e4m3 with e4m3 weights
+        void *act = f8 ? static_cast<void *>(d.xa8) : static_cast<void *>(d.xa);
         // P_{s,l}: x' = LN(x)(1 + scale_a) + shift_a; QKV projection, RoPE, publish
-        if (wf_launch_ln_mod(d.x, d.xa, r0, r1, dim, NC, mod, mod_ld, 0, dim, stream) != cudaSuccess)
+        if (wf_launch_ln_mod(d.x, act, r0, r1, dim, NC, mod, mod_ld, 0, dim, stream, f8) != cudaSuccess)
             return WF_ECUDA;
-        int rc = wf_publish_impl(p, l, d.xa, w.qkv_w, w.qkv_b, nullptr, stream);
+        int rc = f8 ? wf_publish_impl(p, l, d.xa8, w.qkv_w8, w.qkv_b, nullptr, stream, w.qkv_s)
+                    : wf_publish_impl(p, l, d.xa, w.qkv_w, w.qkv_b, nullptr, stream);
         if (rc != WF_OK) return rc;
         // C_{s,l}: round attention (output over x', which is dead), then the rest of the block
-        rc = wf_round_attention(p, l, d.xa, WF_ATTN_TC, stream);
+        rc = wf_attention_impl(p, l, act, WF_ATTN_TC, stream, f8 ? 1 : 0);
         if (rc != WF_OK) return rc;
         gp = base_params(p, r0, r1, dim, dim, w.o_b);
         gp.out = d.x;
@@ -251,17 +271,19 @@ int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_ou
         gp.gate = mod + 2 * dim;
         gp.gate_ld = mod_ld;
         gp.rows_per_group = NC;
-        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, d.xa, rows, dim, w.o_w, gp, p->num_sms, stream) !=
-            cudaSuccess)
+        gp.wscale = w.o_s;
+        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, act, rows, dim, f8 ? (const void *)w.o_w8 : w.o_w, gp,
+                           p->num_sms, stream, f8) != cudaSuccess)
             return WF_ECUDA;
-        if (wf_launch_ln_mod(d.x, d.xa, r0, r1, dim, NC, mod, mod_ld, 3 * dim, 4 * dim, stream) !=
+        if (wf_launch_ln_mod(d.x, act, r0, r1, dim, NC, mod, mod_ld, 3 * dim, 4 * dim, stream, f8) !=
             cudaSuccess)
             return WF_ECUDA;
         gp = base_params(p, r0, r1, d.ffn, dim, w.f1_b);
-        gp.out = d.hmid;
+        gp.out = f8 ? static_cast<void *>(d.h8) : static_cast<void *>(d.hmid);
         gp.ldo = d.ffn;
-        if (wf_launch_gemm(WF_EPI_GELU_BF16, d.xa, rows, dim, w.f1_w, gp, p->num_sms, stream) !=
-            cudaSuccess)
+        gp.wscale = w.f1_s;
+        if (wf_launch_gemm(f8 ? WF_EPI_GELU_E4M3 : WF_EPI_GELU_BF16, act, rows, dim,
+                           f8 ? (const void *)w.f1_w8 : w.f1_w, gp, p->num_sms, stream, f8) != cudaSuccess)
             return WF_ECUDA;
         gp = base_params(p, r0, r1, dim, d.ffn, w.f2_b);
         gp.out = d.x;
@@ -269,8 +291,10 @@ int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_ou
         gp.gate = mod + 5 * dim;
         gp.gate_ld = mod_ld;
         gp.rows_per_group = NC;
-        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, d.hmid, rows, d.ffn, w.f2_w, gp, p->num_sms,
-                           stream) != cudaSuccess)
+        gp.wscale = w.f2_s;
+        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, f8 ? static_cast<const void *>(d.h8) : d.hmid, rows,
+                           d.ffn, f8 ? (const void *)w.f2_w8 : w.f2_w, gp, p->num_sms, stream, f8) !=
+            cudaSuccess)
             return WF_ECUDA;
     }
 

@@ -9,14 +9,16 @@
 //    binding (each stage has a fixed timestep, App. A).
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "wf_internal.h"
 
 namespace {
 
 // ---- LayerNorm + modulation: one warp per row ---------------------------------
+template <bool F8>
 __global__ void __launch_bounds__(256) ln_mod_kernel(const float *__restrict__ x,
-                                                     __nv_bfloat16 *__restrict__ out, int row_begin,
+                                                     void *__restrict__ out, int row_begin,
                                                      int row_end, int dim, int NC,
                                                      const float *__restrict__ mod, int mod_ld,
                                                      int shift_off, int scale_off) {
@@ -47,15 +49,22 @@ __global__ void __launch_bounds__(256) ln_mod_kernel(const float *__restrict__ x
     const int slot = row / NC;
     const float4 *sh = reinterpret_cast<const float4 *>(mod + (size_t)slot * mod_ld + shift_off);
     const float4 *sc = reinterpret_cast<const float4 *>(mod + (size_t)slot * mod_ld + scale_off);
-    uint2 *orow = reinterpret_cast<uint2 *>(out + (size_t)row * dim);
     for (int i = lane; i < nv; i += 32) {
         float4 v = xr[i], a = __ldg(sh + i), b = __ldg(sc + i);
         float y0 = fmaf((v.x - mean) * rstd, 1.f + b.x, a.x);
         float y1 = fmaf((v.y - mean) * rstd, 1.f + b.y, a.y);
         float y2 = fmaf((v.z - mean) * rstd, 1.f + b.z, a.z);
         float y3 = fmaf((v.w - mean) * rstd, 1.f + b.w, a.w);
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(y0, y1), p1 = __floats2bfloat162_rn(y2, y3);
-        orow[i] = make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
+        if constexpr (F8) {
+            // e4m3 with unit scale: the input of an e4m3 linear layer
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y2, y3), __NV_SATFINITE, __NV_E4M3);
+            reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(out) + (size_t)row * dim)[i] = lo | (hi << 16);
+        } else {
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(y0, y1), p1 = __floats2bfloat162_rn(y2, y3);
+            reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + (size_t)row * dim)[i] =
+                make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
+        }
     }
 }
 
@@ -162,13 +171,21 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-size_t wf_dit_workspace_bytes(int S, int NC, int dim, int ffn, int C, int freq, int L, size_t latent) {
+size_t wf_dit_workspace_bytes(int S, int NC, int dim, int ffn, int C, int freq, int L, size_t latent,
+                              int linear_fp8) {
     const size_t rows = (size_t)(S + 1) * NC, B = S + 1;
-    return align256(rows * dim * 4) + align256(rows * dim * 2) + align256(rows * ffn * 2) +
-           align256(rows * 4 * C * 2) + align256(2 * B * latent * 4) +
-           align256((size_t)L * B * 6 * dim * 4) + align256(B * 2 * dim * 4) +
-           align256(B * (size_t)(freq + 9 * dim) * 4) + align256((size_t)L * sizeof(WfDitLayerDev)) +
-           align256(B * 4);
+    size_t b = align256(rows * dim * 4) + align256(rows * dim * 2) + align256(rows * ffn * 2) +
+               align256(rows * 4 * C * 2) + align256(2 * B * latent * 4) +
+               align256((size_t)L * B * 6 * dim * 4) + align256(B * 2 * dim * 4) +
+               align256(B * (size_t)(freq + 9 * dim) * 4) + align256((size_t)L * sizeof(WfDitLayerDev)) +
+               align256(B * 4);
+    if (linear_fp8) {
+        const size_t d = dim, f = ffn;
+        b += align256(rows * d) + align256(rows * f);
+        b += (size_t)L * (align256(3 * d * d) + align256(d * d) + align256(f * d) + align256(d * f) +
+                          align256(3 * d * 4) + align256(d * 4) + align256(f * 4) + align256(d * 4));
+    }
+    return b;
 }
 
 void wf_dit_carve(WfDit *d, void *ws, int S, int NC, size_t latent) {
@@ -186,16 +203,37 @@ void wf_dit_carve(WfDit *d, void *ws, int S, int NC, size_t latent) {
     d->layers_dev = reinterpret_cast<WfDitLayerDev *>(take((size_t)d->L * sizeof(WfDitLayerDev)));
     d->tmodel = reinterpret_cast<float *>(take(B * 4));
     d->latent = latent;
+    d->xa8 = d->h8 = nullptr;
+    if (d->linear_fp8) {
+        const size_t dm = d->dim, f = d->ffn;
+        d->xa8 = reinterpret_cast<uint8_t *>(take(rows * dm));
+        d->h8 = reinterpret_cast<uint8_t *>(take(rows * f));
+        for (int l = 0; l < d->L; ++l) {
+            WfDitLayerDev &w = d->layers[l];
+            w.qkv_w8 = reinterpret_cast<uint8_t *>(take(3 * dm * dm));
+            w.o_w8 = reinterpret_cast<uint8_t *>(take(dm * dm));
+            w.f1_w8 = reinterpret_cast<uint8_t *>(take(f * dm));
+            w.f2_w8 = reinterpret_cast<uint8_t *>(take(dm * f));
+            w.qkv_s = reinterpret_cast<float *>(take(3 * dm * 4));
+            w.o_s = reinterpret_cast<float *>(take(dm * 4));
+            w.f1_s = reinterpret_cast<float *>(take(f * 4));
+            w.f2_s = reinterpret_cast<float *>(take(dm * 4));
+        }
+    }
 }
 
-cudaError_t wf_launch_ln_mod(const float *x, __nv_bfloat16 *out, int row_begin, int row_end,
-                             int dim, int NC, const float *mod, int mod_ld, int shift_off,
-                             int scale_off, cudaStream_t stream) {
+cudaError_t wf_launch_ln_mod(const float *x, void *out, int row_begin, int row_end, int dim, int NC,
+                             const float *mod, int mod_ld, int shift_off, int scale_off,
+                             cudaStream_t stream, bool out_e4m3) {
     if (dim % 4 || row_end <= row_begin) return cudaErrorInvalidValue;
     const int rows = row_end - row_begin;
     const int blocks = (rows + 7) / 8;
-    ln_mod_kernel<<<blocks, 256, 0, stream>>>(x, out, row_begin, row_end, dim, NC, mod, mod_ld,
-                                              shift_off, scale_off);
+    if (out_e4m3)
+        ln_mod_kernel<true><<<blocks, 256, 0, stream>>>(x, out, row_begin, row_end, dim, NC, mod, mod_ld,
+                                                        shift_off, scale_off);
+    else
+        ln_mod_kernel<false><<<blocks, 256, 0, stream>>>(x, out, row_begin, row_end, dim, NC, mod, mod_ld,
+                                                         shift_off, scale_off);
     return cudaGetLastError();
 }
 

@@ -66,7 +66,7 @@ bool wf_attn_tc_supported(const WfGeom &g, int dtype);
 cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out);
 cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int out_e4m3 = 0);
 
 // Variant of wf_launch_attn_tc whose control words live in a static device
 // block inside the library (no caller scratch); see wf_round_attention_noalloc.
@@ -119,10 +119,16 @@ cudaError_t wf_launch_quant_rows(const void *w, int N, int K, void *w8, float *s
 // ---- DiT block pieces (dit_ops.cu) ------------------------------------------
 struct WfDitLayerDev {
     const __nv_bfloat16 *qkv_w, *qkv_b, *o_w, *o_b, *f1_w, *f1_b, *f2_w, *f2_b, *mod;
+    // e4m3 weights and per-output-channel scales (linear_fp8), in the workspace
+    uint8_t *qkv_w8, *o_w8, *f1_w8, *f2_w8;
+    float *qkv_s, *o_s, *f1_s, *f2_s;
 };
 
 struct WfDit {
     int dim, ffn, C, freq, L;
+    int linear_fp8;              // the block's linear layers in e4m3
+    uint8_t *xa8;                // [(S+1) N_C][dim] e4m3 LN output / attention output
+    uint8_t *h8;                 // [(S+1) N_C][ffn] e4m3 FFN hidden
     double shift, context_noise, nu[WF_MAX_STAGES + 1];
     const __nv_bfloat16 *patch_w, *patch_b, *t1_w, *t1_b, *t2_w, *t2_b, *tp_w, *tp_b, *head_w,
         *head_b, *head_mod;
@@ -141,12 +147,13 @@ struct WfDit {
     size_t latent;               // floats of one latent chunk
 };
 
-size_t wf_dit_workspace_bytes(int S, int NC, int dim, int ffn, int C, int freq, int L, size_t latent);
+size_t wf_dit_workspace_bytes(int S, int NC, int dim, int ffn, int C, int freq, int L, size_t latent,
+                              int linear_fp8);
 void wf_dit_carve(WfDit *d, void *ws, int S, int NC, size_t latent);
 
-cudaError_t wf_launch_ln_mod(const float *x, __nv_bfloat16 *out, int row_begin, int row_end,
-                             int dim, int NC, const float *mod, int mod_ld, int shift_off,
-                             int scale_off, cudaStream_t stream);
+cudaError_t wf_launch_ln_mod(const float *x, void *out, int row_begin, int row_end, int dim, int NC,
+                             const float *mod, int mod_ld, int shift_off, int scale_off,
+                             cudaStream_t stream, bool out_e4m3 = false);
 cudaError_t wf_launch_patchify(const WfGeom &g, int C, const float *const *src, int lo, int hi,
                                __nv_bfloat16 *patches, cudaStream_t stream);
 cudaError_t wf_launch_time_embedding(const WfDit &d, int S, cudaStream_t stream);

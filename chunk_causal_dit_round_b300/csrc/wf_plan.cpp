@@ -134,6 +134,23 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
 
 }  // namespace
 
+int wf_attention_impl(wf_plan_s *p, int layer, void *out, int kernel, cudaStream_t stream,
+                      int out_e4m3) {
+    bool tc_ok = p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype);
+    bool simt_ok = p->D % 32 == 0 && p->D <= 128 && p->o.dtype != WF_FP8 && !out_e4m3;
+    if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
+    cudaError_t e;
+    if (kernel == WF_ATTN_TC) {
+        if (!tc_ok) return WF_EUNSUPPORTED;
+        e = wf_launch_attn_tc(p->g, p->rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream,
+                              out_e4m3);
+    } else {
+        if (!simt_ok) return WF_EUNSUPPORTED;
+        e = wf_launch_attn_simt(p->g, p->rd, layer, p->o.dtype, p->qbuf, p->pool, out, stream);
+    }
+    return e == cudaSuccess ? WF_OK : WF_ECUDA;
+}
+
 // Rebuild the current round's contexts from the round state (after a state
 // import): the current round's store is the one recorded for promotion.
 void wf_rebuild_round(wf_plan_s *p) {
@@ -147,7 +164,7 @@ void wf_rebuild_round(wf_plan_s *p) {
 // (x and W_qkv given): one launch publishes every active task; the anchor
 // key is re-rotated from its unrotated copy when the window moved.
 int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
-                    const void *qkv, cudaStream_t stream) {
+                    const void *qkv, cudaStream_t stream, const float *wscale) {
     WfRoundDev rd = p->rd;
     int new_rot = p->anchor_rot[layer];
     bool rerotate = false;
@@ -177,8 +194,9 @@ int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, c
         gp.pool = static_cast<__nv_bfloat16 *>(p->pool);
         gp.rope = reinterpret_cast<const float2 *>(static_cast<const char *>(p->scratch) +
                                                    WF_SCRATCH_TABLES);
+        gp.wscale = wscale;
         if (wf_launch_gemm(WF_EPI_QKV_PUBLISH, x, (long long)(p->S + 1) * p->NC, gp.K, w_qkv, gp,
-                           p->num_sms, stream) != cudaSuccess)
+                           p->num_sms, stream, wscale != nullptr) != cudaSuccess)
             return WF_ECUDA;
         if (rerotate) {
             WfRoundDev rr = rd;
@@ -446,18 +464,7 @@ int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream
     if (!out || ((uintptr_t)out & 15)) return WF_EINVAL;
     if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
     if (p->published[layer] != p->k) return WF_EORDER;
-    bool tc_ok = p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype);
-    bool simt_ok = p->D % 32 == 0 && p->D <= 128 && p->o.dtype != WF_FP8;
-    if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
-    cudaError_t e;
-    if (kernel == WF_ATTN_TC) {
-        if (!tc_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_tc(p->g, p->rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream);
-    } else {
-        if (!simt_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_simt(p->g, p->rd, layer, p->o.dtype, p->qbuf, p->pool, out, stream);
-    }
-    return e == cudaSuccess ? WF_OK : WF_ECUDA;
+    return wf_attention_impl(p, layer, out, kernel, stream);
 }
 
 int wf_round_attention_noalloc(wf_plan_t p, int layer, void *out, cudaStream_t stream) {

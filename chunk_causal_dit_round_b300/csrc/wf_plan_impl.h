@@ -75,5 +75,10 @@ void wf_rebuild_round(wf_plan_s *p);
 // projection GEMM (x != nullptr) or the given Q/K/V; the anchor re-rotation
 // when the window moved.  Returns a WF_* code.
 int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
-                    const void *qkv, cudaStream_t stream);
+                    const void *qkv, cudaStream_t stream, const float *wscale = nullptr);
+
+// Round attention of `layer` after the argument checks of wf_round_attention;
+// out_e4m3 writes O as e4m3 bytes (tensor-core kernel).  Returns a WF_* code.
+int wf_attention_impl(wf_plan_s *p, int layer, void *out, int kernel, cudaStream_t stream,
+                      int out_e4m3 = 0);
 

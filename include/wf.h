@@ -324,13 +324,18 @@ typedef struct wf_dit_model {
     const void *head_w, *head_b;   /* [4C][dim], [4C] */
     const void *head_mod;          /* [2][dim]: shift, scale */
     const wf_dit_layer *layers;    /* host array of `layers` (plan option) entries */
+    int linear_fp8;                /* 1: the block's four linear layers run in e4m3 (weights
+                                      quantised per output channel at bind time, LN output,
+                                      attention output and FFN hidden layer as e4m3 with unit
+                                      scale); patch embedding and head stay bf16 */
 } wf_dit_model;
 
 /* Bytes of the DiT workspace (residual stream, normalised activations, FFN
  * hidden layer, patches, double-buffered latent slot inputs, modulation
- * tables).  No CUDA call.  Errors: WF_EINVAL (dims). */
+ * tables; with linear_fp8 also the e4m3 activations and the quantised
+ * weights of every layer).  No CUDA call.  Errors: WF_EINVAL (dims). */
 int wf_dit_workspace_size(wf_plan_t plan, int model_dim, int ffn_dim, int channels, int freq_dim,
-                          size_t *bytes);
+                          int linear_fp8, size_t *bytes);
 
 /* Attach a model and a caller-owned workspace (256-byte aligned, size from
  * wf_dit_workspace_size) to a bound bf16 or WF_FP8 plan with head_dim 128

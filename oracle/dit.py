@@ -45,6 +45,12 @@ in the design notes:
 anchor's unrotated key) as e4m3 after scaling instead of bf16 (8-bit
 attention, the pages' SageAttention backend and FP8 K/V payload).
 
+``linear_fp8=True`` runs the block's four linear layers in e4m3 (the pages'
+W8A8 backend, Sec. 5): every weight row is scaled by max|w| / 448 (computed
+in float32, as the kernel computes it) and rounded to e4m3; the LN outputs,
+the attention output and the FFN hidden layer enter those layers as e4m3
+with unit scale.
+
 ``bf16=True`` rounds to bfloat16 where a BF16 execution (App. B.1) stores a
 tensor: the latent patches, every linear layer's input (normalised
 activations, attention output, FFN hidden), the RoPE-applied Q/K and V that
@@ -78,6 +84,18 @@ def bf16(x):
     """Round fp64 values to bfloat16 (round to nearest even), back in fp64."""
     import torch
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+
+
+def quantize_rows_e4m3(w):
+    """Effective fp64 weight of a per-row e4m3 quantisation: scale = max|w_n|
+    / 448 in float32 (1 for an all-zero row), q = e4m3(float32(w) / scale),
+    returned as q * scale."""
+    from .round import e4m3
+    w32 = np.asarray(w, np.float32)
+    amax = np.abs(w32).max(axis=1)
+    sc = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0))
+    q = e4m3((w32 / sc[:, None]).astype(np.float32).astype(np.float64))
+    return q * sc.astype(np.float64)[:, None]
 
 
 def layer_norm(x, eps=1e-6):
@@ -195,13 +213,24 @@ class Model:
     k; state (latent slot inputs, K/V of stored chunks) carries over."""
 
     def __init__(self, cfg: sch.Cfg, grid, dims: Dims, w: Weights, timesteps,
-                 shift=5.0, context_noise=0.0, theta=10000.0, bf16_points=True, kv_fp8=None):
+                 shift=5.0, context_noise=0.0, theta=10000.0, bf16_points=True, kv_fp8=None,
+                 linear_fp8=False):
         assert len(timesteps) == cfg.S
         self.cfg, self.grid, self.d, self.w = cfg, tuple(grid), dims, w
         self.nu = list(timesteps) + [0.0]          # nu_0 > ... > nu_{S-1} > nu_S = 0
         self.shift, self.theta = shift, theta
         self.rb = bf16 if bf16_points else (lambda x: np.asarray(x, np.float64))
         self.kv_fp8 = kv_fp8
+        # inputs and weights of the block's linear layers
+        if linear_fp8:
+            from .round import e4m3
+            self.ra = lambda x: e4m3(x)
+            q = quantize_rows_e4m3
+            self.lw = {"qkv": [q(a) for a in w.qkv_w], "o": [q(a) for a in w.o_w],
+                       "f1": [q(a) for a in w.f1_w], "f2": [q(a) for a in w.f2_w]}
+        else:
+            self.ra = self.rb
+            self.lw = {"qkv": w.qkv_w, "o": w.o_w, "f1": w.f1_w, "f2": w.f2_w}
         # model timestep of each slot: stage s -> warped nu_s; the store -> context_noise
         self.slot_t = [1000.0 * warp_sigma(nu, shift) for nu in timesteps]
         self.slot_t.append(1000.0 * warp_sigma(context_noise, shift))
@@ -218,8 +247,8 @@ class Model:
         """Projected, RoPE'd Q, K and V [N_C, H, D] plus the unrotated K."""
         d, w = self.d, self.w
         m = w.mod[layer] + self.emb[slot][1]
-        xa = self.rb(layer_norm(x) * (1.0 + m[1]) + m[0])
-        y = xa @ w.qkv_w[layer].T + w.qkv_b[layer]
+        xa = self.ra(layer_norm(x) * (1.0 + m[1]) + m[0])
+        y = xa @ self.lw["qkv"][layer].T + w.qkv_b[layer]
         q, k, v = (y[:, i * d.dim:(i + 1) * d.dim].reshape(-1, d.heads, d.head_dim) for i in range(3))
         ang = self.angles(chunk)
         if self.kv_fp8 is not None:
@@ -236,10 +265,10 @@ class Model:
         """x + attention output projection, then the FFN half of the block."""
         d, w = self.d, self.w
         m = w.mod[layer] + self.emb[slot][1]
-        x = x + m[2] * (self.rb(o.reshape(-1, d.dim)) @ w.o_w[layer].T + w.o_b[layer])
-        xf = self.rb(layer_norm(x) * (1.0 + m[4]) + m[3])
-        hmid = self.rb(gelu_tanh(xf @ w.f1_w[layer].T + w.f1_b[layer]))
-        return x + m[5] * (hmid @ w.f2_w[layer].T + w.f2_b[layer])
+        x = x + m[2] * (self.ra(o.reshape(-1, d.dim)) @ self.lw["o"][layer].T + w.o_b[layer])
+        xf = self.ra(layer_norm(x) * (1.0 + m[4]) + m[3])
+        hmid = self.ra(gelu_tanh(xf @ self.lw["f1"][layer].T + w.f1_b[layer]))
+        return x + m[5] * (hmid @ self.lw["f2"][layer].T + w.f2_b[layer])
 
     def head(self, x, slot):
         w = self.w

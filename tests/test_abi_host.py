@@ -146,7 +146,7 @@ def test_dit_entry_points_validate_before_any_cuda_call():
     try:
         n = ctypes.c_size_t()
         # model_dim must be heads * head_dim; ffn % 64; 4C % 64; freq even
-        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, ctypes.byref(n)) == wf.WF_OK
+        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, 0, ctypes.byref(n)) == wf.WF_OK
         rows = 5 * 4680
         lat = 16 * 3 * 60 * 104
         want = (rows * 1536 * 4 + rows * 1536 * 2 + rows * 8960 * 2 + rows * 64 * 2 + 2 * 5 * lat * 4
@@ -154,8 +154,14 @@ def test_dit_entry_points_validate_before_any_cuda_call():
         assert want <= n.value <= want + 16 * 256 + 30 * 128
         for bad in ((1535, 8960, 16, 256), (1536, 8961, 16, 256), (1536, 8960, 15, 256),
                     (1536, 8960, 16, 255)):
-            assert wf.lib.wf_dit_workspace_size(h, *bad, ctypes.byref(n)) == wf.WF_EINVAL
-        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, None) == wf.WF_EINVAL
+            assert wf.lib.wf_dit_workspace_size(h, *bad, 0, ctypes.byref(n)) == wf.WF_EINVAL
+        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, 0, None) == wf.WF_EINVAL
+        # e4m3 linear layers add the e4m3 activations and quantised weights
+        n8 = ctypes.c_size_t()
+        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, 1, ctypes.byref(n8)) == wf.WF_OK
+        per_layer = 3 * 1536 * 1536 + 1536 * 1536 + 2 * 1536 * 8960
+        assert n8.value - n.value >= rows * (1536 + 8960) + 30 * per_layer
+        assert wf.lib.wf_dit_workspace_size(h, 1536, 8960, 16, 256, 2, ctypes.byref(n8)) == wf.WF_EINVAL
         m = wf.wf_dit_model()
         assert wf.lib.wf_dit_bind(h, ctypes.byref(m), ctypes.c_void_p(256), None) == wf.WF_EUNBOUND
         assert wf.lib.wf_dit_bind(h, None, ctypes.c_void_p(256), None) == wf.WF_EINVAL

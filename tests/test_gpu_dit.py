@@ -96,14 +96,14 @@ def test_qkv_projection_publish_matches_oracle():
 
 # ---- whole rounds ---------------------------------------------------------------------
 
-def run_request(cfg, grid, heads, dims, std, seed, steps, fp8=None):
+def run_request(cfg, grid, heads, dims, std, seed, steps, fp8=None, linear_fp8=False):
     params = wf_synth.dit_params(seed, dims.dim, dims.ffn, dims.layers, dims.channels, dims.freq,
                                  std=std)
     oracle = dit.Model(cfg, grid, dims, dit.weights_from(params), steps, bf16_points=True,
-                       kv_fp8=fp8)
+                       kv_fp8=fp8, linear_fp8=linear_fp8)
     r = new_round(cfg, grid, heads, dims.layers, fp8)
     model = wf.Dit(r, params, ffn=dims.ffn, channels=dims.channels, freq=dims.freq,
-                   timesteps=steps)
+                   timesteps=steps, linear_fp8=linear_fp8)
     C, F, Hl, Wl = dims.channels, grid[0], 2 * grid[1], 2 * grid[2]
     latent = C * F * Hl * Wl
     worst = [0.0, 0.0, 0.0]
@@ -316,3 +316,15 @@ def test_qkv_projection_publish_fp8():
             assert close(P[sch.raw_anchor_page(cfg), 0, 0].transpose(0, 1), ys[(0, cfg.S)], scales[0])
     assert r.sync_status() == wf.WF_OK
     r.close()
+
+
+
+@pytest.mark.parametrize("fp8", [None, (4.0, 4.0)], ids=["bf16-attention", "e4m3-attention"])
+def test_dit_request_e4m3_linears(fp8):
+    """The block's linear layers in e4m3 (per-channel weight scales, e4m3 LN
+    output, attention output and FFN hidden layer), with bf16 or e4m3
+    attention, against the oracle with the same e4m3 rounding points."""
+    cfg = sch.Cfg(4, 6, 3)
+    mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=0.02, seed=15,
+                                steps=[1000.0, 750.0, 500.0, 250.0], fp8=fp8, linear_fp8=True)
+    assert np.isfinite(mx) and mean <= FP8_MEAN and rel <= FP8_REL, (mx, mean, rel)

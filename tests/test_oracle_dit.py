@@ -281,3 +281,40 @@ def test_sharp_model_tolerance_separates_rounding_from_a_mask_mistake():
     bars = (5e-2, 4e-3, 1e-2)          # SHARP_MAX, SHARP_MEAN, SHARP_REL of tests/test_gpu_dit.py
     assert all(n <= b / 1.5 for n, b in zip(noise, bars)), noise
     assert all(e >= 3 * b for e, b in zip(bad, bars)), bad
+
+
+def test_row_quantisation_e4m3():
+    """Per-row e4m3 weights: the row maximum maps to 448 exactly, each entry
+    is within half an e4m3 step of the original (relative 2^-4 above the
+    subnormal range), and an all-zero row stays zero."""
+    rng = np.random.default_rng(3)
+    w = (rng.normal(size=(6, 40)) * 0.02).astype(np.float32)
+    w[2] = 0.0
+    q = dit.quantize_rows_e4m3(w)
+    sc = np.abs(w).max(axis=1, keepdims=True).astype(np.float64) / 448.0
+    for n in (0, 1, 3, 4, 5):
+        i = np.argmax(np.abs(w[n]))
+        assert np.isclose(abs(q[n, i]), abs(float(w[n, i])), rtol=1e-6)
+    big = np.abs(w) >= 2.0 ** -6 * sc
+    assert np.all(np.abs(q - w)[big] <= 2.0 ** -4 * np.abs(w)[big] * (1 + 1e-6))
+    assert np.all(q[2] == 0.0)
+
+
+def test_linear_fp8_model_runs_and_stays_close():
+    """The e4m3-linear model is the same computation up to e4m3 rounding of
+    weights and activations: close to the bf16 model on a small request."""
+    cfg = sch.Cfg(S=2, n_chunks=3, history=1)
+    dims = dit.Dims(dim=128, heads=1, head_dim=128, ffn=256, layers=1, channels=16, freq=32)
+    grid = (3, 2, 3)
+    params = wf_synth.dit_params(4, dims.dim, dims.ffn, dims.layers, dims.channels, dims.freq,
+                                 std=0.02)
+    a = dit.Model(cfg, grid, dims, dit.weights_from(params), [1000.0, 500.0])
+    b = dit.Model(cfg, grid, dims, dit.weights_from(params), [1000.0, 500.0], linear_fp8=True)
+    for k in range(sch.n_rounds(cfg)):
+        z = lat(4, k, -1, dims, grid)
+        eps = [lat(4, k - s, s, dims, grid) for s in range(2)]
+        xa, _ = a.round(k, z, eps)
+        xb, _ = b.round(k, z, eps)
+        for u, v in zip(xa, xb):
+            rel = np.linalg.norm(u - v) / np.linalg.norm(u)
+            assert 0 < rel < 5e-2, rel
