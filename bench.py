@@ -692,6 +692,7 @@ def main():
     res = run_ours(args, rank, world)
     if not args.no_dit:
         res["dit"] = run_dit(args, "dit13", rank, world, steps=5, warmup=3)
+        res["dit_w8a8"] = run_dit(args, "dit13_w8a8", rank, world, steps=5, warmup=3)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
