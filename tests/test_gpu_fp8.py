@@ -123,3 +123,32 @@ def test_fp8_request_bench_distribution():
     s = 1.0 / np.sqrt(128)
     mx, mean, rel = _request(sch.Cfg(4, 9, 3), SMALL, 3, s, s, (8.0, 8.0), errors)
     assert mx <= 2e-2 and mean <= 2e-3 and rel <= REL, (mx, mean, rel)
+
+
+def test_fp8_wan_shape_sampled_rows():
+    """8-bit attention at the Wan2.1-1.3B shape (S = 4, 4680-token chunks,
+    12 x 128, W = 3) in a steady round with anchor re-rotation, against the
+    oracle with the same e4m3 storage on sampled query rows of 3 heads."""
+    cfg = sch.Cfg(4, 14, 3)
+    geom = Geom(3, 30, 52, 12, 128)
+    heads = [0, 5, 11]
+    s = 1.0 / np.sqrt(128)
+    scales = (8.0, 8.0)
+    r = make_round(cfg, geom, wf.WF_FP8, fp8_scales=scales)
+    raw, traw = raw_fn(21, geom, torch.bfloat16, qk_scale=4 * s, v_scale=1.0, heads=heads)
+    out = r.new_out()
+    k_check = cfg.S + cfg.history + 2
+    for k in range(k_check + 1):
+        info = r.step()
+        r.publish(0, fill_qkv(r, info, traw, 0))
+    r.attention(0, out, wf.WF_ATTN_TC)
+    torch.cuda.synchronize()
+    assert r.sync_status() == wf.WF_OK
+    rows = [0, 1, 127, 128, 2000, 4607, 4608, 4650, 4679]
+    geom_h = Geom(3, 30, 52, len(heads), 128)
+    ref = round_attention(cfg, geom_h, k_check, 0, raw, rows=rows, qk_dtype=Fp8(*scales))
+    for t, o in zip(sch.round_tasks(cfg, k_check), ref):
+        g = out[t.stage][rows][:, heads].float().cpu().numpy()
+        mx, mean, rel = errors(g, o)
+        assert mean <= MEAN and rel <= REL, (t.stage, mx, mean, rel)
+    r.close()
