@@ -455,6 +455,7 @@ def run_ours(args, rank, world):
     # ---- timed: device-resident inputs -----------------------------------
     ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+    ev_pub = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     flops = 0.0
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
@@ -462,6 +463,7 @@ def run_ours(args, rank, world):
         t0.record(stream)
         for i in range(args.steps):
             info = r.step()
+            ev_pub[i].record(stream)
             r.publish(0, qkvs[i % n_in], stream)
             ev_attn[i][0].record(stream)
             r.attention(0, out, wf.WF_ATTN_AUTO, stream)
@@ -472,6 +474,7 @@ def run_ours(args, rank, world):
     clocks = clk.summary()
     ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
+    pub_ms = [a.elapsed_time(b[0]) for a, b in zip(ev_pub, ev_attn)]
     st = r.sync_status()
     if st != wf.WF_OK:
         raise RuntimeError(f"device status {st}")
@@ -531,6 +534,13 @@ def run_ours(args, rank, world):
         # e4m3 tensor peak: the measured bf16 peak times the nominal 4.5 / 2.25 ratio
         peak_tf, peak_kind = 2.0 * peak_tf, "e4m3 dense (burst) = 2 x measured bf16"
     attn_avg = statistics.mean(attn_ms)
+    pub_avg = statistics.mean(pub_ms)
+    # publish: read every task's bf16 Q/K/V, write Q and the K/V pages in the
+    # page dtype, and re-rotate the anchor key (read its unrotated copy, write
+    # the page) -- the window shifts every steady round
+    page_es = 1 if fp8 else 2
+    n_qkv = (S + 1) * NC * 3 * H * D
+    pub_bytes = n_qkv * 2 + n_qkv * page_es + 2 * NC * H * D * page_es
     per_launch = flops / args.steps
     achieved = per_launch / (attn_avg * 1e-3) / 1e12
     value = world * flops / (ms * 1e-3) / 1e12
@@ -564,6 +574,10 @@ def run_ours(args, rank, world):
                      "avg_launch_ms": round(attn_avg, 4),
                      "flops_per_launch": per_launch,
                      "traffic": None if fp8 else ATTN_TC_TRAFFIC_BYTES},
+        "publish": {"bound": "hbm", "kernel": "publish_fp8_kernel" if fp8 else "publish_kernel<bf16>",
+                    "achieved": round(pub_bytes / (pub_avg * 1e-3) / 1e9, 1), "peak": hbm,
+                    "unit": "GB/s", "frac": round(pub_bytes / (pub_avg * 1e-3) / 1e9 / hbm, 4),
+                    "avg_launch_ms": round(pub_avg, 4), "bytes_per_launch": pub_bytes},
         "clocks": clocks,
     }
     return res

@@ -21,7 +21,10 @@
 //  * warps 2-9: epilogue, two warps per TMEM lane quarter (each takes half of
 //    the tile's columns), one accumulator row per thread, tcgen05.ld of 32
 //    columns at a time with the next chunk's load in flight while the
-//    current one is processed; fused elementwise work, direct global stores.
+//    current one is processed; fused elementwise work (packed f32x2
+//    arithmetic), direct global stores -- except the gated residual, whose
+//    32 x 32 blocks go through shared memory into a TMA reduce-add on x, so
+//    the read-modify-write of the fp32 residual stream happens in L2.
 // Every wait is bounded (%globaltimer); on a timeout the kernel records it in
 // the plan's status word, drains its own copies and MMAs, frees TMEM and
 // returns.
@@ -53,9 +56,9 @@ struct Cfg {
     static constexpr int B_FULL = 0, B_EMPTY = NST, B_TFULL = 2 * NST, B_TEMPTY = 2 * NST + 2,
                          B_DRAIN = 2 * NST + 4, NBARS = 2 * NST + 5;
     static constexpr uint32_t SM_MISC = SM_BAR + ((NBARS * 8 + 63) / 64) * 64;
-    // per epilogue warp: a 32 x 32 fp32 staging tile (transposes the residual
-    // read-modify-write into coalesced row segments)
-    static constexpr uint32_t SM_STAGE = SM_MISC + 64;
+    // per epilogue warp: a 32 x 32 fp32 staging tile in the TMA's 128-byte
+    // swizzled layout (1 KB-aligned), the source of the residual reduce-add
+    static constexpr uint32_t SM_STAGE = (SM_MISC + 64 + 1023) / 1024 * 1024;
     static constexpr uint32_t SM_ALLOC = SM_STAGE + 8 * 4096 + 1024;
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
 };
@@ -78,30 +81,114 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// x[box at (c0, c1)] += the shared-memory box at src (fp32 add in L2)
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the bulk copies of this thread have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the bulk copies of this thread are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ float gelu_tanh(float x) {
-    // 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated as
-    // x / (1 + e^(-2u)) since 0.5 (1 + tanh u) = 1 / (1 + e^(-2u)); the
-    // exponent is capped so the divisor stays finite (GELU(x) ~ 0 there).
-    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-    return __fdividef(x, 1.f + __expf(fminf(-2.f * u, 80.f)));
+// Packed f32x2 arithmetic, IEEE round-to-nearest without flushing.
+__device__ __forceinline__ uint64_t p2(float lo, float hi) { return f2_pack(lo, hi); }
+__device__ __forceinline__ uint64_t p2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t p2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t p2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
-// e4m3 operands: accumulator column j times the weight row's scale ws[j]
-__device__ __forceinline__ void scale_cols(uint32_t (&u)[32], const float *ws) {
-    const float4 *w4 = reinterpret_cast<const float4 *>(ws);
+// v = acc (x the e4m3 weight scale of the column when HAS_WS) + bias, as 16
+// packed pairs; bias may be null.
+template <bool HAS_WS>
+__device__ __forceinline__ void affine_cols(const uint32_t (&u)[32], const float *ws,
+                                            const __nv_bfloat16 *bias, uint64_t (&v)[16]) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 w = __ldg(w4 + q);
-        u[4 * q] = __float_as_uint(__uint_as_float(u[4 * q]) * w.x);
-        u[4 * q + 1] = __float_as_uint(__uint_as_float(u[4 * q + 1]) * w.y);
-        u[4 * q + 2] = __float_as_uint(__uint_as_float(u[4 * q + 2]) * w.z);
-        u[4 * q + 3] = __float_as_uint(__uint_as_float(u[4 * q + 3]) * w.w);
+    for (int q = 0; q < 16; ++q) v[q] = p2(__uint_as_float(u[2 * q]), __uint_as_float(u[2 * q + 1]));
+    if constexpr (HAS_WS) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(ws);
+        if (bias) {
+            const uint4 *b4 = reinterpret_cast<const uint4 *>(bias);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 bb = __ldg(b4 + q);
+                const float4 wa = __ldg(w4 + 2 * q), wb = __ldg(w4 + 2 * q + 1);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&bb);
+                const float2 b0 = __bfloat1622float2(h2[0]), b1 = __bfloat1622float2(h2[1]);
+                const float2 b2 = __bfloat1622float2(h2[2]), b3 = __bfloat1622float2(h2[3]);
+                v[4 * q] = p2_fma(v[4 * q], p2(wa.x, wa.y), p2(b0.x, b0.y));
+                v[4 * q + 1] = p2_fma(v[4 * q + 1], p2(wa.z, wa.w), p2(b1.x, b1.y));
+                v[4 * q + 2] = p2_fma(v[4 * q + 2], p2(wb.x, wb.y), p2(b2.x, b2.y));
+                v[4 * q + 3] = p2_fma(v[4 * q + 3], p2(wb.z, wb.w), p2(b3.x, b3.y));
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 w = __ldg(w4 + q);
+                v[2 * q] = p2_mul(v[2 * q], p2(w.x, w.y));
+                v[2 * q + 1] = p2_mul(v[2 * q + 1], p2(w.z, w.w));
+            }
+        }
+    } else if (bias) {
+        const uint4 *b4 = reinterpret_cast<const uint4 *>(bias);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 bb = __ldg(b4 + q);
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&bb);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h2[e]);
+                v[4 * q + e] = p2_add(v[4 * q + e], p2(f.x, f.y));
+            }
+        }
     }
+}
+
+// GELU, tanh form 0.5 x (1 + tanh u), u = sqrt(2/pi) (x + 0.044715 x^3), on a
+// packed pair, evaluated as x / (1 + 2^a) with a = -2 log2(e) u, since
+// 0.5 (1 + tanh u) = 1 / (1 + e^(-2u)): accurate in relative terms also where
+// GELU(x) is tiny.  a is capped at 126 so that 1 + 2^a stays finite.
+__device__ __forceinline__ uint64_t gelu2(uint64_t x) {
+    constexpr float G0 = -2.0f * 1.4426950408889634f * 0.7978845608028654f;
+    constexpr float G1 = G0 * 0.044715f;
+    const uint64_t a2 = p2_mul(x, p2_fma(p2_mul(x, x), p2(G1, G1), p2(G0, G0)));
+    float a0, a1;
+    f2_unpack(a2, a0, a1);
+    const uint64_t d = p2_add(p2(1.f, 1.f), p2(ex2(fminf(a0, 126.f)), ex2(fminf(a1, 126.f))));
+    float d0, d1;
+    f2_unpack(d, d0, d1);
+    return p2_mul(x, p2(rcp_approx(d0), rcp_approx(d1)));
 }
 
 // ---- epilogues -----------------------------------------------------------------
@@ -124,37 +211,41 @@ struct Epi<WF_EPI_BF16> {
 };
 template <>
 struct Epi<WF_EPI_GELU_BF16> {
-    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+    __device__ static void apply2(const GemmParams &p, int row, int col, uint64_t (&v2)[16]) {
+        float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+        for (int q = 0; q < 16; ++q) f2_unpack(gelu2(v2[q]), v[2 * q], v[2 * q + 1]);
         Epi<WF_EPI_BF16>::apply(p, row, col, v);
     }
 };
-// GELU for an e4m3 output: 0.5 x (1 + tanh u) with the hardware tanh
-// approximation (relative error about 2^-11, far below the e4m3 step 2^-4 and
-// at most ~1e-3 absolute where the result is tiny).
-__device__ __forceinline__ float gelu_tanh_fast(float x) {
-    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(u));
-    const float hx = 0.5f * x;
-    return fmaf(hx, t, hx);
+// GELU for an e4m3 output on a packed pair: 0.5 x (1 + tanh u) with the
+// hardware tanh approximation (relative error about 2^-11, far below the
+// e4m3 step 2^-4 and at most ~1e-3 absolute where the result is tiny).
+__device__ __forceinline__ uint64_t gelu2_fast(uint64_t x) {
+    constexpr float C0 = 0.7978845608028654f;
+    constexpr float C1 = C0 * 0.044715f;
+    const uint64_t u2 = p2_mul(x, p2_fma(p2_mul(x, x), p2(C1, C1), p2(C0, C0)));
+    float u0, u1, t0, t1;
+    f2_unpack(u2, u0, u1);
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(u0));
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(u1));
+    const uint64_t hx = p2_mul(x, p2(0.5f, 0.5f));
+    return p2_fma(hx, p2(t0, t1), hx);
+}
+__device__ __forceinline__ uint32_t e4m3x2_of(uint64_t v) {
+    float a, b;
+    f2_unpack(v, a, b);
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
 // FFN hidden layer for an e4m3 FFN2: GELU, then e4m3 bytes (unit scale)
 template <>
 struct Epi<WF_EPI_GELU_E4M3> {
-    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+    __device__ static void apply2(const GemmParams &p, int row, int col, uint64_t (&v2)[16]) {
         uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-                make_float2(gelu_tanh_fast(v[4 * i]), gelu_tanh_fast(v[4 * i + 1])), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-                make_float2(gelu_tanh_fast(v[4 * i + 2]), gelu_tanh_fast(v[4 * i + 3])), __NV_SATFINITE,
-                __NV_E4M3);
-            w[i] = lo | (hi << 16);
-        }
+        for (int i = 0; i < 8; ++i)
+            w[i] = e4m3x2_of(gelu2_fast(v2[2 * i])) | (e4m3x2_of(gelu2_fast(v2[2 * i + 1])) << 16);
         uint4 *d4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) + (size_t)row * p.ldo + col);
         d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -169,7 +260,8 @@ struct Epi<WF_EPI_F32> {
     }
 };
 // The gated residual add x += gate[group(row)][col] * (acc + bias) of the
-// attention and FFN halves of a block runs through residual_staged below.
+// attention and FFN halves of a block is in the kernel body: it stages each
+// 32 x 32 block for a TMA reduce-add.
 
 // QKV projection epilogue: columns [0, dim) are Q, [dim, 2 dim) K, [2 dim,
 // 3 dim) V, head h at columns h*D .. h*D + D - 1 of each part.  RoPE on Q and
@@ -300,54 +392,12 @@ struct Epi<WF_EPI_HEAD> {
     }
 };
 
-// Gated residual add from a staged 32 x 32 block (row r at stg[r * 32],
-// 16-byte units swizzled by r & 7): lane l takes column pair l & 15 of rows
-// 2i + (l >> 4), i = 0..15, in four batches whose loads of x and the gates
-// are all issued before their stores.  row0 is the block's first row, col0
-// its first column.
-__device__ __forceinline__ void residual_staged(const GemmParams &p, const float *stg, int lane,
-                                                int row0, int col0) {
-    const int cp = lane & 15, rp = lane >> 4;
-    const int col = col0 + 2 * cp;
-    float2 b = make_float2(0.f, 0.f);
-    if (p.bias) b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p.bias + col));
-    const int rpg = p.rows_per_group;
-    const int g_lo = row0 / rpg, g_bnd = (g_lo + 1) * rpg;
-    float *out = static_cast<float *>(p.out);
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {          // four batches of 4 row pairs
-        float2 xv[4], gv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = row0 + 2 * (4 * h + i) + rp;
-            if (row < p.row_end) {
-                const int grp = rpg >= 32 ? g_lo + (row >= g_bnd ? 1 : 0) : row / rpg;
-                xv[i] = *reinterpret_cast<const float2 *>(out + (size_t)row * p.ldo + col);
-                gv[i] = __ldg(reinterpret_cast<const float2 *>(p.gate + (size_t)grp * p.gate_ld + col));
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 2 * (4 * h + i) + rp;
-            const int row = row0 + r;
-            const float2 a = *reinterpret_cast<const float2 *>(stg + r * 32 +
-                                                               (((cp >> 1) ^ (r & 7)) * 4) + (cp & 1) * 2);
-            if (row < p.row_end) {
-                float2 x = xv[i];
-                x.x = fmaf(gv[i].x, a.x + b.x, x.x);
-                x.y = fmaf(gv[i].y, a.y + b.y, x.y);
-                *reinterpret_cast<float2 *>(out + (size_t)row * p.ldo + col) = x;
-            }
-        }
-    }
-}
-
 // ---- kernel -----------------------------------------------------------------------
 
 template <int BN, int EPI, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tc, const GemmParams p) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -442,16 +492,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int NPW = BN / 64;                // 32-column chunks per warp
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
         const int half = (warp - 2) >> 2;           // which half of the columns
-        const int row_in = quarter * 32 + lane;
         uint32_t tl = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
             const int buf = tl & 1;
             bool ok = r.wait(bar(C::B_TFULL + buf), (tl >> 1) & 1, 4);
             if (!__all_sync(0xffffffffu, ok)) goto done;
             tc_fence_after();
-            const int row = p.row_begin + (tile / p.tiles_n) * BM + row_in;
+            const int rel_row0 = (tile / p.tiles_n) * BM + quarter * 32;   // warp's first row - row_begin
+            const int row = p.row_begin + rel_row0 + lane;
             const int n0 = (tile % p.tiles_n) * BN + half * (BN / 2);
             const bool live = row < p.row_end;
+            int grp = 0;
+            if constexpr (EPI == WF_EPI_GATED_RESIDUAL) grp = live ? row / p.rows_per_group : 0;
             const uint32_t taddr =
                 tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2);
             uint32_t u[2][32];
@@ -470,51 +522,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const int col = n0 + c * 32;
                 if constexpr (EPI == WF_EPI_GATED_RESIDUAL) {
-                    // Stage the 32 x 32 block through shared memory so that the
-                    // fp32 read-modify-write of x covers two full 128-byte row
-                    // segments per warp instruction instead of 32 rows.
+                    // y = gate[group(row)] * (acc + b) staged as a 32 x 32
+                    // block (row = lane, 16-byte units swizzled by row & 7, the
+                    // TMA's 128-byte pattern), then x[block] += y by a TMA
+                    // reduce-add; rows past row_end are clipped by the map.
                     if (col < p.N) {
-                        uint32_t(&uc)[32] = u[c & 1];
-                        if (F8) scale_cols(uc, p.wscale + col);
-                        float *stg = reinterpret_cast<float *>(smem + C::SM_STAGE) + (warp - 2) * 1024;
-                        float4 *srow = reinterpret_cast<float4 *>(stg + lane * 32);
+                        uint64_t v2[16];
+                        affine_cols<F8>(u[c & 1], F8 ? p.wscale + col : nullptr, p.bias ? p.bias + col : nullptr, v2);
+                        if (live) {
+                            const float4 *g4 = reinterpret_cast<const float4 *>(
+                                p.gate + (size_t)grp * p.gate_ld + col);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            srow[q ^ (lane & 7)] =
-                                make_float4(__uint_as_float(uc[4 * q]), __uint_as_float(uc[4 * q + 1]),
-                                            __uint_as_float(uc[4 * q + 2]), __uint_as_float(uc[4 * q + 3]));
-                        __syncwarp();
-                        residual_staged(p, stg, lane, row - lane, col);
-                        __syncwarp();
-                    }
-                } else if (live && col < p.N) {
-                    uint32_t(&uc)[32] = u[c & 1];
-                    if (F8) scale_cols(uc, p.wscale + col);
-                    float v[32];
-                    if (p.bias) {
-                        const uint4 *b4 = reinterpret_cast<const uint4 *>(p.bias + col);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 bb = __ldg(b4 + q);
-                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&bb);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                float2 f = __bfloat1622float2(h2[e]);
-                                v[8 * q + 2 * e] = __uint_as_float(uc[8 * q + 2 * e]) + f.x;
-                                v[8 * q + 2 * e + 1] = __uint_as_float(uc[8 * q + 2 * e + 1]) + f.y;
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 gv = __ldg(g4 + q);
+                                v2[2 * q] = p2_mul(v2[2 * q], p2(gv.x, gv.y));
+                                v2[2 * q + 1] = p2_mul(v2[2 * q + 1], p2(gv.z, gv.w));
                             }
                         }
-                    } else {
+                        float *stg = reinterpret_cast<float *>(smem + C::SM_STAGE) + (warp - 2) * 1024;
+                        if (lane == 0) bulk_wait_read();      // the previous block has left stg
+                        __syncwarp();
+                        float4 *srow = reinterpret_cast<float4 *>(stg + lane * 32);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(uc[i]);
+                        for (int q = 0; q < 8; ++q) {
+                            float a0, a1, a2, a3;
+                            f2_unpack(v2[2 * q], a0, a1);
+                            f2_unpack(v2[2 * q + 1], a2, a3);
+                            srow[q ^ (lane & 7)] = make_float4(a0, a1, a2, a3);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_2d(&tc, smem_u32(stg), col, rel_row0);
+                            bulk_commit();
+                        }
                     }
-                    Epi<EPI>::apply(p, row, col, v);
+                } else if (live && col < p.N) {
+                    uint64_t v2[16];
+                    affine_cols<F8>(u[c & 1], F8 ? p.wscale + col : nullptr, p.bias ? p.bias + col : nullptr, v2);
+                    if constexpr (EPI == WF_EPI_GELU_BF16 || EPI == WF_EPI_GELU_E4M3) {
+                        Epi<EPI>::apply2(p, row, col, v2);
+                    } else {
+                        float v[32];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) f2_unpack(v2[q], v[2 * q], v[2 * q + 1]);
+                        Epi<EPI>::apply(p, row, col, v);
+                    }
                 }
                 if (c + 1 < NPW) tmem_wait_ld(u[(c + 1) & 1]);
             }
         }
     }
 done:
+    if constexpr (EPI == WF_EPI_GATED_RESIDUAL) {
+        // the reduce-adds this warp issued have completed (shared memory is
+        // released when the CTA exits)
+        if (warp >= 2 && lane == 0) bulk_wait_all();
+    }
     if (*r.abort) {
         if (warp == 0 && lane == 0) {
             uint32_t first = issued > (uint32_t)C::NST ? issued - C::NST : 0;
@@ -534,8 +598,8 @@ done:
 }
 
 template <int BN, int EPI, bool F8>
-cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int num_sms,
-                   cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                   const GemmParams &p, int num_sms, cudaStream_t stream) {
     using C = Cfg<BN>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -546,7 +610,7 @@ cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParam
     }
     const int n_tiles = p.tiles_m * p.tiles_n;
     const int grid = n_tiles < num_sms ? n_tiles : num_sms;
-    gemm_tc_kernel<BN, EPI, F8><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, p);
+    gemm_tc_kernel<BN, EPI, F8><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, tc, p);
     return cudaGetLastError();
 }
 
@@ -597,30 +661,46 @@ cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, co
     if (p.K % ke || p.N % 32 || lda % (f8 ? 16 : 8) || p.row_end <= p.row_begin)
         return cudaErrorInvalidValue;
     if (f8 && !p.wscale) return cudaErrorInvalidValue;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     if (!encode_2d(&ta, a, a_rows, p.K, lda, BM, f8)) return cudaErrorInvalidValue;
     if (!encode_2d(&tb, w, p.N, p.K, p.K, bn, f8)) return cudaErrorInvalidValue;
+    tc = ta;   // unused unless the epilogue reduces into x
+    if (epi == WF_EPI_GATED_RESIDUAL) {
+        // fp32 x rows [row_begin, row_end), 32 x 32 boxes, 128-byte swizzle
+        float *x0 = static_cast<float *>(p.out) + (size_t)p.row_begin * p.ldo;
+        if (p.ldo % 4 || reinterpret_cast<uintptr_t>(x0) % 16) return cudaErrorInvalidValue;
+        EncodeFn enc = encoder();
+        if (!enc) return cudaErrorInvalidValue;
+        const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)(p.row_end - p.row_begin)};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.ldo * 4};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, x0, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     p.tiles_m = (p.row_end - p.row_begin + BM - 1) / BM;
     p.tiles_n = (p.N + bn - 1) / bn;
     if (f8) {
         switch (epi) {
-            case WF_EPI_BF16: return launch<256, WF_EPI_BF16, true>(ta, tb, p, num_sms, stream);
-            case WF_EPI_F32: return launch<256, WF_EPI_F32, true>(ta, tb, p, num_sms, stream);
-            case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, true>(ta, tb, p, num_sms, stream);
-            case WF_EPI_GELU_E4M3: return launch<256, WF_EPI_GELU_E4M3, true>(ta, tb, p, num_sms, stream);
+            case WF_EPI_BF16: return launch<256, WF_EPI_BF16, true>(ta, tb, tc, p, num_sms, stream);
+            case WF_EPI_F32: return launch<256, WF_EPI_F32, true>(ta, tb, tc, p, num_sms, stream);
+            case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, true>(ta, tb, tc, p, num_sms, stream);
+            case WF_EPI_GELU_E4M3: return launch<256, WF_EPI_GELU_E4M3, true>(ta, tb, tc, p, num_sms, stream);
             case WF_EPI_GATED_RESIDUAL:
-                return launch<256, WF_EPI_GATED_RESIDUAL, true>(ta, tb, p, num_sms, stream);
-            case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, true>(ta, tb, p, num_sms, stream);
+                return launch<256, WF_EPI_GATED_RESIDUAL, true>(ta, tb, tc, p, num_sms, stream);
+            case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, true>(ta, tb, tc, p, num_sms, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (epi) {
-        case WF_EPI_BF16: return launch<256, WF_EPI_BF16, false>(ta, tb, p, num_sms, stream);
-        case WF_EPI_F32: return launch<256, WF_EPI_F32, false>(ta, tb, p, num_sms, stream);
-        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, false>(ta, tb, p, num_sms, stream);
-        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL, false>(ta, tb, p, num_sms, stream);
-        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, false>(ta, tb, p, num_sms, stream);
-        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD, false>(ta, tb, p, num_sms, stream);
+        case WF_EPI_BF16: return launch<256, WF_EPI_BF16, false>(ta, tb, tc, p, num_sms, stream);
+        case WF_EPI_F32: return launch<256, WF_EPI_F32, false>(ta, tb, tc, p, num_sms, stream);
+        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, false>(ta, tb, tc, p, num_sms, stream);
+        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL, false>(ta, tb, tc, p, num_sms, stream);
+        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, false>(ta, tb, tc, p, num_sms, stream);
+        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD, false>(ta, tb, tc, p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
