@@ -286,19 +286,20 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
     h_eps.copy_(epss[0].cpu())
     h_out = torch.empty(latent, dtype=torch.float32).pin_memory()
     d_z, d_eps = torch.empty_like(zs[0]), torch.empty_like(epss[0])
-    e2e_steps = 2
+    e2e_steps = steps                       # as many chunks as the device-timed region
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for _ in range(per_step):
-            d_z.copy_(h_z, non_blocking=True)
-            d_eps.copy_(h_eps, non_blocking=True)
-            r.step()
-            model.round(d_z, d_eps, None, chunk, stream)
-        h_out.copy_(chunk, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk_e2e:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for _ in range(per_step):
+                d_z.copy_(h_z, non_blocking=True)
+                d_eps.copy_(h_eps, non_blocking=True)
+                r.step()
+                model.round(d_z, d_eps, None, chunk, stream)
+            h_out.copy_(chunk, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
     ms, e2e_ms = max_over_ranks([t0.elapsed_time(t1), e0.elapsed_time(e1)], world, dev)
     chunks_s = world * steps / (ms * 1e-3)
     peak, src = _sustained_peak()
@@ -317,7 +318,8 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
            "unit": "chunks/s", "forwards_per_chunk_timed": per_step,
            "e2e": {"value": round(world * e2e_steps / (e2e_ms * 1e-3), 3), "unit": "chunks/s",
                    "h2d_bytes_per_step": per_step * (h_z.numel() + h_eps.numel()) * 4,
-                   "d2h_bytes_per_step": h_out.numel() * 4, "steps": e2e_steps},
+                   "d2h_bytes_per_step": h_out.numel() * 4, "steps": e2e_steps,
+                   "clocks": clk_e2e.summary()},
            "frames_per_s": round(12 * chunks_s, 2),
            "ms_per_chunk_p50": round(statistics.median(per), 3),
            "chunks_timed": steps,

@@ -68,6 +68,61 @@ __global__ void __launch_bounds__(256) ln_mod_kernel(const float *__restrict__ x
     }
 }
 
+// The same with the row held in registers (NV float4 per lane, dim = 128 NV):
+// x is read from memory once, all of a lane's loads in flight together.
+template <bool F8, int NV>
+__global__ void __launch_bounds__(256) ln_mod_reg_kernel(const float *__restrict__ x,
+                                                         void *__restrict__ out, int row_begin,
+                                                         int row_end, int NC,
+                                                         const float *__restrict__ mod, int mod_ld,
+                                                         int shift_off, int scale_off) {
+    constexpr int dim = 128 * NV;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row = row_begin + warp;
+    if (row >= row_end) return;
+    const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)row * dim);
+    float4 v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = xr[lane + 32 * k];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mean = s / dim;
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const float a = v[k].x - mean, b = v[k].y - mean, c = v[k].z - mean, d = v[k].w - mean;
+        q += (a * a + b * b) + (c * c + d * d);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float rstd = rsqrtf(q / dim + 1e-6f);
+    const int slot = row / NC;
+    const float4 *sh = reinterpret_cast<const float4 *>(mod + (size_t)slot * mod_ld + shift_off);
+    const float4 *sc = reinterpret_cast<const float4 *>(mod + (size_t)slot * mod_ld + scale_off);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int i = lane + 32 * k;
+        const float4 a = __ldg(sh + i), b = __ldg(sc + i);
+        const float y0 = fmaf((v[k].x - mean) * rstd, 1.f + b.x, a.x);
+        const float y1 = fmaf((v[k].y - mean) * rstd, 1.f + b.y, a.y);
+        const float y2 = fmaf((v[k].z - mean) * rstd, 1.f + b.z, a.z);
+        const float y3 = fmaf((v[k].w - mean) * rstd, 1.f + b.w, a.w);
+        if constexpr (F8) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y2, y3), __NV_SATFINITE, __NV_E4M3);
+            reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(out) + (size_t)row * dim)[i] = lo | (hi << 16);
+        } else {
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(y0, y1), p1 = __floats2bfloat162_rn(y2, y3);
+            reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + (size_t)row * dim)[i] =
+                make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
+        }
+    }
+}
+
 // ---- patchify -------------------------------------------------------------------
 // Row n of slot s: features (channel c, row offset q, column offset r) of the
 // 2 x 2 patch of token (f, h, w); one thread per (token, channel).
@@ -228,6 +283,20 @@ cudaError_t wf_launch_ln_mod(const float *x, void *out, int row_begin, int row_e
     if (dim % 4 || row_end <= row_begin) return cudaErrorInvalidValue;
     const int rows = row_end - row_begin;
     const int blocks = (rows + 7) / 8;
+#define WF_LN_REG(NV)                                                                                  \
+    if (dim == 128 * NV) {                                                                             \
+        if (out_e4m3)                                                                                  \
+            ln_mod_reg_kernel<true, NV><<<blocks, 256, 0, stream>>>(x, out, row_begin, row_end, NC, mod,  \
+                                                                    mod_ld, shift_off, scale_off);     \
+        else                                                                                           \
+            ln_mod_reg_kernel<false, NV><<<blocks, 256, 0, stream>>>(x, out, row_begin, row_end, NC, mod, \
+                                                                     mod_ld, shift_off, scale_off);    \
+        return cudaGetLastError();                                                                     \
+    }
+    WF_LN_REG(12)   // dim 1536 (Wan2.1-1.3B)
+    WF_LN_REG(16)   // dim 2048
+    WF_LN_REG(2)    // dim 256
+#undef WF_LN_REG
     if (out_e4m3)
         ln_mod_kernel<true><<<blocks, 256, 0, stream>>>(x, out, row_begin, row_end, dim, NC, mod, mod_ld,
                                                         shift_off, scale_off);

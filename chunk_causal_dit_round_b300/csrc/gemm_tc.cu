@@ -306,16 +306,35 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
         else
             store32(p.qbuf + off, v);
     }
-    __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
+    // What a row needs, computed once per tile: its slot, token, task, and
+    // the offsets (in float2 units, to be added to the pair index m) of its
+    // rotary rows in the t / h / w tables.
+    struct Row {
+        int slot, n, ti;
+        int t_off, h_off, w_off;
+    };
+    __device__ static Row row_info(const GemmParams &p, int row) {
+        const WfGeom &g = p.g;
+        Row r;
+        r.slot = row / g.NC;
+        r.n = row - r.slot * g.NC;
+        r.ti = p.slot_task[r.slot];
+        const int hw = g.gh * g.gw;
+        const int f = r.n / hw, hh = (r.n / g.gw) % g.gh, ww = r.n - (r.n / g.gw) * g.gw;
+        const int t = g.gt * p.rd.chunk[r.ti] + f;
+        r.t_off = g.rope_t_off + t * g.dt2;
+        r.h_off = g.rope_h_off + hh * g.dh2 - g.dt2;
+        r.w_off = g.rope_w_off + ww * g.dw2 - g.dt2 - g.dh2;
+        return r;
+    }
+    __device__ static void apply(const GemmParams &p, const Row &ri, int col, float (&v)[32]) {
         const WfGeom &g = p.g;
         const int dim = g.H * g.D;
         const int part = col / dim;                 // 0 Q, 1 K, 2 V
         const int cc = col - part * dim;
         const int h = cc / g.D;
         const int d0 = cc - h * g.D;                // 32 consecutive channels d0 .. d0 + 31
-        const int slot = row / g.NC;
-        const int n = row - slot * g.NC;
-        const int ti = p.slot_task[slot];
+        const int slot = ri.slot, n = ri.n, ti = ri.ti;
         const size_t plane = (size_t)g.NC * g.D;
         if (part == 2) {
             size_t kvp = (((size_t)p.rd.dest[ti] * g.L + p.layer) * 2 + 1) * g.H + h;
@@ -326,23 +345,19 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
             size_t rawp = (((size_t)g.raw_anchor_page * g.L + p.layer) * 2) * g.H + h;
             put(p, rawp * plane + (size_t)n * g.D + d0, v, g.qk_scale);
         }
-        const int hw = g.gh * g.gw;
-        const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n - (n / g.gw) * g.gw;
-        const int t = g.gt * p.rd.chunk[ti] + f;
         const float2 *tab = p.rope;
+        float2 cs[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int m = d0 / 2 + i;
-            float2 cs;
-            if (m < g.dt2)
-                cs = __ldg(tab + g.rope_t_off + t * g.dt2 + m);
-            else if (m < g.dt2 + g.dh2)
-                cs = __ldg(tab + g.rope_h_off + hh * g.dh2 + (m - g.dt2));
-            else
-                cs = __ldg(tab + g.rope_w_off + ww * g.dw2 + (m - g.dt2 - g.dh2));
+            const int off = m < g.dt2 ? ri.t_off : (m < g.dt2 + g.dh2 ? ri.h_off : ri.w_off);
+            cs[i] = __ldg(tab + off + m);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
             const float a = v[2 * i], b = v[2 * i + 1];
-            v[2 * i] = a * cs.x - b * cs.y;
-            v[2 * i + 1] = a * cs.y + b * cs.x;
+            v[2 * i] = a * cs[i].x - b * cs[i].y;
+            v[2 * i + 1] = a * cs[i].y + b * cs[i].x;
         }
         if (part == 0) {
             putq(p, ((size_t)slot * g.H + h) * plane + (size_t)n * g.D + d0, v, g.qk_scale);
@@ -390,6 +405,17 @@ struct Epi<WF_EPI_HEAD> {
             }
         }
     }
+};
+
+// per-row state kept across a tile's column chunks (only the QKV epilogue has any)
+struct NoRow {};
+template <int EPI>
+struct QkvRowT {
+    using type = NoRow;
+};
+template <>
+struct QkvRowT<WF_EPI_QKV_PUBLISH> {
+    using type = Epi<WF_EPI_QKV_PUBLISH>::Row;
 };
 
 // ---- kernel -----------------------------------------------------------------------
@@ -504,6 +530,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool live = row < p.row_end;
             int grp = 0;
             if constexpr (EPI == WF_EPI_GATED_RESIDUAL) grp = live ? row / p.rows_per_group : 0;
+            typename QkvRowT<EPI>::type qrow{};
+            if constexpr (EPI == WF_EPI_QKV_PUBLISH)
+                if (live) qrow = Epi<WF_EPI_QKV_PUBLISH>::row_info(p, row);
             const uint32_t taddr =
                 tmem + ((uint32_t)(quarter * 32) << 16) + buf * BN + half * (BN / 2);
             uint32_t u[2][32];
@@ -566,7 +595,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int q = 0; q < 16; ++q) f2_unpack(v2[q], v[2 * q], v[2 * q + 1]);
-                        Epi<EPI>::apply(p, row, col, v);
+                        if constexpr (EPI == WF_EPI_QKV_PUBLISH)
+                            Epi<EPI>::apply(p, qrow, col, v);
+                        else
+                            Epi<EPI>::apply(p, row, col, v);
                     }
                 }
                 if (c + 1 < NPW) tmem_wait_ld(u[(c + 1) & 1]);

@@ -89,6 +89,32 @@ def test_row_range_and_gated_residual(plan):
     assert np.abs(got - ref).max() <= 3 * tol_f32(K)
 
 
+@pytest.mark.parametrize("M,N,K,r0,r1,G", [
+    (300, 800, 192, 37, 300, 7),        # ragged 32-column remainder, groups smaller than a warp
+    (517, 256, 1536, 129, 390, 200),    # row range starting inside a tile, ragged last tile
+    (64, 1536, 64, 0, 1, 1),            # a single row
+])
+def test_gated_residual_ranges(plan, M, N, K, r0, r1, G):
+    """x += gate[row // G] * (A W^T + b) on rows [r0, r1) only, through the
+    reduce-add epilogue; every other element of x keeps its bits."""
+    a, w, b = operands(11, M, N, K)
+    n_groups = (M + G - 1) // G
+    gate = wf_synth.normal(wf_synth.key_of(11, 9), (n_groups, N), 1.0, torch.float32)
+    x0 = wf_synth.normal(wf_synth.key_of(11, 10), (M, N), 1.0, torch.float32)
+    out = x0.clone().cuda()
+    plan.linear(a.cuda(), w.cuda(), b.cuda(), out, wf.WF_EPI_GATED_RESIDUAL, row_begin=r0,
+                row_end=r1, gate=gate.cuda(), rows_per_group=G)
+    torch.cuda.synchronize()
+    got = out.cpu().double().numpy()
+    ref = x0.double().numpy().copy()
+    ref[r0:r1] += gate.double().numpy()[np.arange(r0, r1) // G] * ref_linear(a, w, b, r0, r1)
+    keep = np.ones(M, dtype=bool)
+    keep[r0:r1] = False
+    assert np.array_equal(got[keep], x0.double().numpy()[keep])
+    assert np.abs(got - ref).max() <= 3 * tol_f32(K)
+    assert plan.sync_status() == wf.WF_OK
+
+
 def test_no_bias(plan):
     M, N, K = 200, 256, 128
     a, w, _ = operands(4, M, N, K)
