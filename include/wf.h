@@ -238,11 +238,16 @@ int wf_round_attention_noalloc(wf_plan_t plan, int layer, void *out, cudaStream_
  *   w     bf16 [N][K] row-major weight of a linear layer, output-major (device)
  *   bias  bf16 [N] or NULL
  *   out   WF_EPI_BF16 / WF_EPI_GELU_BF16: bf16 [.][ldo]; WF_EPI_F32 and
- *         WF_EPI_GATED_RESIDUAL: float [.][ldo] (read-modify-write for the
- *         latter); row r of out corresponds to row r of a
+ *         WF_EPI_GATED_RESIDUAL: float [.][ldo]; row r of out corresponds to
+ *         row r of a.  For the gated residual, out[r] += gate-row * (A W^T +
+ *         bias)[r]: the sum is added in place by the GPU's memory system (a
+ *         tensor reduce-add per 32 x 32 block), once per element, only on
+ *         rows row_begin .. row_end-1; nothing else may write those rows
+ *         while the call runs
  *   gate  WF_EPI_GATED_RESIDUAL only: float rows of gate_ld values, row
  *         r / rows_per_group gates output row r (one gate vector per task slot
- *         when rows_per_group = N_C)
+ *         when rows_per_group = N_C); at least (row_end - 1) / rows_per_group
+ *         + 1 rows
  * These are the dense operators of one DiT block ("Wave Forcing" Sec. 4.1:
  * attention and "the remaining block" of the standard Wan2.1 transformer,
  * App. D.2): output projection and FFN with gated residual adds, GELU FFN
