@@ -12,8 +12,15 @@ wf_round_attention (one launch over all 5 tasks).  Inputs are seeded
 synthetic tensors already resident in HBM; each step reads > 126 MB (larger
 than L2), so no explicit flush is needed.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
-a bounded sample of the same round instead.
+Prints one JSON line (rank 0): the attention TFLOP/s with the attention
+kernel's roofline (CUDA-event time per launch against the measured peak),
+the publish kernel's GB/s against the measured HBM bandwidth, the same
+metric end to end with host buffers (``e2e``), the clocks seen during the
+timed region, the oracle timed on the host cores (``cpu_baseline``), and the
+whole DiT round (chunks/s, frames/s) for the bf16 model (``dit``) and the
+8-bit one (``dit_w8a8``).  ``--config`` selects the other workloads;
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+round instead.
 """
 
 from __future__ import annotations
@@ -34,10 +41,13 @@ sys.path.insert(0, ROOT)
 METRIC = "chunk-causal attention TFLOP/s (% bf16 peak); DiT chunks/s per 1F1C round"
 UNIT = "TFLOP/s"
 
-# DRAM bytes (read + write) of one steady attn_tc_kernel launch, from the ncu
-# capture summarised in profiles/attn_tc_kernel_wan13_round.md.  Set to None
-# whenever the kernel changes, until it is captured again.
-ATTN_TC_TRAFFIC_BYTES = 1.259e9
+# DRAM bytes (read + write) of one steady attn_tc_kernel launch (bf16 and
+# e4m3 pages), from the ncu captures summarised in
+# profiles/attn_tc_kernel_wan13_round.md and
+# profiles/attn_tc_kernel_fp8_wan13_round.md.  Set to None whenever the
+# kernel changes, until it is captured again.
+ATTN_TC_TRAFFIC_BYTES = 1.2571e9
+ATTN_TC_FP8_TRAFFIC_BYTES = 6.061e8
 
 CONFIGS = {
     # name: (S, grid (t,h,w), heads, head_dim, history W)
@@ -575,7 +585,7 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_src} {peak_kind}",
                      "avg_launch_ms": round(attn_avg, 4),
                      "flops_per_launch": per_launch,
-                     "traffic": None if fp8 else ATTN_TC_TRAFFIC_BYTES},
+                     "traffic": ATTN_TC_FP8_TRAFFIC_BYTES if fp8 else ATTN_TC_TRAFFIC_BYTES},
         "publish": {"bound": "hbm", "kernel": "publish_fp8_kernel" if fp8 else "publish_kernel<bf16>",
                     "achieved": round(pub_bytes / (pub_avg * 1e-3) / 1e9, 1), "peak": hbm,
                     "unit": "GB/s", "frac": round(pub_bytes / (pub_avg * 1e-3) / 1e9 / hbm, 4),
