@@ -3,6 +3,8 @@ the same bf16 operands: plain bf16 / f32 outputs, the GELU hidden layer and
 the gated residual add of the DiT block ("Wave Forcing" Sec. 4.1, the
 remaining block of a Wan2.1 transformer layer)."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -170,4 +172,36 @@ def test_e4m3_linear_epilogues(plan, M, N, K):
     torch.cuda.synchronize()
     want = x0.double().numpy() + gate.double().numpy()[np.arange(M) // 200] * ref
     assert np.abs(x.cpu().double().numpy() - want).max() <= 3e-4 * np.sqrt(K) * max(1.0, np.abs(ref).max())
+    assert plan.sync_status() == wf.WF_OK
+
+
+def test_argument_checks_reject_before_launch(plan):
+    """Arguments wf_linear cannot serve are rejected with an error code and
+    launch nothing: a gated residual without a gate or with rows_per_group 0,
+    a misaligned output pitch, rows outside A, K not a multiple of 64."""
+    M, N, K = 256, 256, 128
+    a, w, b = (t.cuda() for t in operands(12, M, N, K))
+    out = torch.zeros((M, N), device="cuda")
+    gate = torch.ones((2, N), device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    lib, h = wf.lib, plan.plan
+
+    def call(row_begin=0, row_end=M, epi=wf.WF_EPI_GATED_RESIDUAL, g=gate, g_ld=N, rpg=200, ldo=N,
+             k=K, a_rows=M):
+        return lib.wf_linear(h, P(a), a_rows, K, row_begin, row_end, P(w), P(b), N, k, epi, P(out), ldo,
+                             P(g), g_ld, rpg, None)
+
+    x0 = out.clone()
+    assert call(g=None) == wf.WF_EINVAL
+    assert call(rpg=0) == wf.WF_EINVAL
+    assert call(g_ld=N - 4) == wf.WF_EINVAL
+    assert call(ldo=N + 4) == wf.WF_EINVAL                 # pitch not a multiple of 8
+    assert call(row_end=M + 1) == wf.WF_ERANGE
+    assert call(row_begin=5, row_end=5) == wf.WF_ERANGE
+    assert call(k=96) == wf.WF_EINVAL
+    assert call(epi=99) == wf.WF_EINVAL
+    assert lib.wf_linear_e4m3(h, P(a), M, K, 0, M, P(w), None, P(b), N, K, wf.WF_EPI_F32, P(out), N,
+                              None, 0, 1, None) == wf.WF_EINVAL    # no weight scales
+    torch.cuda.synchronize()
+    assert torch.equal(out, x0)
     assert plan.sync_status() == wf.WF_OK
