@@ -63,7 +63,8 @@ def test_fp8_publish_placement():
 
 
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(3, 7, 1, mask=sch.MASK_RF),
-                                 sch.Cfg(2, 4, 1, sequential=True)], ids=str)
+                                 sch.Cfg(2, 4, 1, sequential=True), sch.Cfg(1, 4, 1), sch.Cfg(3, 1, -1),
+                                 sch.Cfg(3, 7, 0), sch.Cfg(2, 6, 0, use_anchor=False)], ids=str)
 def test_fp8_visibility_fingerprint(cfg):
     geom = SMALL
     r = make_round(cfg, geom, wf.WF_FP8, fp8_scales=(2.0, 1.0))

@@ -85,12 +85,28 @@ def test_fp32_tiny_wavefront():
     assert mx <= FP32_MAX, (mx, mean, rel)
 
 
+# The method's degenerate cases: one denoising stage (S = 1), a one-chunk
+# request, no history window (W = 0: anchor, store and live chunks only),
+# both at once, no anchor and no history, and the comparison graphs without
+# history.
+DEGENERATE = [sch.Cfg(1, 4, 1), sch.Cfg(3, 1, -1), sch.Cfg(3, 7, 0), sch.Cfg(1, 1, 0),
+              sch.Cfg(2, 6, 0, use_anchor=False), sch.Cfg(2, 5, 0, mask=sch.MASK_RF),
+              sch.Cfg(1, 3, 0, sequential=True)]
+
+
+@pytest.mark.parametrize("cfg", DEGENERATE, ids=str)
+def test_bf16_degenerate_requests(cfg):
+    mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, wf.WF_ATTN_TC, seed=17, qk_scale=2.0,
+                                 err=scaled_errors)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
+
+
+@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3)] + DEGENERATE, ids=str)
 @pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
-def test_visibility_fingerprint(kernel):
+def test_visibility_fingerprint(kernel, cfg):
     """Q = 0 makes softmax uniform over the visible keys; V one-hot in the
     producing (chunk, stage) gives O = share of each visible chunk, exactly
     1/len(context) per entry (ragged last tile included)."""
-    cfg = sch.Cfg(4, 10, 3)
     geom = SMALL
     r = make_round(cfg, geom, wf.WF_BF16)
     out = r.new_out()
