@@ -531,16 +531,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // compiled to exactly the register count the setmaxnreg split assumes.
 template <bool F8>
 cudaError_t prepare_kernel() {
-    static bool done = false;
-    if (done) return cudaSuccess;
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<F8>);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LayMisc<F8>::ALLOC);
-    if (e == cudaSuccess) done = true;
-    return e;
+    static std::atomic<unsigned long long> done{0};
+    return wf_once_per_device(done, [] {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<F8>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        return cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    LayMisc<F8>::ALLOC);
+    });
 }
 
 // Parameters and launch of one round's attention (ctl: the control words).
@@ -582,16 +581,18 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    static EncodeFn encode = nullptr;
-    if (!encode) {
+    // looked up once (thread-safe static initialisation); the driver entry
+    // point is the same for every device
+    static const EncodeFn encode = [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                              cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-            return cudaErrorUnknown;
-        encode = reinterpret_cast<EncodeFn>(fn);
-    }
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<EncodeFn>(fn);
+    }();
+    if (!encode) return cudaErrorUnknown;
     // bf16: 64-element (128-byte) boxes, two per 128-wide tile; e4m3: one
     // 128-element (128-byte) box
     const bool f8 = g.dtype == WF_FP8;

@@ -633,13 +633,12 @@ template <int BN, int EPI, bool F8>
 cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                    const GemmParams &p, int num_sms, cudaStream_t stream) {
     using C = Cfg<BN>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SM_ALLOC);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> attr_set{0};
+    cudaError_t e = wf_once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SM_ALLOC);
+    });
+    if (e != cudaSuccess) return e;
     const int n_tiles = p.tiles_m * p.tiles_n;
     const int grid = n_tiles < num_sms ? n_tiles : num_sms;
     gemm_tc_kernel<BN, EPI, F8><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, tc, p);
@@ -651,17 +650,18 @@ typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, voi
                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (thread-safe static
+// initialisation); the entry point is the same for every device.
 EncodeFn encoder() {
-    static EncodeFn fn = nullptr;
-    if (!fn) {
+    static const EncodeFn fn = [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                              &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<EncodeFn>(f);
-    }
+            f = nullptr;
+        return reinterpret_cast<EncodeFn>(f);
+    }();
     return fn;
 }
 

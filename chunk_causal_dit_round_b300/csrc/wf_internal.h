@@ -2,6 +2,7 @@
 // kernels.  Not part of the public C ABI (include/wf.h).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cstddef>
 
@@ -10,6 +11,21 @@
 #include <cuda_runtime.h>
 
 #include "../../include/wf.h"
+
+// Runs fn() -- a per-device CUDA setting such as a kernel's shared-memory
+// opt-in -- once per device for the calling process; done holds one bit per
+// device.  Repeating fn() is harmless, so concurrent first calls need no lock.
+template <typename F>
+inline cudaError_t wf_once_per_device(std::atomic<unsigned long long> &done, F &&fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = fn();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 #define WF_MAX_TASKS (WF_MAX_STAGES + 1)
 
