@@ -360,6 +360,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.out = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -367,11 +368,12 @@ class ClockSampler:
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self.out = open(self.path, "w")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                stdout=self.out, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except OSError:
             self.proc = None
@@ -384,6 +386,10 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+                self.proc.wait()
+        if self.out is not None:
+            self.out.close()
+            self.out = None
 
     def summary(self):
         sm, mx, reasons = [], [], set()
