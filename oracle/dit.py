@@ -318,13 +318,14 @@ class Model:
         new_cache = {}
         for layer in range(d.layers):
             proj = [self.qkv(x, t.stage, layer, t.chunk) for x, t in zip(xs, tasks)]
-            # key universe: cached entries (label S + 1), then every live task (label = stage)
+            # key universe: cached entries (label S + 1; S + 2 for history
+            # only the store keeps), then every live task (label = stage)
             ks, vs, lab = [], [], []
             for e in sorted(cached.values(), key=lambda e: (e.kind, e.chunk)):
                 kk, vv = self.cached_kv(e, layer)
                 ks.append(kk)
                 vs.append(vv)
-                lab.append(np.full(self.nc, cfg.S + 1))
+                lab.append(np.full(self.nc, e.j))
             for t, (_, kk, vv, _) in zip(tasks, proj):
                 ks.append(kk)
                 vs.append(vv)

@@ -40,18 +40,27 @@ Readings where the pages are silent (each also listed in the design notes):
   position is one before the oldest non-anchor chunk present in the round
   (history, store or live), clamped at 0; with full history it never moves.
   Mode ABSOLUTE keeps it at chunk position 0.
+* The store's longer prefix (App. B.3: under a token budget the store
+  reserves one query chunk where a denoising task reserves S, so their
+  prefixes can differ): by default both use the same W history chunks; the
+  option store_extra = E >= 0 (with bounded history) lets the store keep the
+  E next-older clean chunks too.  E = S gives the store the key count of a
+  stage-0 denoising task (anchor + W + store + S live = anchor + W + S +
+  itself).
 * Page ids are this implementation's own convention, written here in closed
   form so the library's ring allocator can be checked against it bit for bit:
   page 0 = anchor; ring pages 1..R hold clean chunks, chunk c on page
-  1 + ((c - c0) mod R) with c0 = 1 (anchor on) or 0; R = W + 1 (W history +
-  the live store), or every non-anchor chunk for full history; the live
-  denoising chunk of stage s is on page 1 + R + s; page 1 + R + S keeps the
-  anchor's unrotated key.
+  1 + ((c - c0) mod R) with c0 = 1 (anchor on) or 0; R = W + E + 1 (the
+  store's history + the live store), or every non-anchor chunk for full
+  history; the live denoising chunk of stage s is on page 1 + R + s; page
+  1 + R + S keeps the anchor's unrotated key.
 """
 
 from __future__ import annotations
 
 from dataclasses import dataclass
+
+import numpy as np
 
 ANCHOR_ADJACENT = 0
 ANCHOR_ABSOLUTE = 1
@@ -60,6 +69,7 @@ MASK_WF = 0
 MASK_RF = 1
 
 # cleanliness labels j of Eq. 4, extended to the cached entries of Eq. 5
+# (anchor and history S+1, live store S, the store's extra history S+2)
 KIND_ANCHOR = 0
 KIND_HISTORY = 1
 KIND_STORE = 2
@@ -75,6 +85,7 @@ class Cfg:
     anchor_mode: int = ANCHOR_ADJACENT
     mask: int = MASK_WF
     sequential: bool = False
+    store_extra: int = 0   # E: extra history chunks of the store (bounded history only)
 
 
 @dataclass(frozen=True)
@@ -127,18 +138,24 @@ def store_chunk(cfg: Cfg, k: int):
     return u if 0 <= u < cfg.n_chunks else None
 
 
-def sees(cfg: Cfg, s: int, j: int) -> bool:
+def sees(cfg: Cfg, s: int, j):
     """Mask of Sec. 3.1 Eq. 4 extended to the labels of cached entries
     (anchor/history S+1, live store S): WF 1[j >= s]; RF lets a denoising
-    query see every live label of the window as well."""
+    query see every live label of the window as well.  History kept for the
+    store only (store_extra > 0) carries label S+2, which only the store
+    (s = S) sees -- no label of Eq. 4's form j >= s can express that."""
     if cfg.mask == MASK_RF and s < cfg.S:
-        return j >= 0                      # every label (elementwise for arrays)
-    return j >= s
+        base = j >= 0                      # every label (elementwise for arrays)
+    else:
+        base = j >= s
+    if cfg.store_extra > 0 and s < cfg.S:
+        return np.logical_and(base, np.asarray(j) != cfg.S + 2)
+    return base
 
 
 def ring_size(cfg: Cfg) -> int:
     if cfg.history >= 0:
-        return cfg.history + 1
+        return cfg.history + cfg.store_extra + 1
     return max(1, cfg.n_chunks - (1 if cfg.use_anchor else 0))
 
 
@@ -173,11 +190,13 @@ def anchor_present(cfg: Cfg, k: int) -> bool:
     return cfg.use_anchor and 0 in clean_before(cfg, k)
 
 
-def history_chunks(cfg: Cfg, k: int) -> list[int]:
-    """Bounded clean history H_k: the W newest clean non-anchor chunks, oldest first."""
+def history_chunks(cfg: Cfg, k: int, store: bool = False) -> list[int]:
+    """Bounded clean history H_k: the W newest clean non-anchor chunks, oldest
+    first; the store's keeps the W + E newest."""
     clean = [c for c in clean_before(cfg, k) if not (cfg.use_anchor and c == 0)]
     if cfg.history >= 0:
-        clean = clean[max(0, len(clean) - cfg.history):] if cfg.history > 0 else []
+        keep = cfg.history + (cfg.store_extra if store else 0)
+        clean = clean[max(0, len(clean) - keep):] if keep > 0 else []
     return clean
 
 
@@ -185,7 +204,7 @@ def anchor_tpos(cfg: Cfg, k: int) -> int:
     """Temporal chunk position the anchor's key is rotated at in round k."""
     if cfg.anchor_mode == ANCHOR_ABSOLUTE:
         return 0
-    others = list(history_chunks(cfg, k))
+    others = list(history_chunks(cfg, k, store=True))
     u = store_chunk(cfg, k)
     if u is not None and not (cfg.use_anchor and u == 0):
         others.append(u)
@@ -201,11 +220,14 @@ def round_tasks(cfg: Cfg, k: int) -> list[Task]:
     S = cfg.S
     live = live_tasks(cfg, k)
     u = store_chunk(cfg, k)
-    prefix = []
+    anchor = []
     if anchor_present(cfg, k):
-        prefix.append(Entry(KIND_ANCHOR, 0, S + 1, 0, anchor_tpos(cfg, k)))
-    for h in history_chunks(cfg, k):
-        prefix.append(Entry(KIND_HISTORY, h, S + 1, clean_page(cfg, h), h))
+        anchor.append(Entry(KIND_ANCHOR, 0, S + 1, 0, anchor_tpos(cfg, k)))
+    prefix = anchor + [Entry(KIND_HISTORY, h, S + 1, clean_page(cfg, h), h)
+                       for h in history_chunks(cfg, k)]
+    window = set(history_chunks(cfg, k))
+    store_prefix = anchor + [Entry(KIND_HISTORY, h, S + 1 if h in window else S + 2, clean_page(cfg, h), h)
+                             for h in history_chunks(cfg, k, store=True)]
     store_entry = None
     if u is not None:
         store_entry = Entry(KIND_STORE, u, S, clean_page(cfg, u), u)
@@ -219,7 +241,7 @@ def round_tasks(cfg: Cfg, k: int) -> list[Task]:
                 ctx.append(Entry(KIND_LIVE, c2, j, live_page(cfg, j), c2))
         tasks.append(Task(c, s, live_page(cfg, s), tuple(ctx)))
     if u is not None:
-        ctx = list(prefix) + [store_entry]
+        ctx = list(store_prefix) + [store_entry]
         tasks.append(Task(u, S, clean_page(cfg, u), tuple(ctx)))
     return tasks
 

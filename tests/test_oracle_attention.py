@@ -62,7 +62,10 @@ def _raw_random(seed):
 
 
 CFGS = [sch.Cfg(2, 6, -1), sch.Cfg(4, 10, 3), sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE),
-        sch.Cfg(3, 5, 2, use_anchor=False)]
+        sch.Cfg(3, 5, 2, use_anchor=False),
+        # the store keeps E more history chunks than the denoising tasks
+        sch.Cfg(4, 11, 2, store_extra=4), sch.Cfg(3, 8, 1, store_extra=1),
+        sch.Cfg(2, 7, 0, store_extra=2, use_anchor=False), sch.Cfg(2, 5, 1, sequential=True, store_extra=2)]
 
 
 @pytest.mark.parametrize("cfg", CFGS, ids=str)

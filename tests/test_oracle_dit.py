@@ -189,12 +189,13 @@ def test_zero_gates_leave_the_residual_stream_alone():
 
 # ---- the round ---------------------------------------------------------------------
 
-@pytest.mark.parametrize("S,n,W", [(2, 5, -1), (2, 6, 1), (3, 7, 2)])
+@pytest.mark.parametrize("S,n,W,E", [(2, 5, -1, 0), (2, 6, 1, 0), (3, 7, 2, 0), (2, 7, 1, 2)])
 @pytest.mark.parametrize("bf16_points", [False, True])
-def test_layer_major_masked_round_equals_sequential_replay(S, n, W, bf16_points):
+def test_layer_major_masked_round_equals_sequential_replay(S, n, W, E, bf16_points):
     """App. B.6 Proposition 1: the batched, masked layer-major round equals
-    task-at-a-time execution over the ordered contexts, round after round."""
-    cfg = sch.Cfg(S=S, n_chunks=n, history=W)
+    task-at-a-time execution over the ordered contexts, round after round
+    (E: history kept by the store only, label S + 2 in the mask)."""
+    cfg = sch.Cfg(S=S, n_chunks=n, history=W, store_extra=E)
     a = model(cfg, bf16_points=bf16_points)
     b = model(cfg, bf16_points=bf16_points)
     for k in range(sch.n_rounds(cfg)):

@@ -235,3 +235,62 @@ def test_sequential_schedule_invariants(S, N, W):
     # N = S + 1 forwards per chunk (NF1C), chunks strictly in order
     assert seen == [(i, s) for i in range(N) for s in range(S + 1)]
     assert sch.slot_occupancy(cfg) == pytest.approx(1 / (S + 1))
+
+
+# ---- the store's longer prefix (App. B.3: the store reserves one query chunk,
+# a denoising task S, so under a token budget the store may keep more history)
+
+EXTRA = [sch.Cfg(4, 14, 3, store_extra=4), sch.Cfg(2, 9, 0, store_extra=2),
+         sch.Cfg(3, 10, 1, store_extra=1, use_anchor=False),
+         sch.Cfg(3, 10, 2, store_extra=3, mask=sch.MASK_RF),
+         sch.Cfg(2, 5, 1, store_extra=2, sequential=True),
+         sch.Cfg(3, 9, 2, store_extra=3, anchor_mode=sch.ANCHOR_ABSOLUTE)]
+
+
+@pytest.mark.parametrize("cfg", EXTRA, ids=str)
+def test_store_extra_history_contexts(cfg):
+    """Denoising tasks keep the W newest clean chunks, the store the W + E
+    newest (label S + 2 on the ones only it keeps); within a round no page
+    holds two chunks; the adjacent anchor sits before the oldest kept chunk."""
+    W, E, S = cfg.history, cfg.store_extra, cfg.S
+    for k in range(sch.n_rounds(cfg)):
+        clean = [c for c in sch.clean_before(cfg, k) if not (cfg.use_anchor and c == 0)]
+        page_of = {}
+        for t in sch.round_tasks(cfg, k):
+            hist = [e for e in t.context if e.kind == sch.KIND_HISTORY]
+            keep = W + E if t.stage == S else W
+            assert [e.chunk for e in hist] == clean[max(0, len(clean) - keep):] if keep else hist == []
+            for e in hist:
+                only_store = e.chunk not in clean[max(0, len(clean) - W):] if W else True
+                assert e.j == (S + 2 if only_store else S + 1)
+                assert t.stage == S or not only_store
+            for e in t.context:
+                if e.kind != sch.KIND_LIVE:
+                    assert page_of.setdefault(e.page, e.chunk) == e.chunk, (k, e)
+        if sch.anchor_present(cfg, k) and cfg.anchor_mode == sch.ANCHOR_ADJACENT:
+            store_hist = sch.history_chunks(cfg, k, store=True)
+            if store_hist:
+                assert sch.anchor_tpos(cfg, k) == store_hist[0] - 1
+
+
+def test_store_extra_equal_to_s_equalises_the_key_budget():
+    """With E = S the store reads as many key chunks as a stage-0 task once
+    the history is full (anchor + W + E + itself = anchor + W + store + S)."""
+    for S, W in ((2, 1), (4, 3), (3, 0)):
+        cfg = sch.Cfg(S, 20, W, store_extra=S)
+        seen = 0
+        for k in range(sch.n_rounds(cfg)):
+            tasks = sch.round_tasks(cfg, k)
+            clean = [c for c in sch.clean_before(cfg, k) if c != 0]
+            if len(tasks) == S + 1 and len(clean) >= W + S:
+                assert len(tasks[-1].context) == len(tasks[0].context) == 1 + W + S + 1
+                seen += 1
+        assert seen > 0
+
+
+def test_store_extra_zero_is_the_default_schedule():
+    for cfg in (sch.Cfg(4, 12, 3), sch.Cfg(2, 6, -1), sch.Cfg(3, 7, 1, mask=sch.MASK_RF)):
+        alt = sch.Cfg(cfg.S, cfg.n_chunks, cfg.history, cfg.use_anchor, cfg.anchor_mode, cfg.mask,
+                      cfg.sequential, store_extra=0)
+        for k in range(sch.n_rounds(cfg)):
+            assert sch.round_tasks(cfg, k) == sch.round_tasks(alt, k)
