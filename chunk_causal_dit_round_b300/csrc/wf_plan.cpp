@@ -82,8 +82,23 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
                              ? 0 : adjacent_anchor_pos(p, store_chunk, lchunk, na);
         prefix[np++] = {WF_KIND_ANCHOR, 0, S + 1, 0, p->anchor_tpos};
     }
-    for (auto &h : p->history) prefix[np++] = {WF_KIND_HISTORY, h.first, S + 1, h.second, h.first};
-    if (store_chunk >= 0) prefix[np++] = {WF_KIND_STORE, store_chunk, S, store_page, store_chunk};
+    // the denoising tasks see the W newest history chunks; the store also the
+    // E older ones it alone keeps (label S + 2)
+    const int n_hist = (int)p->history.size();
+    const int n_shared = p->W >= 0 ? std::min(n_hist, p->W) : n_hist;
+    CtxEntry store_prefix[WF_MAX_CTX];
+    int nsp = 0;
+    for (int e = 0; e < np; ++e) store_prefix[nsp++] = prefix[e];   // the anchor
+    int at = 0;
+    for (auto &h : p->history) {
+        const bool shared = at++ >= n_hist - n_shared;
+        if (shared) prefix[np++] = {WF_KIND_HISTORY, h.first, S + 1, h.second, h.first};
+        store_prefix[nsp++] = {WF_KIND_HISTORY, h.first, shared ? S + 1 : S + 2, h.second, h.first};
+    }
+    if (store_chunk >= 0) {
+        prefix[np++] = {WF_KIND_STORE, store_chunk, S, store_page, store_chunk};
+        store_prefix[nsp++] = prefix[np - 1];
+    }
 
     p->n_tasks = 0;
     for (int a = 0; a < na; ++a) {
@@ -108,7 +123,7 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
         t.stage = S;
         t.dest = store_page;
         t.n_ctx = 0;
-        for (int e = 0; e < np; ++e) t.ctx[t.n_ctx++] = prefix[e];
+        for (int e = 0; e < nsp; ++e) t.ctx[t.n_ctx++] = store_prefix[e];
     }
 
     // device view
@@ -275,6 +290,8 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
     if (!(o.rope_theta > 1.0) || !std::isfinite(o.rope_theta)) return WF_EINVAL;
     if (o.mask != WF_MASK_WF && o.mask != WF_MASK_RF) return WF_EINVAL;
     if (o.schedule != WF_SCHED_WAVEFRONT && o.schedule != WF_SCHED_SEQUENTIAL) return WF_EINVAL;
+    if (o.store_extra_history < 0) return WF_EINVAL;
+    if (o.store_extra_history > 0 && history_chunks < 0) return WF_EINVAL;
     if (o.grid_t < 1) return WF_EINVAL;
     if (o.grid_h == 0 && o.grid_w == 0) {
         if (chunk_tokens % o.grid_t) return WF_EINVAL;
@@ -285,11 +302,14 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
         (long long)o.grid_t * o.grid_h * o.grid_w != (long long)chunk_tokens)
         return WF_EINVAL;
 
-    int R = history_chunks >= 0 ? history_chunks + 1
+    const int E = o.store_extra_history;
+    // ring: the store's history (W + E) and the live store
+    int R = history_chunks >= 0 ? history_chunks + E + 1
                                 : std::max(1, o.n_chunks - (o.use_anchor ? 1 : 0));
-    // longest context: anchor + history + store + S live chunks
+    // longest context: anchor + history + store + S live chunks (a denoising
+    // task), or anchor + W + E history + itself (the store)
     int hist_max = history_chunks >= 0 ? history_chunks : std::max(0, o.n_chunks - 1);
-    if (1 + hist_max + 1 + S > WF_MAX_CTX) return WF_ERANGE;
+    if (1 + hist_max + 1 + S > WF_MAX_CTX || 1 + hist_max + E + 1 > WF_MAX_CTX) return WF_ERANGE;
     int P = 1 + R + S + 1;
     if (P > 255) return WF_ERANGE;
 
@@ -388,7 +408,7 @@ int wf_round_step(wf_plan_t p, wf_round_info *info) {
             p->anchor_stored = true;
         } else {
             p->history.emplace_back(p->prev_store_chunk, p->prev_store_page);
-            while (p->W >= 0 && (int)p->history.size() > p->W) {
+            while (p->W >= 0 && (int)p->history.size() > p->W + p->o.store_extra_history) {
                 p->free_pages.push_back(p->history.front().second);
                 p->history.pop_front();
             }
@@ -509,18 +529,19 @@ int wf_selftest_timeout(wf_plan_t p, unsigned int limit_us, cudaStream_t stream)
 
 // ---- checkpoint / resume of the host round state ----------------------------
 // Layout (int32 words): magic, version, S, N_C, H, D, W, n_chunks, layers,
-// use_anchor, anchor_mode, mask, schedule, k, have_prev_store,
+// use_anchor, anchor_mode, mask, schedule, store_extra_history, k, have_prev_store,
 // prev_store_chunk, prev_store_page, anchor_stored, n_history,
 // (chunk, page) x n_history, n_free, page x n_free, anchor_rot[layers],
 // published[layers].
 namespace {
 constexpr int32_t kStateMagic = 0x57465354;  // "WFST"
-constexpr int32_t kStateVersion = 1;
+constexpr int32_t kStateVersion = 2;
+constexpr int kStateHead = 20;   // words before the history list
 }  // namespace
 
 int wf_plan_state_size(wf_plan_t p, size_t *bytes) {
     if (!p || !bytes) return WF_EINVAL;
-    *bytes = sizeof(int32_t) * (19 + 2 * p->history.size() + 1 + p->free_pages.size() +
+    *bytes = sizeof(int32_t) * (kStateHead + 2 * p->history.size() + 1 + p->free_pages.size() +
                                 2 * (size_t)p->o.layers);
     return WF_OK;
 }
@@ -532,12 +553,13 @@ int wf_plan_export_state(wf_plan_t p, void *buf, size_t cap, size_t *written) {
     if (cap < need) return WF_ENOMEM;
     std::vector<int32_t> w;
     w.reserve(need / 4);
-    const int32_t head[] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
-                            p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
-                            p->o.mask, p->o.schedule, p->k, p->have_prev_store ? 1 : 0,
-                            p->prev_store_chunk, p->prev_store_page, p->anchor_stored ? 1 : 0,
-                            (int32_t)p->history.size()};
-    w.insert(w.end(), head, head + 19);
+    const int32_t head[kStateHead] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
+                                      p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
+                                      p->o.mask, p->o.schedule, p->o.store_extra_history, p->k,
+                                      p->have_prev_store ? 1 : 0, p->prev_store_chunk,
+                                      p->prev_store_page, p->anchor_stored ? 1 : 0,
+                                      (int32_t)p->history.size()};
+    w.insert(w.end(), head, head + kStateHead);
     for (auto &h : p->history) { w.push_back(h.first); w.push_back(h.second); }
     w.push_back((int32_t)p->free_pages.size());
     for (int f : p->free_pages) w.push_back(f);
@@ -549,20 +571,20 @@ int wf_plan_export_state(wf_plan_t p, void *buf, size_t cap, size_t *written) {
 }
 
 int wf_plan_import_state(wf_plan_t p, const void *buf, size_t n) {
-    if (!p || !buf || n % 4 || n < 19 * 4) return WF_EINVAL;
+    if (!p || !buf || n % 4 || n < kStateHead * 4) return WF_EINVAL;
     const int32_t *w = static_cast<const int32_t *>(buf);
     const size_t nw = n / 4;
     const int32_t want[] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
                             p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
-                            p->o.mask, p->o.schedule};
-    for (int i = 0; i < 13; ++i)
+                            p->o.mask, p->o.schedule, p->o.store_extra_history};
+    for (int i = 0; i < 14; ++i)
         if (w[i] != want[i]) return WF_EINVAL;
     const int S = p->S, N = p->o.n_chunks;
     const bool seq = p->o.schedule == WF_SCHED_SEQUENTIAL;
-    const int k = w[13];
+    const int k = w[14];
     if (k < -1 || k >= (seq ? N * (S + 1) : N + S)) return WF_EINVAL;
-    size_t at = 19;
-    const int nh = w[18];
+    size_t at = kStateHead;
+    const int nh = w[19];
     if (nh < 0 || nh > p->R || at + 2 * (size_t)nh + 1 > nw) return WF_EINVAL;
     std::deque<std::pair<int, int>> hist;
     for (int i = 0; i < nh; ++i, at += 2) {
@@ -579,15 +601,15 @@ int wf_plan_import_state(wf_plan_t p, const void *buf, size_t n) {
     std::vector<int> rot(p->o.layers), pub(p->o.layers);
     for (int l = 0; l < p->o.layers; ++l) rot[l] = w[at++];
     for (int l = 0; l < p->o.layers; ++l) pub[l] = w[at++];
-    const bool have_prev = w[14] != 0;
-    const int prev_chunk = w[15], prev_page = w[16];
+    const bool have_prev = w[15] != 0;
+    const int prev_chunk = w[16], prev_page = w[17];
     if (have_prev && (prev_chunk < 0 || prev_chunk >= N || prev_page < 0 || prev_page > p->R))
         return WF_EINVAL;
     p->k = k;
     p->have_prev_store = have_prev;
     p->prev_store_chunk = prev_chunk;
     p->prev_store_page = prev_page;
-    p->anchor_stored = w[17] != 0;
+    p->anchor_stored = w[18] != 0;
     p->history = hist;
     p->free_pages = freep;
     p->anchor_rot = rot;

@@ -111,6 +111,13 @@ typedef struct wf_plan_opts {
     int schedule;       /* WF_SCHED_WAVEFRONT (default) or WF_SCHED_SEQUENTIAL */
     double fp8_qk_scale;  /* WF_FP8: scale of Q and K before e4m3 rounding (default 1) */
     double fp8_v_scale;   /* WF_FP8: scale of V before e4m3 rounding (default 1) */
+    int store_extra_history; /* E >= 0 (default 0): the store pass keeps the E next-older
+                                clean chunks besides the W all tasks see ("Wave Forcing"
+                                App. B.3: the store reserves one query chunk where a
+                                denoising task reserves S, so under a token budget its
+                                prefix can be longer; E = S gives it the key count of a
+                                stage-0 task).  Needs history_chunks >= 0.  Page-table
+                                label of those entries: S + 2 (seen by the store only). */
 } wf_plan_opts;
 
 typedef struct wf_buffer_sizes {

@@ -14,7 +14,7 @@ def make_round(cfg: sch.Cfg, geom: Geom, dtype, layers=1, fp8_scales=(1.0, 1.0))
     return wf.Round(cfg.S, geom.chunk_tokens, geom.heads, geom.head_dim, cfg.history, fp8_scales=fp8_scales,
                     n_chunks=cfg.n_chunks, layers=layers, grid=geom.grid, dtype=dtype,
                     use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode,
-                    rope_theta=geom.theta, mask=cfg.mask,
+                    rope_theta=geom.theta, mask=cfg.mask, store_extra=cfg.store_extra,
                     schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
 
 

@@ -47,6 +47,9 @@ def test_validation_codes():
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, grid_h=5, grid_w=4)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, dtype=7)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, anchor_mode=3)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, 1, n_chunks=6, store_extra_history=-1)[0] == wf.WF_EINVAL
+    assert _plan(2, 48, 2, 32, -1, n_chunks=6, store_extra_history=1)[0] == wf.WF_EINVAL   # full history
+    assert _plan(2, 48, 2, 32, 3, n_chunks=6, store_extra_history=wf.WF_MAX_CTX)[0] == wf.WF_ERANGE
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, mask=2)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, schedule=2)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=40)[0] == wf.WF_ERANGE      # context > 32 chunks
@@ -103,14 +106,21 @@ CFGS += [sch.Cfg(S, N, W, a, mask=sch.MASK_RF) for S, N, W, a in itertools.produ
     [1, 2, 4], [3, 12], [-1, 1, 3], [True, False])]
 CFGS += [sch.Cfg(S, N, W, a, m, sequential=True) for S, N, W, a, m in itertools.product(
     [1, 2, 4], [1, 5], [-1, 0, 2], [True, False], [sch.ANCHOR_ADJACENT, sch.ANCHOR_ABSOLUTE])]
+# the store's longer prefix (E extra history chunks for the store pass)
+CFGS += [sch.Cfg(S, N, W, a, m, store_extra=E) for S, N, W, E, a, m in itertools.product(
+    [1, 2, 4], [3, 12], [0, 1, 3], [1, 4], [True, False], [sch.ANCHOR_ADJACENT, sch.ANCHOR_ABSOLUTE])]
+CFGS += [sch.Cfg(3, 12, 1, mask=sch.MASK_RF, store_extra=3), sch.Cfg(2, 5, 1, sequential=True, store_extra=2),
+         sch.Cfg(4, 133, 3, store_extra=4)]
 
 
 @pytest.mark.parametrize("cfg", CFGS, ids=str)
 def test_page_table_bit_exact_vs_oracle(cfg):
     rc, h = _plan(cfg.S, 12, 1, 8, cfg.history, n_chunks=cfg.n_chunks, grid_h=2, grid_w=2,
                   use_anchor=int(cfg.use_anchor), anchor_mode=cfg.anchor_mode, mask=cfg.mask,
-                  schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
-    if 1 + (cfg.history if cfg.history >= 0 else cfg.n_chunks - 1) + 1 + cfg.S > wf.WF_MAX_CTX:
+                  schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT,
+                  store_extra_history=cfg.store_extra)
+    hist = cfg.history if cfg.history >= 0 else cfg.n_chunks - 1
+    if 1 + hist + 1 + max(cfg.S, cfg.store_extra) > wf.WF_MAX_CTX:
         assert rc == wf.WF_ERANGE
         return
     assert rc == wf.WF_OK
@@ -180,7 +190,7 @@ def _round_plan(cfg, **kw):
     return _plan(cfg.S, 12, 1, 8, cfg.history, n_chunks=cfg.n_chunks, grid_h=2, grid_w=2,
                  use_anchor=int(cfg.use_anchor), anchor_mode=cfg.anchor_mode, mask=cfg.mask,
                  schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT,
-                 layers=3, **kw)
+                 store_extra_history=cfg.store_extra, layers=3, **kw)
 
 
 def _table(h):
@@ -204,7 +214,8 @@ def _export(h):
 
 
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 14, 3), sch.Cfg(2, 7, -1), sch.Cfg(3, 9, 1, mask=sch.MASK_RF),
-                                 sch.Cfg(2, 4, 1, sequential=True)], ids=str)
+                                 sch.Cfg(2, 4, 1, sequential=True), sch.Cfg(3, 12, 1, store_extra=3)],
+                         ids=str)
 def test_state_export_import_resumes_the_request(cfg):
     """A request checkpointed at every round and resumed in a fresh plan
     follows the uninterrupted plan's schedule bit for bit to the end."""
@@ -239,7 +250,7 @@ def test_state_import_rejects_foreign_or_corrupt_state():
     rc, b = _round_plan(cfg)
     assert wf.lib.wf_plan_import_state(b, bytes(state[:-4]), len(state) - 4) == wf.WF_EINVAL
     bad = bytearray(state)
-    bad[19 * 4:19 * 4 + 4] = (999).to_bytes(4, "little", signed=True)   # history chunk id
+    bad[20 * 4:20 * 4 + 4] = (999).to_bytes(4, "little", signed=True)   # history chunk id
     assert wf.lib.wf_plan_import_state(b, bytes(bad), len(bad)) == wf.WF_EINVAL
     bad = bytearray(state)
     bad[0] ^= 1                                                       # magic

@@ -38,6 +38,7 @@ def new_round(cfg, grid, heads, layers, fp8=None):
                     n_chunks=cfg.n_chunks, layers=layers, grid=grid,
                     dtype=wf.WF_FP8 if fp8 else wf.WF_BF16, fp8_scales=fp8 or (1.0, 1.0),
                     use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode, mask=cfg.mask,
+                    store_extra=cfg.store_extra,
                     schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
 
 
@@ -142,7 +143,8 @@ GRID = (3, 8, 10)       # 240 tokens per chunk: one full 128-row tile and a ragg
 @pytest.mark.parametrize("cfg", [sch.Cfg(2, 6, 1), sch.Cfg(3, 5, -1),
                                  sch.Cfg(2, 5, 2, anchor_mode=sch.ANCHOR_ABSOLUTE),
                                  sch.Cfg(2, 5, 1, mask=sch.MASK_RF),
-                                 sch.Cfg(2, 4, 1, sequential=True)], ids=str)
+                                 sch.Cfg(2, 4, 1, sequential=True),
+                                 sch.Cfg(2, 6, 1, store_extra=2)], ids=str)
 def test_dit_request_matches_oracle(cfg):
     steps = [1000.0, 750.0, 500.0, 250.0][:cfg.S] if cfg.S != 2 else [1000.0, 500.0]
     mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=SHARP_STD, seed=12, steps=steps)

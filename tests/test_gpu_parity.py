@@ -94,14 +94,19 @@ DEGENERATE = [sch.Cfg(1, 4, 1), sch.Cfg(3, 1, -1), sch.Cfg(3, 7, 0), sch.Cfg(1, 
               sch.Cfg(1, 3, 0, sequential=True)]
 
 
-@pytest.mark.parametrize("cfg", DEGENERATE, ids=str)
+# the store keeps E history chunks the denoising tasks do not see
+STORE_EXTRA = [sch.Cfg(4, 10, 2, store_extra=4), sch.Cfg(2, 7, 0, store_extra=2),
+               sch.Cfg(3, 8, 1, mask=sch.MASK_RF, store_extra=2)]
+
+
+@pytest.mark.parametrize("cfg", DEGENERATE + STORE_EXTRA, ids=str)
 def test_bf16_degenerate_requests(cfg):
     mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, wf.WF_ATTN_TC, seed=17, qk_scale=2.0,
                                  err=scaled_errors)
     assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
-@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3)] + DEGENERATE, ids=str)
+@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3)] + DEGENERATE + STORE_EXTRA, ids=str)
 @pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 def test_visibility_fingerprint(kernel, cfg):
     """Q = 0 makes softmax uniform over the visible keys; V one-hot in the
