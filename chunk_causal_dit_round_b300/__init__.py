@@ -65,7 +65,8 @@ class wf_plan_opts(ctypes.Structure):
                 ("use_anchor", ctypes.c_int), ("anchor_mode", ctypes.c_int),
                 ("rope_theta", ctypes.c_double), ("mask", ctypes.c_int),
                 ("schedule", ctypes.c_int), ("fp8_qk_scale", ctypes.c_double),
-                ("fp8_v_scale", ctypes.c_double), ("store_extra_history", ctypes.c_int)]
+                ("fp8_v_scale", ctypes.c_double), ("store_extra_history", ctypes.c_int),
+                ("rope_split", ctypes.c_int * 3)]
 
 
 class wf_buffer_sizes(ctypes.Structure):
@@ -178,8 +179,8 @@ class Round:
     def __init__(self, S, chunk_tokens, heads, head_dim, history, *, n_chunks, layers=1,
                  grid=(3, 0, 0), dtype=WF_BF16, use_anchor=True,
                  anchor_mode=WF_ANCHOR_ADJACENT, rope_theta=10000.0, mask=WF_MASK_WF,
-                 schedule=WF_SCHED_WAVEFRONT, fp8_scales=(1.0, 1.0), store_extra=0, device="cuda",
-                 bind=True):
+                 schedule=WF_SCHED_WAVEFRONT, fp8_scales=(1.0, 1.0), store_extra=0, rope_split=None,
+                 device="cuda", bind=True):
         o = default_opts()
         o.n_chunks, o.layers = n_chunks, layers
         o.grid_t, o.grid_h, o.grid_w = grid
@@ -187,6 +188,8 @@ class Round:
         o.mask, o.schedule = mask, schedule
         o.fp8_qk_scale, o.fp8_v_scale = fp8_scales
         o.store_extra_history = store_extra
+        if rope_split is not None:
+            o.rope_split[0], o.rope_split[1], o.rope_split[2] = rope_split
         self.S, self.NC, self.H, self.D = S, chunk_tokens, heads, head_dim
         self.dtype = dtype
         h = ctypes.c_void_p()

@@ -290,6 +290,12 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
     if (!(o.rope_theta > 1.0) || !std::isfinite(o.rope_theta)) return WF_EINVAL;
     if (o.mask != WF_MASK_WF && o.mask != WF_MASK_RF) return WF_EINVAL;
     if (o.schedule != WF_SCHED_WAVEFRONT && o.schedule != WF_SCHED_SEQUENTIAL) return WF_EINVAL;
+    const bool custom_split = o.rope_split[0] || o.rope_split[1] || o.rope_split[2];
+    if (custom_split) {
+        for (int a = 0; a < 3; ++a)
+            if (o.rope_split[a] < 0 || o.rope_split[a] % 2) return WF_EINVAL;
+        if (o.rope_split[0] + o.rope_split[1] + o.rope_split[2] != head_dim) return WF_EINVAL;
+    }
     if (o.store_extra_history < 0) return WF_EINVAL;
     if (o.store_extra_history > 0 && history_chunks < 0) return WF_EINVAL;
     if (o.grid_t < 1) return WF_EINVAL;
@@ -324,8 +330,12 @@ int wf_plan(int S, int chunk_tokens, int heads, int head_dim, int history_chunks
     g.dtype = o.dtype;
     g.qk_scale = (float)o.fp8_qk_scale;
     g.v_scale = (float)o.fp8_v_scale;
-    int q6 = head_dim / 6;
-    g.dt2 = (head_dim - 4 * q6) / 2; g.dh2 = q6; g.dw2 = q6;
+    if (custom_split) {
+        g.dt2 = o.rope_split[0] / 2; g.dh2 = o.rope_split[1] / 2; g.dw2 = o.rope_split[2] / 2;
+    } else {
+        const int q6 = head_dim / 6;
+        g.dt2 = (head_dim - 4 * q6) / 2; g.dh2 = q6; g.dw2 = q6;
+    }
     g.t_max = o.grid_t * o.n_chunks;
     g.rope_t_off = 0;
     g.rope_h_off = g.t_max * g.dt2;

@@ -118,6 +118,11 @@ typedef struct wf_plan_opts {
                                 prefix can be longer; E = S gives it the key count of a
                                 stage-0 task).  Needs history_chunks >= 0.  Page-table
                                 label of those entries: S + 2 (seen by the store only). */
+    int rope_split[3];  /* sizes (d_t, d_h, d_w) of the temporal / height / width parts of the
+                           head dimension rotated by 3D RoPE (Sec. 4.2 applies RoPE; the
+                           pages give no split): all 0 (default) = D - 4 floor(D/6),
+                           2 floor(D/6), 2 floor(D/6) (128 -> 44/42/42); otherwise even,
+                           >= 0 and summing to head_dim, else WF_EINVAL */
 } wf_plan_opts;
 
 typedef struct wf_buffer_sizes {

@@ -7,7 +7,8 @@ the base or the pair convention, so this oracle adopts the Wan2.1 video
 convention as its reading (stated again in the design notes):
 
 * head_dim D is split into a temporal, a height and a width part of sizes
-  D - 4*floor(D/6), 2*floor(D/6), 2*floor(D/6)  (128 -> 44/42/42);
+  D - 4*floor(D/6), 2*floor(D/6), 2*floor(D/6)  (128 -> 44/42/42), unless a
+  split (d_t, d_h, d_w) of even sizes summing to D is given (a plan option);
 * channels are rotated in interleaved pairs (2m, 2m+1);
 * pair m of a part of size d rotates by angle pos * theta^(-2m/d), theta = 1e4;
 * (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a);
@@ -25,15 +26,20 @@ from __future__ import annotations
 import numpy as np
 
 
-def sections(head_dim: int) -> tuple[int, int, int]:
+def sections(head_dim: int, split=None) -> tuple[int, int, int]:
     """Sizes of the (t, h, w) parts of the head dimension."""
+    if split is not None:
+        dt, dh, dw = (int(v) for v in split)
+        if min(dt, dh, dw) < 0 or dt % 2 or dh % 2 or dw % 2 or dt + dh + dw != head_dim:
+            raise ValueError(f"bad RoPE split {split} for head_dim {head_dim}")
+        return dt, dh, dw
     q = head_dim // 6
     return head_dim - 4 * q, 2 * q, 2 * q
 
 
-def pair_angles(head_dim: int, theta: float, t, h, w) -> np.ndarray:
+def pair_angles(head_dim: int, theta: float, t, h, w, split=None) -> np.ndarray:
     """Angles [n, head_dim/2] for positions given as arrays t, h, w of length n."""
-    dt, dh, dw = sections(head_dim)
+    dt, dh, dw = sections(head_dim, split)
     t = np.asarray(t, dtype=np.float64)[:, None]
     h = np.asarray(h, dtype=np.float64)[:, None]
     w = np.asarray(w, dtype=np.float64)[:, None]
@@ -70,7 +76,7 @@ def chunk_positions(chunk_tpos: int, grid_t: int, grid_h: int, grid_w: int):
     return grid_t * chunk_tpos + f, hh, ww
 
 
-def rope_chunk(x: np.ndarray, chunk_tpos: int, grid, theta: float) -> np.ndarray:
+def rope_chunk(x: np.ndarray, chunk_tpos: int, grid, theta: float, split=None) -> np.ndarray:
     """RoPE for a whole chunk x [N_C, H, D] placed at ``chunk_tpos``."""
     t, h, w = chunk_positions(chunk_tpos, *grid)
-    return rotate(x, pair_angles(x.shape[-1], theta, t, h, w))
+    return rotate(x, pair_angles(x.shape[-1], theta, t, h, w, split))

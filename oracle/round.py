@@ -91,6 +91,7 @@ class Geom:
     heads: int
     head_dim: int
     theta: float = 10000.0
+    rope_split: tuple | None = None   # (d_t, d_h, d_w); None = the default split
 
     @property
     def chunk_tokens(self) -> int:
@@ -109,13 +110,13 @@ def entry_kv(cfg: sch.Cfg, geom: Geom, e: sch.Entry, layer: int, raw, qk_dtype=N
     if isinstance(qk_dtype, Fp8) and e.kind == sch.KIND_ANCHOR and e.tpos != e.chunk:
         # re-rotated from the stored 8-bit unrotated copy (App. B.3)
         k_in = e4m3(k_in, qk_dtype.qk_scale)
-    k = rope_chunk(k_in, e.tpos, geom.grid, geom.theta)
+    k = rope_chunk(k_in, e.tpos, geom.grid, geom.theta, geom.rope_split)
     return round_to(k, qk_dtype), round_v(x[:, 2], qk_dtype)
 
 
 def task_queries(geom: Geom, t: sch.Task, layer: int, raw, qk_dtype=None) -> np.ndarray:
     x = np.asarray(raw(t.chunk, t.stage, layer), dtype=np.float64)
-    return round_to(rope_chunk(x[:, 0], t.chunk, geom.grid, geom.theta), qk_dtype)
+    return round_to(rope_chunk(x[:, 0], t.chunk, geom.grid, geom.theta, geom.rope_split), qk_dtype)
 
 
 def round_universe(cfg: sch.Cfg, geom: Geom, k: int, layer: int, raw, qk_dtype=None):

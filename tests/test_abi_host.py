@@ -50,6 +50,13 @@ def test_validation_codes():
     assert _plan(2, 48, 2, 32, 1, n_chunks=6, store_extra_history=-1)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, store_extra_history=1)[0] == wf.WF_EINVAL   # full history
     assert _plan(2, 48, 2, 32, 3, n_chunks=6, store_extra_history=wf.WF_MAX_CTX)[0] == wf.WF_ERANGE
+    # RoPE split: even parts >= 0 summing to head_dim, or all zero (default)
+    for bad in ((15, 9, 8), (16, 8, 6), (-2, 18, 16), (34, 0, 0)):
+        o = wf.default_opts()
+        o.n_chunks = 6
+        o.rope_split[0], o.rope_split[1], o.rope_split[2] = bad
+        h = ctypes.c_void_p()
+        assert wf.lib.wf_plan(2, 48, 2, 32, -1, ctypes.byref(o), ctypes.byref(h)) == wf.WF_EINVAL, bad
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, mask=2)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=6, schedule=2)[0] == wf.WF_EINVAL
     assert _plan(2, 48, 2, 32, -1, n_chunks=40)[0] == wf.WF_ERANGE      # context > 32 chunks
@@ -259,3 +266,25 @@ def test_state_import_rejects_foreign_or_corrupt_state():
     assert wf.lib.wf_selftest_timeout(b, 1000, None) == wf.WF_EUNBOUND
     for h in (a, other, b):
         wf.lib.wf_plan_destroy(h)
+
+
+def test_rope_split_sizes_the_tables():
+    """A custom split changes exactly the rotary tables in scratch: 8 bytes
+    per (position, pair) of each part (t over all chunks' frames, h, w)."""
+    def scratch(split):
+        o = wf.default_opts()
+        o.n_chunks, o.grid_t, o.grid_h, o.grid_w = 5, 3, 4, 4
+        if split:
+            o.rope_split[0], o.rope_split[1], o.rope_split[2] = split
+        h = ctypes.c_void_p()
+        assert wf.lib.wf_plan(2, 48, 1, 32, 1, ctypes.byref(o), ctypes.byref(h)) == wf.WF_OK
+        s = wf.wf_buffer_sizes()
+        assert wf.lib.wf_plan_buffer_sizes(h, ctypes.byref(s)) == wf.WF_OK
+        wf.lib.wf_plan_destroy(h)
+        return s.scratch
+    t_max, gh, gw = 3 * 5, 4, 4
+    pairs = lambda dt, dh, dw: t_max * dt // 2 + gh * dh // 2 + gw * dw // 2
+    base = scratch(None)
+    assert scratch((12, 10, 10)) == base                  # the default split for D = 32
+    for split in ((32, 0, 0), (16, 8, 8), (0, 16, 16)):
+        assert scratch(split) - base == 8 * (pairs(*split) - pairs(12, 10, 10)), split

@@ -94,3 +94,50 @@ def test_chunk_positions_layout():
     assert (t[1559], h[1559], w[1559]) == (6, 29, 51)
     assert (t[1560], h[1560], w[1560]) == (7, 0, 0)
     assert (t[53], h[53], w[53]) == (6, 1, 1)
+
+
+# ---- a custom (d_t, d_h, d_w) split (plan option) ----------------------------------
+
+def test_custom_split_equal_to_default_changes_nothing():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((60, 2, 128))
+    assert np.array_equal(rope.rope_chunk(x, 4, (3, 4, 5), 1e4),
+                          rope.rope_chunk(x, 4, (3, 4, 5), 1e4, split=(44, 42, 42)))
+
+
+def test_temporal_only_split_is_one_dimensional_rope():
+    """(D, 0, 0): every pair rotates by t * theta^(-2m/D), the textbook 1-D
+    rotary embedding of the frame index; tokens of one frame rotate alike."""
+    D, theta = 32, 1e4
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((24, 1, D))
+    y = rope.rope_chunk(x, 2, (3, 2, 4), theta, split=(D, 0, 0))
+    t = 3 * 2 + np.arange(24) // 8
+    for n in range(24):
+        for m in range(D // 2):
+            a = t[n] * theta ** (-2.0 * m / D)
+            c, s = np.cos(a), np.sin(a)
+            x0, x1 = x[n, 0, 2 * m], x[n, 0, 2 * m + 1]
+            assert np.isclose(y[n, 0, 2 * m], x0 * c - x1 * s, rtol=0, atol=1e-12)
+            assert np.isclose(y[n, 0, 2 * m + 1], x0 * s + x1 * c, rtol=0, atol=1e-12)
+
+
+def test_custom_split_parts_follow_their_axes():
+    """With split (d_t, d_h, d_w) the pairs of each part depend only on that
+    axis' coordinate: moving a token along w leaves the t and h parts alone."""
+    D, split = 64, (16, 32, 16)
+    ang_a = rope.pair_angles(D, 1e4, [5], [2], [1], split)
+    ang_b = rope.pair_angles(D, 1e4, [5], [2], [7], split)
+    nt, nh = split[0] // 2, split[1] // 2
+    assert np.array_equal(ang_a[:, :nt + nh], ang_b[:, :nt + nh])
+    assert not np.array_equal(ang_a[:, nt + nh:], ang_b[:, nt + nh:])
+    x = np.random.default_rng(5).standard_normal((1, 1, D))
+    for sp in (split, (64, 0, 0), (0, 0, 64)):
+        y = rope.rotate(x, rope.pair_angles(D, 1e4, [3], [1], [2], sp))
+        assert np.allclose(np.hypot(y[..., 0::2], y[..., 1::2]), np.hypot(x[..., 0::2], x[..., 1::2]))
+
+
+@pytest.mark.parametrize("bad", [(15, 9, 8), (16, 8, 6), (-2, 18, 16)])
+def test_bad_split_is_rejected(bad):
+    with pytest.raises(ValueError):
+        rope.sections(32, bad)
