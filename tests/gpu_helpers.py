@@ -15,6 +15,7 @@ def make_round(cfg: sch.Cfg, geom: Geom, dtype, layers=1, fp8_scales=(1.0, 1.0))
                     n_chunks=cfg.n_chunks, layers=layers, grid=geom.grid, dtype=dtype,
                     use_anchor=cfg.use_anchor, anchor_mode=cfg.anchor_mode,
                     rope_theta=geom.theta, mask=cfg.mask, store_extra=cfg.store_extra,
+                    rope_split=geom.rope_split,
                     schedule=wf.WF_SCHED_SEQUENTIAL if cfg.sequential else wf.WF_SCHED_WAVEFRONT)
 
 

@@ -106,6 +106,16 @@ def test_bf16_degenerate_requests(cfg):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
+def test_bf16_request_custom_rope_split():
+    """A non-default RoPE axis split (plan option) end to end: the kernels
+    read the split from the plan; sharp scores make a wrong rotation an O(1)
+    error."""
+    geom = Geom(grid_t=3, grid_h=10, grid_w=10, heads=2, head_dim=128, rope_split=(64, 32, 32))
+    mx, mean, rel = _run_request(sch.Cfg(3, 6, 1), geom, wf.WF_BF16, wf.WF_ATTN_TC, seed=19, qk_scale=2.0,
+                                 err=scaled_errors)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
+
+
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3)] + DEGENERATE + STORE_EXTRA, ids=str)
 @pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 def test_visibility_fingerprint(kernel, cfg):
