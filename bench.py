@@ -41,13 +41,34 @@ sys.path.insert(0, ROOT)
 METRIC = "chunk-causal attention TFLOP/s (% bf16 peak); DiT chunks/s per 1F1C round"
 UNIT = "TFLOP/s"
 
-# DRAM bytes (read + write) of one steady attn_tc_kernel launch (bf16 and
-# e4m3 pages), from the ncu captures summarised in
-# profiles/attn_tc_kernel_wan13_round.md and
-# profiles/attn_tc_kernel_fp8_wan13_round.md.  Set to None whenever the
-# kernel changes, until it is captured again.
-ATTN_TC_TRAFFIC_BYTES = 1.2571e9
-ATTN_TC_FP8_TRAFFIC_BYTES = 6.061e8
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one steady
+# attn_tc_kernel launch of the wan13_attn round (bf16 and e4m3 pages), from an
+# ncu capture, with the sha256 (first 16 hex digits) of the kernel's sources
+# at capture time.  The bench reports the figure only while the sources still
+# hash to that value, so a changed kernel reports null until it is captured
+# again.
+ATTN_TC_SOURCES = ("chunk_causal_dit_round_b300/csrc/attn_tc.cu",
+                   "chunk_causal_dit_round_b300/csrc/wf_ptx.cuh")
+ATTN_TC_TRAFFIC = {"bf16": (1.2571e9, "0" * 16), "e4m3": (6.061e8, "0" * 16)}
+
+
+def _sources_sha16(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def attn_traffic(kind):
+    """(bytes, note): the captured DRAM traffic of one launch, or None when
+    the kernel's sources changed since the capture."""
+    nbytes, sha = ATTN_TC_TRAFFIC[kind]
+    now = _sources_sha16(ATTN_TC_SOURCES)
+    if now != sha:
+        return None, f"kernel sources {now} differ from the captured {sha}: not re-captured yet"
+    return nbytes, f"ncu capture of one steady launch, kernel sources {sha}"
 
 CONFIGS = {
     # name: (S, grid (t,h,w), heads, head_dim, history W)
@@ -591,7 +612,8 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_src} {peak_kind}",
                      "avg_launch_ms": round(attn_avg, 4),
                      "flops_per_launch": per_launch,
-                     "traffic": ATTN_TC_FP8_TRAFFIC_BYTES if fp8 else ATTN_TC_TRAFFIC_BYTES},
+                     "traffic": attn_traffic("e4m3" if fp8 else "bf16")[0],
+                     "traffic_source": attn_traffic("e4m3" if fp8 else "bf16")[1]},
         "publish": {"bound": "hbm", "kernel": "publish_fp8_kernel" if fp8 else "publish_kernel<bf16>",
                     "achieved": round(pub_bytes / (pub_avg * 1e-3) / 1e9, 1), "peak": hbm,
                     "unit": "GB/s", "frac": round(pub_bytes / (pub_avg * 1e-3) / 1e9 / hbm, 4),

@@ -97,7 +97,8 @@ struct TcParams {
     float o_scale;        // 1 (bf16) or 1 / v_scale (e4m3 V)
     __nv_bfloat16 *out;   // [slot][N_C][H][D] bf16, or e4m3 bytes when out_e4m3
     int out_e4m3;         // O as e4m3 (unit scale): the input of an e4m3 output projection
-    uint32_t *ctl;        // scratch control words
+    uint32_t *ctl;        // scheduler counters (work, finished CTAs)
+    uint32_t *stat;       // status and wait-site words (the plan's scratch, read by wf_sync_status)
 };
 
 __device__ __forceinline__ int kseq(int j) { return j == 0 ? 0 : 2 * j - 1; }
@@ -423,8 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC);
     int *unit_slot = reinterpret_cast<int *>(smem + MISC + 8);
     c.abort = reinterpret_cast<volatile int *>(smem + MISC + 16);
-    c.status = p.ctl + WF_SCRATCH_STATUS / 4;
-    c.where = p.ctl + WF_SCRATCH_WHERE / 4;
+    c.status = p.stat + WF_SCRATCH_STATUS / 4;
+    c.where = p.stat + WF_SCRATCH_WHERE / 4;
     uint32_t *work = p.ctl + WF_SCRATCH_WORK / 4;
     uint32_t *done = p.ctl + WF_SCRATCH_DONE / 4;
 
@@ -542,9 +543,11 @@ cudaError_t prepare_kernel() {
     });
 }
 
-// Parameters and launch of one round's attention (ctl: the control words).
+// Parameters and launch of one round's attention (ctl: the scheduler
+// counters; stat: the status and wait-site words).
 cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const WfTmaps &maps,
-                      void *out, uint32_t *ctl, int num_sms, cudaStream_t stream, int out_e4m3 = 0) {
+                      void *out, uint32_t *ctl, uint32_t *stat, int num_sms, cudaStream_t stream,
+                      int out_e4m3 = 0) {
     const bool f8 = g.dtype == WF_FP8;
     cudaError_t e = f8 ? prepare_kernel<true>() : prepare_kernel<false>();
     if (e != cudaSuccess) return e;
@@ -562,6 +565,7 @@ cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const Wf
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.out_e4m3 = out_e4m3;
     p.ctl = ctl;
+    p.stat = stat;
     int grid = p.n_units < num_sms ? p.n_units : num_sms;
     if (f8)
         attn_tc_kernel<true><<<grid, NUM_THREADS, LayMisc<true>::ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
@@ -618,17 +622,19 @@ cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
                               cudaStream_t stream, int out_e4m3) {
     if (rd.n_tasks < 1) return cudaSuccess;
-    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(scratch), num_sms, stream,
-                     out_e4m3);
+    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(scratch),
+                     static_cast<uint32_t *>(scratch), num_sms, stream, out_e4m3);
 }
 
 // ---- launch without caller scratch ------------------------------------------
-// The attention kernel's control words (status, work counter, finished-CTA
-// counter, wait site) in a fixed device block owned by the library.  Static
-// device memory starts zeroed when the module loads; each call clears the
-// control words on its stream before launching, so a call never inherits a
-// previous call's counters.  All calls share this block: kernels that overlap
-// on the GPU race on it.
+// The attention kernel's scheduler counters (work counter, finished-CTA
+// counter) in a fixed device block owned by the library.  Static device
+// memory starts zeroed when the module loads; each call clears the counters
+// on its stream before launching, so a call never inherits a previous call's
+// counters.  All calls share this block: kernels that overlap on the GPU race
+// on it.  A bounded-wait timeout is recorded where wf_round_attention records
+// it -- the status word of the plan's scratch, which wf_sync_status reads --
+// so a failed call is never hidden by the next call's clearing.
 static __device__ __align__(256) uint32_t wf_noalloc_scratch[WF_NOALLOC_SCRATCH_BYTES / 4];
 
 namespace {
@@ -638,11 +644,11 @@ void *g_noalloc_addr[kMaxDevices] = {};  // device address of the block, per dev
 }  // namespace
 
 cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int layer,
-                                      const WfTmaps &maps, void *out, int num_sms,
-                                      cudaStream_t stream, int *wf_err) {
+                                      const WfTmaps &maps, void *out, void *status_scratch,
+                                      int num_sms, cudaStream_t stream, int *wf_err) {
     *wf_err = WF_OK;
-    // bytes of control words the kernel reads and writes (up to the wait-site word)
-    const size_t need = WF_SCRATCH_WHERE + sizeof(uint32_t);
+    // bytes of scheduler counters the kernel reads and writes (work, finished CTAs)
+    const size_t need = WF_SCRATCH_DONE + sizeof(uint32_t);
     if (need > WF_NOALLOC_SCRATCH_BYTES) {
         *wf_err = WF_ERANGE;
         return cudaSuccess;
@@ -658,6 +664,8 @@ cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int
     {
         // once per device, with that device current: the host-side name of a
         // __device__ array is not a device address, so look the address up.
+        // The address is kept for the life of the process; it is no longer
+        // valid once the device's context is destroyed (cudaDeviceReset).
         std::lock_guard<std::mutex> lock(g_noalloc_mu);
         if (!g_noalloc_addr[dev]) {
             void *a = nullptr;
@@ -670,5 +678,6 @@ cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int
     if (rd.n_tasks < 1) return cudaSuccess;
     e = cudaMemsetAsync(ctl, 0, need, stream);
     if (e != cudaSuccess) return e;
-    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(ctl), num_sms, stream);
+    return launch_tc(g, rd, layer, maps, out, static_cast<uint32_t *>(ctl),
+                     static_cast<uint32_t *>(status_scratch), num_sms, stream);
 }

@@ -84,11 +84,12 @@ cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
                               cudaStream_t stream, int out_e4m3 = 0);
 
-// Variant of wf_launch_attn_tc whose control words live in a static device
-// block inside the library (no caller scratch); see wf_round_attention_noalloc.
+// Variant of wf_launch_attn_tc whose scheduler counters live in a static
+// device block inside the library; status_scratch receives the status and
+// wait-site words (the plan's scratch); see wf_round_attention_noalloc.
 cudaError_t wf_launch_attn_tc_noalloc(const WfGeom &g, const WfRoundDev &rd, int layer,
-                                      const WfTmaps &maps, void *out, int num_sms,
-                                      cudaStream_t stream, int *wf_err);
+                                      const WfTmaps &maps, void *out, void *status_scratch,
+                                      int num_sms, cudaStream_t stream, int *wf_err);
 
 // ---- linear layers (gemm_tc.cu) -------------------------------------------
 // Internal epilogue of the QKV projection (RoPE + paged publication) and of

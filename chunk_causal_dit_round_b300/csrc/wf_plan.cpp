@@ -506,8 +506,8 @@ int wf_round_attention_noalloc(wf_plan_t p, int layer, void *out, cudaStream_t s
     if (p->published[layer] != p->k) return WF_EORDER;
     if (!(p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype))) return WF_EUNSUPPORTED;
     int wf_err = WF_OK;
-    cudaError_t e = wf_launch_attn_tc_noalloc(p->g, p->rd, layer, p->tmaps, out, p->num_sms,
-                                              stream, &wf_err);
+    cudaError_t e = wf_launch_attn_tc_noalloc(p->g, p->rd, layer, p->tmaps, out, p->scratch,
+                                              p->num_sms, stream, &wf_err);
     if (e != cudaSuccess) return WF_ECUDA;
     return wf_err;
 }
@@ -538,15 +538,32 @@ int wf_selftest_timeout(wf_plan_t p, unsigned int limit_us, cudaStream_t stream)
 }
 
 // ---- checkpoint / resume of the host round state ----------------------------
-// Layout (int32 words): magic, version, S, N_C, H, D, W, n_chunks, layers,
-// use_anchor, anchor_mode, mask, schedule, store_extra_history, k, have_prev_store,
-// prev_store_chunk, prev_store_page, anchor_stored, n_history,
-// (chunk, page) x n_history, n_free, page x n_free, anchor_rot[layers],
-// published[layers].
+// Layout (int32 words): the shape words (magic, version, S, N_C, H, D, W,
+// n_chunks, layers, use_anchor, anchor_mode, mask, schedule,
+// store_extra_history, dtype, the three rotary pair counts d_t/2, d_h/2,
+// d_w/2, rope_theta as two words of its IEEE bits, the float bits of the two
+// e4m3 scales), then k, have_prev_store, prev_store_chunk, prev_store_page,
+// anchor_stored, n_history, (chunk, page) x n_history, n_free,
+// page x n_free, anchor_rot[layers], published[layers].
 namespace {
 constexpr int32_t kStateMagic = 0x57465354;  // "WFST"
-constexpr int32_t kStateVersion = 2;
-constexpr int kStateHead = 20;   // words before the history list
+constexpr int32_t kStateVersion = 3;
+constexpr int kShapeWords = 22;  // words that must equal the importing plan's
+constexpr int kStateHead = kShapeWords + 6;   // words before the history list
+
+void shape_words(const wf_plan_s *p, int32_t *w) {
+    uint64_t theta;
+    std::memcpy(&theta, &p->o.rope_theta, 8);
+    uint32_t sqk, sv;
+    std::memcpy(&sqk, &p->g.qk_scale, 4);
+    std::memcpy(&sv, &p->g.v_scale, 4);
+    const int32_t v[kShapeWords] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
+                                    p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
+                                    p->o.mask, p->o.schedule, p->o.store_extra_history, p->o.dtype,
+                                    p->g.dt2, p->g.dh2, p->g.dw2, (int32_t)(uint32_t)theta,
+                                    (int32_t)(uint32_t)(theta >> 32), (int32_t)sqk, (int32_t)sv};
+    std::memcpy(w, v, sizeof(v));
+}
 }  // namespace
 
 int wf_plan_state_size(wf_plan_t p, size_t *bytes) {
@@ -561,15 +578,12 @@ int wf_plan_export_state(wf_plan_t p, void *buf, size_t cap, size_t *written) {
     size_t need;
     wf_plan_state_size(p, &need);
     if (cap < need) return WF_ENOMEM;
-    std::vector<int32_t> w;
-    w.reserve(need / 4);
-    const int32_t head[kStateHead] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
-                                      p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
-                                      p->o.mask, p->o.schedule, p->o.store_extra_history, p->k,
-                                      p->have_prev_store ? 1 : 0, p->prev_store_chunk,
-                                      p->prev_store_page, p->anchor_stored ? 1 : 0,
-                                      (int32_t)p->history.size()};
-    w.insert(w.end(), head, head + kStateHead);
+    std::vector<int32_t> w(kStateHead);
+    shape_words(p, w.data());
+    const int32_t round[6] = {p->k, p->have_prev_store ? 1 : 0, p->prev_store_chunk,
+                              p->prev_store_page, p->anchor_stored ? 1 : 0,
+                              (int32_t)p->history.size()};
+    std::memcpy(w.data() + kShapeWords, round, sizeof(round));
     for (auto &h : p->history) { w.push_back(h.first); w.push_back(h.second); }
     w.push_back((int32_t)p->free_pages.size());
     for (int f : p->free_pages) w.push_back(f);
@@ -584,42 +598,58 @@ int wf_plan_import_state(wf_plan_t p, const void *buf, size_t n) {
     if (!p || !buf || n % 4 || n < kStateHead * 4) return WF_EINVAL;
     const int32_t *w = static_cast<const int32_t *>(buf);
     const size_t nw = n / 4;
-    const int32_t want[] = {kStateMagic, kStateVersion, p->S, p->NC, p->H, p->D, p->W,
-                            p->o.n_chunks, p->o.layers, p->o.use_anchor, p->o.anchor_mode,
-                            p->o.mask, p->o.schedule, p->o.store_extra_history};
-    for (int i = 0; i < 14; ++i)
+    int32_t want[kShapeWords];
+    shape_words(p, want);
+    for (int i = 0; i < kShapeWords; ++i)
         if (w[i] != want[i]) return WF_EINVAL;
-    const int S = p->S, N = p->o.n_chunks;
+    const int32_t *rw = w + kShapeWords;
+    const int S = p->S, N = p->o.n_chunks, R = p->R;
     const bool seq = p->o.schedule == WF_SCHED_SEQUENTIAL;
-    const int k = w[14];
+    const int k = rw[0];
     if (k < -1 || k >= (seq ? N * (S + 1) : N + S)) return WF_EINVAL;
     size_t at = kStateHead;
-    const int nh = w[19];
-    if (nh < 0 || nh > p->R || at + 2 * (size_t)nh + 1 > nw) return WF_EINVAL;
+    const int nh = rw[5];
+    if (nh < 0 || nh > R || at + 2 * (size_t)nh + 1 > nw) return WF_EINVAL;
+    // every ring page 1..R is in exactly one place: history, the free list,
+    // or the previous round's store page awaiting promotion
+    std::vector<int> owner(R + 1, 0);
+    auto claim = [&](int page) {
+        if (page < 1 || page > R || owner[page]) return false;
+        owner[page] = 1;
+        return true;
+    };
     std::deque<std::pair<int, int>> hist;
     for (int i = 0; i < nh; ++i, at += 2) {
-        if (w[at] < 0 || w[at] >= N || w[at + 1] < 1 || w[at + 1] > p->R) return WF_EINVAL;
-        hist.emplace_back(w[at], w[at + 1]);
+        const int c = w[at], pg = w[at + 1];
+        if (c < 0 || c >= N || !claim(pg)) return WF_EINVAL;
+        if (!hist.empty() && c <= hist.back().first) return WF_EINVAL;   // oldest first
+        hist.emplace_back(c, pg);
     }
     const int nf = w[at++];
-    if (nf < 0 || nf > p->R || at + (size_t)nf + 2 * (size_t)p->o.layers != nw) return WF_EINVAL;
+    if (nf < 0 || nf > R || at + (size_t)nf + 2 * (size_t)p->o.layers != nw) return WF_EINVAL;
     std::deque<int> freep;
     for (int i = 0; i < nf; ++i, ++at) {
-        if (w[at] < 1 || w[at] > p->R) return WF_EINVAL;
+        if (!claim(w[at])) return WF_EINVAL;
         freep.push_back(w[at]);
     }
     std::vector<int> rot(p->o.layers), pub(p->o.layers);
     for (int l = 0; l < p->o.layers; ++l) rot[l] = w[at++];
     for (int l = 0; l < p->o.layers; ++l) pub[l] = w[at++];
-    const bool have_prev = w[15] != 0;
-    const int prev_chunk = w[16], prev_page = w[17];
-    if (have_prev && (prev_chunk < 0 || prev_chunk >= N || prev_page < 0 || prev_page > p->R))
-        return WF_EINVAL;
+    const bool have_prev = rw[1] != 0;
+    const int prev_chunk = rw[2], prev_page = rw[3];
+    if (have_prev) {
+        if (prev_chunk < 0 || prev_chunk >= N) return WF_EINVAL;
+        // the store of the anchor chunk writes page 0; every other store a ring page
+        const bool anchor_store = p->o.use_anchor && prev_chunk == 0;
+        if (anchor_store ? prev_page != 0 : !claim(prev_page)) return WF_EINVAL;
+    }
+    for (int pg = 1; pg <= R; ++pg)
+        if (!owner[pg]) return WF_EINVAL;
     p->k = k;
     p->have_prev_store = have_prev;
     p->prev_store_chunk = prev_chunk;
     p->prev_store_page = prev_page;
-    p->anchor_stored = w[18] != 0;
+    p->anchor_stored = rw[4] != 0;
     p->history = hist;
     p->free_pages = freep;
     p->anchor_rot = rot;

@@ -216,29 +216,31 @@ int wf_round_attention(wf_plan_t plan, int layer, void *out, int kernel, cudaStr
  * counterpart: this is a library convenience.
  *
  * Same computation, kernel and output as wf_round_attention(plan, layer, out,
- * WF_ATTN_TC, stream) -- the tensor-core kernel, so bf16 with head_dim 128
- * only (else WF_EUNSUPPORTED) -- but the kernel's scheduler counters and
- * status word live in a fixed block of WF_NOALLOC_SCRATCH_BYTES inside
- * libwf.so instead of the plan's scratch buffer.  It is meant for callers
- * that cannot allocate device memory at the point where they launch
- * attention: code running under a memory manager that owns every device
- * byte (a caching allocator or an arena sized at start-up), or a
- * steady-state loop that must not call cudaMalloc because it can
- * synchronise the whole device.  This call itself calls no cudaMalloc,
- * cudaFree or other allocating routine.
+ * WF_ATTN_TC, stream) -- the tensor-core kernel, so bf16 or WF_FP8 plans with
+ * head_dim 128 only (else WF_EUNSUPPORTED) -- but the kernel's scheduler
+ * counters live in a fixed block of WF_NOALLOC_SCRATCH_BYTES inside libwf.so
+ * instead of the plan's scratch buffer.  It is meant for callers that cannot
+ * allocate device memory at the point where they launch attention: code
+ * running under a memory manager that owns every device byte (a caching
+ * allocator or an arena sized at start-up), or a steady-state loop that must
+ * not call cudaMalloc because it can synchronise the whole device.  This
+ * call itself calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * - The first call on a device (the current device) looks up the block's
  *   device address once (cudaGetSymbolAddress); make that first call before
- *   any stream capture.  Every GPU that loads the library holds the block
- *   until the process exits.
+ *   any stream capture.  The address is kept for the life of the process:
+ *   after the device's context is destroyed (cudaDeviceReset) it is stale,
+ *   so do not call this entry point again in that process.  Every GPU that
+ *   loads the library holds the block until the process exits.
  * - Each call clears the block's counters on `stream` (cudaMemsetAsync of
- *   the control words) before the launch.  All calls share the one block,
+ *   the counter words) before the launch.  All calls share the one block,
  *   so calls whose kernels overlap on the GPU (different streams, or
  *   different plans on the same device) race; serialise them.
- * - The control words the kernel needs must fit in the block; a larger need
- *   is rejected with WF_ERANGE before anything is launched.
- * - A bounded-wait timeout inside the kernel is recorded in the block, not
- *   in the plan's scratch, so wf_sync_status does not see it.
+ * - The counters the kernel needs must fit in the block; a larger need is
+ *   rejected with WF_ERANGE before anything is launched.
+ * - A bounded-wait timeout inside the kernel is recorded in the status word
+ *   of the plan's scratch, as wf_round_attention records it, so
+ *   wf_sync_status reports it (the next call does not clear it).
  * Errors: as wf_round_attention, plus WF_ERANGE (control block too small)
  * and WF_ECUDA (symbol lookup, memset or launch failed). */
 #define WF_NOALLOC_SCRATCH_BYTES 256
@@ -403,9 +405,12 @@ int wf_selftest_timeout(wf_plan_t plan, unsigned int limit_us, cudaStream_t stre
  * page pool (caller-owned device memory, which the caller keeps) this lets a
  * request continue in a new plan of the same shape.  Import checks the shape
  * words (S, N_C, heads, head_dim, W, n_chunks, layers, anchor, mask,
- * schedule) and every page and chunk id, then rebuilds the current round's
- * contexts.  No CUDA call.  Errors: WF_EINVAL (null, foreign or corrupt
- * state), WF_ENOMEM (cap smaller than wf_plan_state_size). */
+ * schedule, store history, and what fixes the pages' bytes: dtype, RoPE base
+ * and split, e4m3 scales), every page and chunk id, and that each ring page
+ * sits in exactly one of history (oldest first), the free list and the
+ * pending store page; then it rebuilds the current round's contexts.  No
+ * CUDA call.  Errors: WF_EINVAL (null, foreign or corrupt state), WF_ENOMEM
+ * (cap smaller than wf_plan_state_size). */
 int wf_plan_state_size(wf_plan_t plan, size_t *bytes);
 int wf_plan_export_state(wf_plan_t plan, void *buf, size_t cap, size_t *written);
 int wf_plan_import_state(wf_plan_t plan, const void *buf, size_t n);

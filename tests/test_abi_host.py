@@ -246,6 +246,21 @@ def test_state_export_import_resumes_the_request(cfg):
         wf.lib.wf_plan_destroy(b)
 
 
+# word offsets of the checkpoint format: 22 shape words, then k,
+# have_prev_store, prev_store_chunk, prev_store_page, anchor_stored, n_history
+_SHAPE_WORDS = 22
+_HEAD = _SHAPE_WORDS + 6
+
+
+def _words(state):
+    return list(memoryview(bytes(state)).cast("i"))
+
+
+def _state(words):
+    import array
+    return array.array("i", words).tobytes()
+
+
 def test_state_import_rejects_foreign_or_corrupt_state():
     cfg = sch.Cfg(4, 14, 3)
     rc, a = _round_plan(cfg)
@@ -256,15 +271,86 @@ def test_state_import_rejects_foreign_or_corrupt_state():
     assert wf.lib.wf_plan_import_state(other, bytes(state), len(state)) == wf.WF_EINVAL
     rc, b = _round_plan(cfg)
     assert wf.lib.wf_plan_import_state(b, bytes(state[:-4]), len(state) - 4) == wf.WF_EINVAL
-    bad = bytearray(state)
-    bad[20 * 4:20 * 4 + 4] = (999).to_bytes(4, "little", signed=True)   # history chunk id
-    assert wf.lib.wf_plan_import_state(b, bytes(bad), len(bad)) == wf.WF_EINVAL
+    w = _words(state)
+    bad = list(w)
+    bad[_HEAD] = 999                                                   # history chunk id
+    assert wf.lib.wf_plan_import_state(b, _state(bad), len(state)) == wf.WF_EINVAL
     bad = bytearray(state)
     bad[0] ^= 1                                                       # magic
     assert wf.lib.wf_plan_import_state(b, bytes(bad), len(bad)) == wf.WF_EINVAL
     assert wf.lib.wf_plan_import_state(b, None, 0) == wf.WF_EINVAL
+    assert wf.lib.wf_plan_import_state(b, bytes(state), len(state)) == wf.WF_OK
     assert wf.lib.wf_selftest_timeout(b, 1000, None) == wf.WF_EUNBOUND
     for h in (a, other, b):
+        wf.lib.wf_plan_destroy(h)
+
+
+def test_state_import_rejects_aliased_or_missing_pages():
+    """Every ring page is in exactly one of history, the free list and the
+    pending store page: a state that puts two chunks on one page (they would
+    read each other's K/V) or loses a page is refused."""
+    cfg = sch.Cfg(4, 14, 3)
+    rc, a = _round_plan(cfg)
+    for _ in range(9):        # k = 8: three history chunks, a pending store page
+        wf.lib.wf_round_step(a, None)
+    w = _words(_export(a))
+    nh = w[_HEAD - 1]
+    assert nh == 3 and w[_SHAPE_WORDS + 1] == 1
+    hist_pages = [w[_HEAD + 2 * i + 1] for i in range(nh)]
+    at_free = _HEAD + 2 * nh
+    rc, b = _round_plan(cfg)
+    # two history chunks on one page
+    bad = list(w)
+    bad[_HEAD + 3] = hist_pages[0]
+    assert wf.lib.wf_plan_import_state(b, _state(bad), 4 * len(bad)) == wf.WF_EINVAL
+    # the pending store page also in history
+    bad = list(w)
+    bad[_HEAD + 1] = w[_SHAPE_WORDS + 3]
+    assert wf.lib.wf_plan_import_state(b, _state(bad), 4 * len(bad)) == wf.WF_EINVAL
+    # a free page that is also in history (the ring has R = 4 pages, none free here)
+    assert w[at_free] == 0
+    bad = w[:at_free] + [1, hist_pages[1]] + w[at_free + 1:]
+    assert wf.lib.wf_plan_import_state(b, _state(bad), 4 * len(bad)) == wf.WF_EINVAL
+    # a page that belongs nowhere (the history list loses its oldest chunk)
+    bad = list(w)
+    bad[_HEAD - 1] = nh - 1
+    del bad[_HEAD:_HEAD + 2]
+    assert wf.lib.wf_plan_import_state(b, _state(bad), 4 * len(bad)) == wf.WF_EINVAL
+    # history not oldest first
+    bad = list(w)
+    bad[_HEAD], bad[_HEAD + 2] = bad[_HEAD + 2], bad[_HEAD]
+    assert wf.lib.wf_plan_import_state(b, _state(bad), 4 * len(bad)) == wf.WF_EINVAL
+    assert wf.lib.wf_plan_import_state(b, _state(w), 4 * len(w)) == wf.WF_OK
+    for h in (a, b):
+        wf.lib.wf_plan_destroy(h)
+
+
+@pytest.mark.parametrize("change", [dict(dtype=wf.WF_FP8), dict(rope_theta=500.0),
+                                    dict(rope_split=(16, 8, 8)), dict(dtype=wf.WF_FP8, fp8_qk_scale=4.0)],
+                         ids=["dtype", "theta", "split", "fp8_scale"])
+def test_state_import_rejects_other_page_format(change):
+    """A checkpoint resumes only into a plan whose pages hold the same bytes:
+    same dtype, RoPE base and split, and the same e4m3 scales."""
+    def plan(**kw):
+        o = wf.default_opts()
+        o.n_chunks, o.layers, o.grid_t, o.grid_h, o.grid_w = 9, 2, 3, 4, 4
+        for k, v in kw.items():
+            if k == "rope_split":
+                o.rope_split[0], o.rope_split[1], o.rope_split[2] = v
+            else:
+                setattr(o, k, v)
+        h = ctypes.c_void_p()
+        assert wf.lib.wf_plan(2, 48, 1, 32, 2, ctypes.byref(o), ctypes.byref(h)) == wf.WF_OK
+        return h
+    base = dict(dtype=wf.WF_FP8) if "fp8_qk_scale" in change else {}
+    a = plan(**base)
+    for _ in range(5):
+        assert wf.lib.wf_round_step(a, None) == wf.WF_OK
+    st = _export(a)
+    same, other = plan(**base), plan(**change)
+    assert wf.lib.wf_plan_import_state(same, st, len(st)) == wf.WF_OK
+    assert wf.lib.wf_plan_import_state(other, st, len(st)) == wf.WF_EINVAL
+    for h in (a, same, other):
         wf.lib.wf_plan_destroy(h)
 
 
