@@ -29,7 +29,10 @@ in the design notes:
 * block l: (shift_a, scale_a, gate_a, shift_f, scale_f, gate_f) = the six
   rows of m_l + e0 (m_l a learned [6, dim] table);
   x' = LN(x) (1 + scale_a) + shift_a           (LayerNorm eps 1e-6, no affine)
-  q, k, v = split(x' W_qkv^T + b_qkv), RoPE on q and k, no Q/K normalisation
+  q, k, v = split(x' W_qkv^T + b_qkv)
+  q = RMSNorm(q) g_q, k = RMSNorm(k) g_k   (over the full width dim, all heads
+                                           together, eps 1e-6; learned gains)
+  RoPE on q and k
   x = x + gate_a * (Attn(q, k, v) W_o^T + b_o)
   x = x + gate_f * (GELU_tanh((LN(x)(1 + scale_f) + shift_f) W_1^T + b_1) W_2^T + b_2)
 * head: (shift, scale) = head table [2, dim] + e; y = (LN(x)(1 + scale) +
@@ -39,7 +42,11 @@ in the design notes:
   sigma = nu / 1000, sigma' = 5 sigma / (1 + 4 sigma); the model sees
   t = 1000 sigma'; Psi_{nu}(x, eps) = (1 - sigma') x + sigma' eps (flow
   matching; Psi_0 = identity as Eq. 1 requires);
-* the store pass uses context_noise = 0 (App. B.3 leaves the value open).
+* the store pass uses context_noise = 0 (App. B.3 leaves the value open);
+* the q/k normalisation is the standard Wan2.1 block's (App. D.2 keeps that
+  architecture): RMSNorm(y) = y / sqrt(mean(y^2) + eps) over the full model
+  width, times a learned per-channel gain, applied to the projected q and k
+  before RoPE.
 
 ``kv_fp8=(qk_scale, v_scale)`` stores the RoPE'd Q and K and V (and the
 anchor's unrotated key) as e4m3 after scaling instead of bf16 (8-bit
@@ -53,8 +60,9 @@ with unit scale.
 
 ``bf16=True`` rounds to bfloat16 where a BF16 execution (App. B.1) stores a
 tensor: the latent patches, every linear layer's input (normalised
-activations, attention output, FFN hidden), the RoPE-applied Q/K and V that
-enter attention (App. B.2 pages), and the weights (given already rounded).
+activations, attention output, FFN hidden), the projected q and k that the
+RMSNorm reads, the RoPE-applied Q/K and V that enter attention (App. B.2
+pages), and the weights (given already rounded).
 The residual stream, statistics and accumulations stay fp64.
 
 Two formulations of a round (they must agree, App. B.6 Proposition 1):
@@ -104,6 +112,12 @@ def layer_norm(x, eps=1e-6):
     mu = x.mean(axis=-1, keepdims=True)
     var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
     return (x - mu) / np.sqrt(var + eps)
+
+
+def rms_norm(x, gain, eps=1e-6):
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gain."""
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * np.asarray(gain, np.float64)
 
 
 def gelu_tanh(x):
@@ -199,6 +213,8 @@ class Weights:
     f2_w: list = field(default_factory=list)
     f2_b: list = field(default_factory=list)
     mod: list = field(default_factory=list)   # [6, dim] per layer
+    nq: list = field(default_factory=list)    # [dim] RMSNorm gain of q per layer
+    nk: list = field(default_factory=list)    # [dim] RMSNorm gain of k per layer
 
 
 def time_embedding(w: Weights, t):
@@ -244,12 +260,16 @@ class Model:
         return self.rb(patchify(z)) @ self.w.patch_w.T + self.w.patch_b
 
     def qkv(self, x, slot, layer, chunk):
-        """Projected, RoPE'd Q, K and V [N_C, H, D] plus the unrotated K."""
+        """Projected, normalised, RoPE'd Q, K and V [N_C, H, D] plus the
+        unrotated (normalised) K."""
         d, w = self.d, self.w
         m = w.mod[layer] + self.emb[slot][1]
         xa = self.ra(layer_norm(x) * (1.0 + m[1]) + m[0])
         y = xa @ self.lw["qkv"][layer].T + w.qkv_b[layer]
-        q, k, v = (y[:, i * d.dim:(i + 1) * d.dim].reshape(-1, d.heads, d.head_dim) for i in range(3))
+        q, k, v = (y[:, i * d.dim:(i + 1) * d.dim] for i in range(3))
+        q = rms_norm(self.rb(q), w.nq[layer])
+        k = rms_norm(self.rb(k), w.nk[layer])
+        q, k, v = (a.reshape(-1, d.heads, d.head_dim) for a in (q, k, v))
         ang = self.angles(chunk)
         if self.kv_fp8 is not None:
             from .round import e4m3
@@ -397,6 +417,6 @@ def weights_from(params: dict) -> Weights:
     w = Weights(**{k: f(params[k]) for k in ("patch_w", "patch_b", "t1_w", "t1_b", "t2_w",
                                              "t2_b", "tp_w", "tp_b", "head_w", "head_b",
                                              "head_mod")})
-    for k in ("qkv_w", "qkv_b", "o_w", "o_b", "f1_w", "f1_b", "f2_w", "f2_b", "mod"):
+    for k in ("qkv_w", "qkv_b", "o_w", "o_b", "f1_w", "f1_b", "f2_w", "f2_b", "mod", "nq", "nk"):
         setattr(w, k, [f(t) for t in params[k]])
     return w

@@ -42,6 +42,47 @@ def test_layer_norm_matches_torch_and_is_standardised():
     assert np.allclose((y ** 2).mean(-1), 1, atol=1e-5)
 
 
+def test_rms_norm_matches_torch_and_closed_forms():
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(6, 48)) * 3 + 0.5
+    g = 1 + 0.3 * rng.normal(size=48)
+    y = dit.rms_norm(x, g)
+    ref = F.rms_norm(torch.from_numpy(x), (48,), weight=torch.from_numpy(g), eps=1e-6).numpy()
+    assert np.allclose(y, ref, atol=1e-12)
+    # unit gain: mean square m / (m + eps) per row
+    y1 = dit.rms_norm(x, np.ones(48))
+    m = (x * x).mean(-1)
+    assert np.allclose((y1 * y1).mean(-1), m / (m + 1e-6), atol=1e-13)
+    # a constant row c maps to c / sqrt(c^2 + eps) times the gain
+    for c in (-2.5, 1e-3, 7.0):
+        row = dit.rms_norm(np.full(48, c), g)
+        assert np.allclose(row, c / math.sqrt(c * c + 1e-6) * g, atol=1e-14)
+    assert np.array_equal(dit.rms_norm(np.zeros(48), g), np.zeros(48))
+
+
+def test_qk_norm_spans_the_full_width():
+    """The q/k RMSNorm of the block normalises all heads of a token together:
+    heads whose projections differ in size by 8x still differ by 8x after
+    the norm and RoPE (a per-head norm would equalise them)."""
+    cfg = sch.Cfg(S=1, n_chunks=1, history=-1)
+    params = wf_synth.dit_params(5, SMALL.dim, SMALL.ffn, SMALL.layers, SMALL.channels,
+                                 SMALL.freq, std=0.2)
+    hd = SMALL.head_dim
+    for name in ("nq", "nk"):
+        params[name][0] = torch.ones(SMALL.dim, dtype=torch.bfloat16)
+    w = params["qkv_w"][0].clone()
+    w[hd:2 * hd] = w[:hd] * 8                               # q head 1 = 8 x q head 0 (exact in bf16)
+    w[SMALL.dim + hd:SMALL.dim + 2 * hd] = w[SMALL.dim:SMALL.dim + hd] * 8
+    params["qkv_w"][0] = w
+    params["qkv_b"][0] = torch.zeros(3 * SMALL.dim, dtype=torch.bfloat16)
+    m = model(cfg, params=params, steps=[1000.0])
+    q, k, _, kraw = m.qkv(m.embed(lat(9, 0, -1)), 0, 0, 0)
+    for t in (q, k, kraw):
+        r = np.linalg.norm(t[:, 1], axis=-1) / np.linalg.norm(t[:, 0], axis=-1)
+        assert np.allclose(r, 8.0, rtol=1e-9)
+        assert np.allclose((t ** 2).mean(axis=(1, 2)), 1.0, atol=1e-5)   # unit RMS over the width
+
+
 def test_gelu_tanh_odd_identity_and_torch():
     x = np.linspace(-6, 6, 241)
     g = dit.gelu_tanh(x)
@@ -140,6 +181,8 @@ def torch_dense_forward(params, dims, grid, z, t_model, theta=10000.0):
         xa = F.layer_norm(x, (dims.dim,), eps=1e-6) * (1 + m[1]) + m[0]
         qkv = F.linear(xa, P["qkv_w"][l], P["qkv_b"][l])
         q, k, v = qkv.split(dims.dim, dim=1)
+        q = F.rms_norm(q, (dims.dim,), weight=P["nq"][l], eps=1e-6)
+        k = F.rms_norm(k, (dims.dim,), weight=P["nk"][l], eps=1e-6)
         q = torch.from_numpy(rope_chunk(q.reshape(n, dims.heads, -1).numpy(), 0, grid, theta))
         k = torch.from_numpy(rope_chunk(k.reshape(n, dims.heads, -1).numpy(), 0, grid, theta))
         v = v.reshape(n, dims.heads, -1)

@@ -62,7 +62,8 @@ def qkv_raw(seed: int, chunk: int, stage: int, layer: int, n_tokens: int,
 
 
 def dit_params(seed: int, dim: int, ffn: int, layers: int, channels: int = 16,
-               freq: int = 256, std: float = 0.02, dtype=torch.bfloat16) -> dict:
+               freq: int = 256, std: float = 0.02, dtype=torch.bfloat16,
+               norm_gain: float = 1.0) -> dict:
     """Random-initialised DiT parameters ~ N(0, std^2), rounded to ``dtype``.
 
     Matrices are [out, in] (the layout of a linear layer's weight).  Keys:
@@ -70,7 +71,9 @@ def dit_params(seed: int, dim: int, ffn: int, layers: int, channels: int = 16,
     t2_b, tp_w [6 dim, dim], tp_b, head_w [4C, dim], head_b, head_mod
     [2, dim]; per layer (lists of length ``layers``): qkv_w [3 dim, dim],
     qkv_b, o_w [dim, dim], o_b, f1_w [ffn, dim], f1_b, f2_w [dim, ffn], f2_b,
-    mod [6, dim]."""
+    mod [6, dim], and the q / k RMSNorm gains nq, nk [dim] drawn as
+    ``norm_gain`` + N(0, std^2) (a normalisation gain starts at 1; the draw
+    makes every channel's gain distinct)."""
     p = 4 * channels
 
     def g(tag, *shape):
@@ -89,6 +92,9 @@ def dit_params(seed: int, dim: int, ffn: int, layers: int, channels: int = 16,
            "mod": (6, dim)}
     for i, (name, shape) in enumerate(per.items()):
         out[name] = [g((10, l, i), *shape) for l in range(layers)]
+    for i, name in ((9, "nq"), (10, "nk")):
+        out[name] = [(norm_gain + normal(key_of(seed, 7, 10, l, i), (dim,), std)).to(dtype)
+                     for l in range(layers)]
     return out
 
 
