@@ -121,16 +121,18 @@ QKV_ATTN_CONFIGS = {
 }
 
 
-def run_qkv_attn(args, name, rank, world):
+def run_qkv_attn(args, name, rank, world, steps=None, warmup=None):
     """Steady rounds of the per-layer P and attention of a 14B-scale model:
-    for each layer, wf_qkv_proj_rope_publish (QKV GEMM 5120 -> 15360 with
-    RoPE + paged publish) and wf_round_attention; the normalised layer input
-    is a synthetic N(0, 1) bf16 activation (the rest of the block is out of
-    this workload)."""
+    for each layer, wf_qkv_proj_rope_publish (QKV GEMM 5120 -> 15360, the
+    q/k RMSNorm, RoPE + paged publish) and wf_round_attention; the normalised
+    layer input is a synthetic N(0, 1) bf16 activation (the rest of the block
+    is out of this workload)."""
     import torch
     import chunk_causal_dit_round_b300 as wf
 
     cfg = QKV_ATTN_CONFIGS[name]
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     S, W = cfg["S"], cfg["history"]
     L = getattr(args, "layers", None) or cfg["layers"]
     NC = math.prod(cfg["grid"])
@@ -138,7 +140,7 @@ def run_qkv_attn(args, name, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     k_steady = S + W + 2
-    n_chunks = max(cfg["n_chunks"], k_steady + args.warmup + args.steps + 1)
+    n_chunks = max(cfg["n_chunks"], k_steady + warmup + steps + 1)
     r = wf.Round(S, NC, H, D, W, n_chunks=n_chunks, layers=L, grid=cfg["grid"], dtype=wf.WF_BF16)
     g = torch.Generator(device=dev)
     g.manual_seed(777 + rank)
@@ -146,6 +148,11 @@ def run_qkv_attn(args, name, rank, world):
           for _ in range(L)]
     bs = [(torch.randn((3 * dim,), generator=g, device=dev) * 0.02).to(torch.bfloat16)
           for _ in range(L)]
+    # q / k RMSNorm gains of the standard Wan2.1 block: 1 + N(0, 0.02^2)
+    nqs = [(1 + torch.randn((dim,), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+           for _ in range(L)]
+    nks = [(1 + torch.randn((dim,), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+           for _ in range(L)]
     xs = [torch.randn((S + 1, NC, dim), generator=g, device=dev).to(torch.bfloat16) for _ in range(2)]
     out = torch.empty((S + 1, NC, dim), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
@@ -153,26 +160,33 @@ def run_qkv_attn(args, name, rank, world):
     def one_round(i):
         info = r.step()
         for l in range(L):
-            r.publish_proj(l, xs[i % 2], ws[l], bs[l], stream)
+            r.publish_proj(l, xs[i % 2], ws[l], bs[l], nqs[l], nks[l], stream)
             r.attention(l, out, wf.WF_ATTN_TC, stream)
         return info
 
-    for i in range(k_steady + args.warmup):
+    for i in range(k_steady + warmup):
         one_round(i)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     flops = 0.0
+    launches = 0
+    prev_anchor = r.info.anchor_tpos
     with ClockSampler(dev.index) as clk:
         torch.cuda.synchronize()
-        for j in range(args.steps):
+        for j in range(steps):
             evs[j][0].record(stream)
             info = one_round(j)
             evs[j][1].record(stream)
             T = info.n_tasks * NC
             flops += L * (info.attn_flops + 2.0 * T * dim * 3 * dim)
+            # per layer: QKV GEMM, q/k RMSNorm + RoPE + publish, attention, and
+            # the anchor re-rotation in rounds where the window moved
+            moved = info.anchor_tpos >= 0 and info.anchor_tpos != prev_anchor
+            launches += (4 if moved else 3) * L
+            prev_anchor = info.anchor_tpos
         torch.cuda.synchronize()
     st = r.sync_status()
     if st != wf.WF_OK:
@@ -182,16 +196,98 @@ def run_qkv_attn(args, name, rank, world):
     peak, src = _sustained_peak()
     tf = flops / (ms * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L,
-           "value": round(world * args.steps / (ms * 1e-3), 3), "unit": "chunks/s",
-           "round_ms_p50": round(statistics.median(per), 3), "rounds": args.steps,
-           "flops_per_round": flops / args.steps,
+           "value": round(world * steps / (ms * 1e-3), 3), "unit": "chunks/s",
+           "value_p50": round(world * 1e3 / statistics.median(per), 3),
+           "round_ms_p50": round(statistics.median(per), 3), "rounds": steps,
+           "flops_per_round": flops / steps,
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
                         "peak_source": f"{src} bf16 dense (sustained)"},
-           "gpu_launches_per_round": 3 * L, "clocks": clk.summary()}
+           "gpu_launches": launches, "clocks": clk.summary()}
     del r, ws, xs
     torch.cuda.empty_cache()
     return res
+
+
+STREAM_SHAPES = {
+    # chunk geometries of the batched-requests measurement: the Wan2.1-1.3B
+    # chunk (3 latent frames) and a one-latent-frame chunk
+    "chunk4680": dict(grid=(3, 30, 52), desc="3 latent frames x 30 x 52 patches"),
+    "chunk1560": dict(grid=(1, 30, 52), desc="1 latent frame x 30 x 52 patches"),
+}
+
+
+def run_streams(args, rank, world, counts=(1, 2, 4, 8), steps=10, warmup=3):
+    """Several requests batched into one round (wf_group_*): for R requests
+    of the Wan2.1-1.3B attention layer (S = 4, 12 x 128 heads, W = 3 +
+    anchor), each steady round runs one batched publication (RoPE + paged
+    placement of all R (S+1) tasks) and one batched attention launch; every
+    request completes one chunk per round, so chunks/s = R / round time.
+    Measured at two chunk sizes; the gain over R = 1 is the occupancy the
+    batching recovers."""
+    import torch
+    import chunk_causal_dit_round_b300 as wf
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    base = CONFIGS["wan13_attn"]
+    S, W, H, D = base["S"], base["history"], base["heads"], base["head_dim"]
+    k_steady = S + W + 2
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, shp in STREAM_SHAPES.items():
+        NC = math.prod(shp["grid"])
+        rows = []
+        for R in counts:
+            grp = wf.Group(R, S, NC, H, D, W, n_chunks=k_steady + warmup + steps + 2, grid=shp["grid"],
+                           dtype=wf.WF_BF16, device=dev)
+            g = torch.Generator(device=dev)
+            g.manual_seed(99 + R)
+            qkvs = []
+            for _ in range(2):
+                x = torch.randn((R, S + 1, NC, 3, H, D), generator=g, device=dev)
+                qkvs.append((x / math.sqrt(D)).to(torch.bfloat16))
+                del x
+            o = grp.new_out()
+            mask = (1 << R) - 1
+
+            def one(i):
+                fl = 0.0
+                for r in grp.rounds:
+                    fl += r.step().attn_flops
+                grp.publish(mask, 0, qkvs[i % 2], stream)
+                grp.attention(mask, 0, o, wf.WF_ATTN_TC, stream)
+                return fl
+
+            for i in range(k_steady + warmup):
+                one(i)
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps)]
+            flops = 0.0
+            for j in range(steps):
+                evs[j][0].record(stream)
+                flops += one(j)
+                evs[j][1].record(stream)
+            torch.cuda.synchronize()
+            st = grp.rounds[0].sync_status()
+            if st != wf.WF_OK:
+                raise RuntimeError(f"device status {st}")
+            per = [a.elapsed_time(b) for a, b in evs]
+            ms, = max_over_ranks([sum(per)], world, dev)
+            rows.append({"requests": R, "chunks_per_s": round(world * R * steps / (ms * 1e-3), 2),
+                         "round_ms": round(ms / steps, 4),
+                         "attn_tflops": round(flops / (ms * 1e-3) / 1e12, 1)})
+            grp.close()
+            del grp, qkvs, o
+            torch.cuda.empty_cache()
+        base1 = rows[0]["chunks_per_s"]
+        for r_ in rows:
+            r_["vs_one_request"] = round(r_["chunks_per_s"] / base1, 3)
+        out[name] = {"chunk_tokens": NC, "desc": shp["desc"], "rows": rows}
+    return {"workload": "batched requests, Wan2.1-1.3B attention layer (publish + attention per round)",
+            "unit": "chunks/s", "steady_rounds_timed": steps, "shapes": out,
+            "gpu_launches_per_round": 2}
 
 
 def max_over_ranks(values, world, device="cpu"):
@@ -254,6 +350,8 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
                     ("o_b", (dim,)), ("f1_w", (ffn, dim)), ("f1_b", (ffn,)), ("f2_w", (dim, ffn)),
                     ("f2_b", (dim,)), ("mod", (6, dim))):
         P[k_] = [rnd(*shp) for _ in range(L)]
+    for k_ in ("nq", "nk"):          # q / k RMSNorm gains: 1 + N(0, 0.02^2)
+        P[k_] = [(1 + rnd(dim).float()).to(torch.bfloat16) for _ in range(L)]
     model = wf.Dit(r, P, ffn=ffn, channels=C, freq=256, timesteps=cfg["steps"],
                    linear_fp8=cfg.get("linear_fp8", False))
     latent = C * cfg["grid"][0] * 4 * cfg["grid"][1] * cfg["grid"][2]
@@ -294,10 +392,11 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
                 info = r.step()
                 model.round(zs[i % n_in], epss[i % n_in], None, chunk, stream)
                 flops += round_flops(info)
-                # patchify, patch GEMM, head LN, head GEMM; 7 per layer; plus a
-                # re-rotation launch per layer when the anchor moved
+                # patchify, patch GEMM, head LN, head GEMM; 8 per layer (LN,
+                # QKV GEMM, q/k RMSNorm, attention, output GEMM, LN, FFN1,
+                # FFN2); plus a re-rotation launch per layer when the anchor moved
                 moved = info.anchor_tpos >= 0 and info.anchor_tpos != prev_anchor
-                launches += 4 + 7 * L + (L if moved else 0)
+                launches += 4 + 8 * L + (L if moved else 0)
                 prev_anchor = info.anchor_tpos
                 i += 1
             evs[j][1].record(stream)
@@ -346,7 +445,9 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
         peak = flops / t_min
     tf = flops / steps / (statistics.median(per) * 1e-3) / 1e12
     res = {"workload": name, "desc": cfg["desc"], "layers": L, "value": round(chunks_s, 3),
-           "unit": "chunks/s", "forwards_per_chunk_timed": per_step,
+           "unit": "chunks/s", "value_stat": "timed chunks / whole timed region",
+           "value_p50": round(world * 1e3 / statistics.median(per), 3),
+           "forwards_per_chunk_timed": per_step,
            "e2e": {"value": round(world * e2e_steps / (e2e_ms * 1e-3), 3), "unit": "chunks/s",
                    "h2d_bytes_per_step": per_step * (h_z.numel() + h_eps.numel()) * 4,
                    "d2h_bytes_per_step": h_out.numel() * 4, "steps": e2e_steps,
@@ -668,6 +769,115 @@ class OracleSample:
         return fl, dt
 
 
+def tiny_all_rounds():
+    """The fp64 oracle on the tiny fp32 wavefront (S = 2, 6 chunks of 3 x 4 x 4
+    tokens, 2 heads x 32, full history): every one of its 8 rounds.
+    -> (algorithmic FLOPs, seconds)."""
+    import torch
+    import wf_synth
+    from oracle import schedule as sch
+    from oracle.round import Geom, round_attention
+
+    cfg, geom = sch.Cfg(2, 6, -1), Geom(3, 4, 4, 2, 32)
+    NC = geom.chunk_tokens
+    cache = {}
+
+    def raw(c, s_, l):
+        if (c, s_, l) not in cache:
+            cache[(c, s_, l)] = wf_synth.qkv_raw(1, c, s_, l, NC, geom.heads, geom.head_dim,
+                                                 dtype=torch.float32).double().numpy()
+        return cache[(c, s_, l)]
+
+    for k in range(sch.n_rounds(cfg)):          # inputs drawn before the clock runs
+        for t in sch.round_tasks(cfg, k):
+            raw(t.chunk, t.stage, 0)
+    fl = 0.0
+    t0 = time.perf_counter()
+    for k in range(sch.n_rounds(cfg)):
+        round_attention(cfg, geom, k, 0, raw)
+        fl += sum(4 * NC * len(t.context) * NC * geom.head_dim * geom.heads
+                  for t in sch.round_tasks(cfg, k))
+    return fl, time.perf_counter() - t0
+
+
+class DitBlockSample:
+    """The fp64 DiT oracle on one block of one steady round of the
+    random-init Wan2.1-1.3B 4-step DiT (4680-token chunks, dim 1536, 12 heads,
+    FFN 8960, W = 3; round k = 9 of a 64-chunk request): the QKV projection,
+    q/k RMSNorm and RoPE of every chunk the round's attention reads (the 5
+    live tasks, the anchor and the 3 history chunks, each over all its 4680
+    tokens), then, for ``rows`` sampled query rows of each task, the masked
+    attention over the round's key universe and the rest of the block
+    (output projection with gated residual, LN, FFN).  Inputs (weights ~ N(0,
+    0.02), N(0, 1) residual-stream rows) are drawn in the constructor."""
+
+    def __init__(self, rows=64, seed=9):
+        import numpy as np
+        import wf_synth
+        from oracle import dit
+        from oracle import schedule as sch
+
+        self.S, self.W = 4, 3
+        self.cfg = sch.Cfg(self.S, 64, self.W)
+        self.grid = (3, 30, 52)
+        self.dims = dit.Dims(dim=1536, heads=12, head_dim=128, ffn=8960, layers=1)
+        params = wf_synth.dit_params(seed, 1536, 8960, 1, 16, 256, std=0.02)
+        self.model = dit.Model(self.cfg, self.grid, self.dims, dit.weights_from(params),
+                               [1000.0, 750.0, 500.0, 250.0])
+        self.k = self.S + self.W + 2
+        self.tasks = sch.round_tasks(self.cfg, self.k)
+        self.cached = sorted({(e.kind, e.chunk) for t in self.tasks for e in t.context
+                              if e.kind in (sch.KIND_ANCHOR, sch.KIND_HISTORY)})
+        NC = 4680
+        rng = np.random.default_rng(seed)
+        self.x = {(t.chunk, t.stage): rng.standard_normal((NC, 1536)) for t in self.tasks}
+        self.xc = {c: rng.standard_normal((NC, 1536)) for _, c in self.cached}
+        self.rows = np.linspace(0, NC - 1, rows).astype(int)
+
+    def run(self):
+        """-> (algorithmic FLOPs, seconds)."""
+        import numpy as np
+        from oracle import schedule as sch
+        from oracle.attention import masked_attention
+
+        m, S, NC, d = self.model, self.S, 4680, self.dims
+        t0 = time.perf_counter()
+        m.cache = {}
+        for _, c in self.cached:                      # store-pass K/V of the cached chunks
+            _, kk, vv, kraw = m.qkv(self.xc[c], S, 0, c)
+            m.cache[c] = [(kk, vv, kraw)]
+        proj = [m.qkv(self.x[(t.chunk, t.stage)], t.stage, 0, t.chunk) for t in self.tasks]
+        entries = {}
+        for t in self.tasks:
+            for e in t.context:
+                if e.kind in (sch.KIND_ANCHOR, sch.KIND_HISTORY):
+                    entries[(e.kind, e.chunk)] = e
+        ks, vs, lab = [], [], []
+        for e in sorted(entries.values(), key=lambda e: (e.kind, e.chunk)):
+            kk, vv = m.cached_kv(e, 0)
+            ks.append(kk)
+            vs.append(vv)
+            lab.append(np.full(NC, e.j))
+        for t, (_, kk, vv, _) in zip(self.tasks, proj):
+            ks.append(kk)
+            vs.append(vv)
+            lab.append(np.full(NC, t.stage))
+        K = np.concatenate(ks).transpose(1, 0, 2)
+        V = np.concatenate(vs).transpose(1, 0, 2)
+        lab = np.concatenate(lab)
+        r = self.rows
+        for t, (q, _, _, _) in zip(self.tasks, proj):
+            mask = np.broadcast_to(sch.sees(self.cfg, t.stage, lab)[None, :], (len(r), lab.shape[0]))
+            o = masked_attention(q[r].transpose(1, 0, 2), K, V, mask).transpose(1, 0, 2)
+            m.finish_layer(self.x[(t.chunk, t.stage)][r], o, t.stage, 0)
+        dt = time.perf_counter() - t0
+        n_proj = len(self.cached) + len(self.tasks)
+        fl = n_proj * 2.0 * NC * d.dim * 3 * d.dim
+        fl += sum(4.0 * len(r) * len(t.context) * NC * d.head_dim * d.heads for t in self.tasks)
+        fl += len(self.tasks) * 2.0 * len(r) * (d.dim * d.dim + 2 * d.dim * d.ffn)
+        return fl, dt
+
+
 def _threads():
     try:
         from threadpoolctl import threadpool_info
@@ -677,12 +887,28 @@ def _threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(rows=3072):
+def cpu_baseline(rows=3072, dit_rows=64):
+    """The oracle on the host cores, on the samples the measurement plan
+    names: the Wan-1.3B attention round (the headline unit), the tiny fp32
+    wavefront over all its rounds, and one block of one round of the 1.3B DiT."""
     fl, dt = OracleSample().run(rows)
+    fl1, dt1 = tiny_all_rounds()
+    blk = DitBlockSample(rows=dit_rows)
+    fl3, dt3 = blk.run()
     return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": _threads(),
             "kind": "oracle",
             "sample": f"fp64 oracle on the steady Wan-1.3B round (k=9): {rows} of 4680 query rows "
-                      f"of each of the 5 tasks, 1 of 12 heads, mask materialised; {dt:.1f} s"}
+                      f"of each of the 5 tasks, 1 of 12 heads, mask materialised; {dt:.1f} s",
+            "tiny_all_rounds": {"seconds": round(dt1, 4), "tflops": round(fl1 / dt1 / 1e12, 6),
+                                "flops": fl1,
+                                "sample": "fp64 oracle on the tiny fp32 wavefront (S=2, 6 chunks of 48 "
+                                          "tokens, 2 x 32 heads, full history): all 8 rounds"},
+            "dit13_one_block_one_round": {
+                "seconds": round(dt3, 3), "tflops": round(fl3 / dt3 / 1e12, 6), "flops": fl3,
+                "sample": f"fp64 DiT oracle, one block of one steady round (k=9) of the 1.3B 4-step "
+                          f"DiT: QKV + q/k RMSNorm + RoPE of all 9 chunks the round reads (4680 "
+                          f"tokens each), masked attention and the rest of the block for {dit_rows} "
+                          f"sampled query rows of each of the 5 tasks"}}
 
 
 def run_reference(args, rows=64):
@@ -716,11 +942,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="wan13_attn",
-                    choices=sorted(CONFIGS) + sorted(DIT_CONFIGS) + sorted(QKV_ATTN_CONFIGS))
+                    choices=sorted(CONFIGS) + sorted(DIT_CONFIGS) + sorted(QKV_ATTN_CONFIGS)
+                    + ["streams"])
     ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--dit-steps", type=int, default=20,
+                    help="steady chunks timed per DiT leg of the default line (14B leg: half)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -735,6 +964,13 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    if args.config == "streams":
+        d = run_streams(args, rank, world, steps=args.steps, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps(d), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.config in DIT_CONFIGS or args.config in QKV_ATTN_CONFIGS:
         fn = run_dit if args.config in DIT_CONFIGS else run_qkv_attn
         d = fn(args, args.config, rank, world)
@@ -745,8 +981,15 @@ def main():
         return
     res = run_ours(args, rank, world)
     if not args.no_dit:
-        res["dit"] = run_dit(args, "dit13", rank, world, steps=5, warmup=3)
-        res["dit_w8a8"] = run_dit(args, "dit13_w8a8", rank, world, steps=5, warmup=3)
+        # the other workloads of the measurement plan, each with its clocks and
+        # roofline: the 1.3B DiT (bf16 and 8-bit), the 5-step long rollout and
+        # the 14B-scale QKV + attention stack
+        res["dit"] = run_dit(args, "dit13", rank, world, steps=args.dit_steps, warmup=3)
+        res["dit_w8a8"] = run_dit(args, "dit13_w8a8", rank, world, steps=args.dit_steps, warmup=3)
+        res["dit_s5"] = run_dit(args, "dit13_s5", rank, world, steps=args.dit_steps, warmup=3)
+        res["qkv_attn14b"] = run_qkv_attn(args, "qkv_attn14b", rank, world,
+                                          steps=max(5, args.dit_steps // 2), warmup=3)
+        res["streams"] = run_streams(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()

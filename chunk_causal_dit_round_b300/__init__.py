@@ -39,6 +39,7 @@ WF_MASK_WF = 0
 WF_MASK_RF = 1
 WF_SCHED_WAVEFRONT = 0
 WF_SCHED_SEQUENTIAL = 1
+WF_MAX_GROUP_PLANS = 8
 WF_ATTN_AUTO = 0
 WF_ATTN_TC = 1
 WF_ATTN_SIMT = 2
@@ -53,10 +54,12 @@ WF_NOALLOC_SCRATCH_BYTES = 256
 # every symbol include/wf.h declares
 SYMBOLS = ["wf_plan_opts_default", "wf_plan", "wf_plan_buffer_sizes", "wf_bind",
            "wf_round_step", "wf_page_table", "wf_qkv_rope_publish", "wf_round_attention",
-           "wf_round_attention_noalloc", "wf_sync_status", "wf_plan_destroy", "wf_strerror",
+           "wf_round_attention_noalloc", "wf_round_attention_tasks", "wf_sync_status", "wf_plan_destroy", "wf_strerror",
            "wf_linear", "wf_qkv_proj_rope_publish", "wf_dit_workspace_size", "wf_dit_bind",
            "wf_dit_round", "wf_selftest_timeout", "wf_plan_state_size", "wf_plan_export_state",
-           "wf_plan_import_state", "wf_quantize_weight_e4m3", "wf_linear_e4m3"]
+           "wf_plan_import_state", "wf_quantize_weight_e4m3", "wf_linear_e4m3",
+           "wf_group_create", "wf_group_publish", "wf_group_proj_publish", "wf_group_attention",
+           "wf_group_destroy"]
 
 
 class wf_plan_opts(ctypes.Structure):
@@ -72,7 +75,8 @@ class wf_plan_opts(ctypes.Structure):
 class wf_buffer_sizes(ctypes.Structure):
     _fields_ = [("qkv", ctypes.c_size_t), ("qbuf", ctypes.c_size_t), ("pool", ctypes.c_size_t),
                 ("out", ctypes.c_size_t), ("scratch", ctypes.c_size_t),
-                ("n_pages", ctypes.c_int), ("ring_pages", ctypes.c_int)]
+                ("n_pages", ctypes.c_int), ("ring_pages", ctypes.c_int),
+                ("qk_norm_tmp", ctypes.c_size_t)]
 
 
 _T = WF_MAX_STAGES + 1
@@ -87,7 +91,7 @@ class wf_round_info(ctypes.Structure):
 
 class wf_dit_layer(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("qkv_w", "qkv_b", "o_w", "o_b", "ffn1_w", "ffn1_b",
-                                               "ffn2_w", "ffn2_b", "modulation")]
+                                               "ffn2_w", "ffn2_b", "modulation", "norm_q", "norm_k")]
 
 
 class wf_dit_model(ctypes.Structure):
@@ -115,11 +119,12 @@ def _load():
         "wf_qkv_rope_publish": (I, [P, I, VP, VP]),
         "wf_round_attention": (I, [P, I, VP, I, VP]),
         "wf_round_attention_noalloc": (I, [P, I, VP, VP]),
+        "wf_round_attention_tasks": (I, [P, I, VP, I, ctypes.c_uint, VP]),
         "wf_sync_status": (I, [P, VP]),
         "wf_plan_destroy": (None, [P]),
         "wf_strerror": (ctypes.c_char_p, [I]),
         "wf_linear": (I, [P, VP, ctypes.c_longlong, I, I, I, VP, VP, I, I, I, VP, I, VP, I, I, VP]),
-        "wf_qkv_proj_rope_publish": (I, [P, I, VP, VP, VP, VP]),
+        "wf_qkv_proj_rope_publish": (I, [P, I, VP, VP, VP, VP, VP, VP, VP]),
         "wf_dit_workspace_size": (I, [P, I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_dit_bind": (I, [P, ctypes.POINTER(wf_dit_model), VP, VP]),
         "wf_dit_round": (I, [P, VP, VP, VP, VP, VP]),
@@ -130,6 +135,11 @@ def _load():
         "wf_plan_state_size": (I, [P, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_plan_export_state": (I, [P, VP, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
         "wf_plan_import_state": (I, [P, VP, ctypes.c_size_t]),
+        "wf_group_create": (I, [ctypes.POINTER(P), I, ctypes.POINTER(P)]),
+        "wf_group_publish": (I, [P, ctypes.c_uint, I, VP, VP]),
+        "wf_group_proj_publish": (I, [P, ctypes.c_uint, I, VP, VP, VP, VP, VP, VP, VP]),
+        "wf_group_attention": (I, [P, ctypes.c_uint, I, VP, I, VP]),
+        "wf_group_destroy": (None, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -214,14 +224,15 @@ class Round:
         import torch
         return torch.float8_e4m3fn if self.dtype == WF_FP8 else self.torch_dtype
 
-    def bind(self, device="cuda"):
+    def bind(self, device="cuda", pool=None, qbuf=None):
+        """wf_bind to new device buffers, or to the given 1-D ``pool`` /
+        ``qbuf`` tensors (slices of a group's allocation)."""
         import torch
         es = {WF_FP32: 4, WF_BF16: 2, WF_FP8: 1}[self.dtype]
         s = self.sizes
-        self.pool = torch.zeros(s.pool // es, dtype=torch.uint8 if es == 1 else self.torch_dtype,
-                                device=device)
-        self.qbuf = torch.zeros(s.qbuf // es, dtype=torch.uint8 if es == 1 else self.torch_dtype,
-                                device=device)
+        store = torch.uint8 if es == 1 else self.torch_dtype
+        self.pool = pool if pool is not None else torch.zeros(s.pool // es, dtype=store, device=device)
+        self.qbuf = qbuf if qbuf is not None else torch.zeros(s.qbuf // es, dtype=store, device=device)
         if es == 1:
             self.pool = self.pool.view(self.page_dtype)
             self.qbuf = self.qbuf.view(self.page_dtype)
@@ -265,16 +276,33 @@ class Round:
         check(lib.wf_round_attention(self.plan, layer, ctypes.c_void_p(out.data_ptr()), kernel,
                                      _stream_handle(stream)), "wf_round_attention")
 
+    def attention_tasks(self, layer, out, slot_mask, kernel=WF_ATTN_AUTO, stream=None):
+        """wf_round_attention_tasks: the round attention of the active tasks
+        whose slot bit is set in slot_mask."""
+        check(lib.wf_round_attention_tasks(self.plan, layer, ctypes.c_void_p(out.data_ptr()), kernel,
+                                           slot_mask, _stream_handle(stream)),
+              "wf_round_attention_tasks")
+
     def attention_noalloc(self, layer, out, stream=None):
         """wf_round_attention_noalloc: the tensor-core kernel with its control
         words in the library's static device block (no caller scratch)."""
         check(lib.wf_round_attention_noalloc(self.plan, layer, ctypes.c_void_p(out.data_ptr()),
                                              _stream_handle(stream)), "wf_round_attention_noalloc")
 
-    def publish_proj(self, layer, x, w_qkv, b_qkv=None, stream=None):
+    def publish_proj(self, layer, x, w_qkv, b_qkv=None, norm_q=None, norm_k=None, stream=None):
         """wf_qkv_proj_rope_publish: QKV projection of x [S+1, N_C, dim] fused
-        with RoPE and paged publication."""
+        with RoPE and paged publication; with the gains norm_q / norm_k the
+        q/k RMSNorm runs before RoPE (its q | k workspace is allocated here
+        on first use)."""
+        tmp = None
+        if norm_q is not None:
+            import torch
+            if getattr(self, "_qk_tmp", None) is None:
+                self._qk_tmp = torch.empty(self.sizes.qk_norm_tmp, dtype=torch.uint8,
+                                           device=self.pool.device)
+            tmp = self._qk_tmp
         check(lib.wf_qkv_proj_rope_publish(self.plan, layer, _ptr(x), _ptr(w_qkv), _ptr(b_qkv),
+                                           _ptr(norm_q), _ptr(norm_k), _ptr(tmp),
                                            _stream_handle(stream)), "wf_qkv_proj_rope_publish")
 
     def linear(self, a, w, bias, out, epilogue, row_begin=0, row_end=None, gate=None,
@@ -347,6 +375,78 @@ class Round:
             pass
 
 
+class Group:
+    """A wf_group over ``n`` plans of one shape: one allocation for their
+    pools and query workspaces (sliced per plan), the plans themselves
+    (``rounds[r]``, each advanced with its own ``step()``), and the batched
+    launches over the members selected by ``mask``."""
+
+    def __init__(self, n, S, chunk_tokens, heads, head_dim, history, device="cuda", **kw):
+        import torch
+        self.rounds = [Round(S, chunk_tokens, heads, head_dim, history, bind=False, **kw)
+                       for _ in range(n)]
+        r0 = self.rounds[0]
+        es = {WF_FP32: 4, WF_BF16: 2, WF_FP8: 1}[r0.dtype]
+        store = torch.uint8 if es == 1 else r0.torch_dtype
+        s = r0.sizes
+        self.pool = torch.zeros(n * s.pool // es, dtype=store, device=device)
+        self.qbuf = torch.zeros(n * s.qbuf // es, dtype=store, device=device)
+        for i, r in enumerate(self.rounds):
+            r.bind(device, pool=self.pool[i * s.pool // es:(i + 1) * s.pool // es],
+                   qbuf=self.qbuf[i * s.qbuf // es:(i + 1) * s.qbuf // es])
+        plans = (ctypes.c_void_p * n)(*[r.plan.value for r in self.rounds])
+        h = ctypes.c_void_p()
+        check(lib.wf_group_create(plans, n, ctypes.byref(h)), "wf_group_create")
+        self.group, self.n = h, n
+        self.S, self.NC, self.H, self.D = S, chunk_tokens, heads, head_dim
+        self._qk_tmp = None
+
+    def new_qkv(self):
+        import torch
+        r0 = self.rounds[0]
+        return torch.zeros((self.n, self.S + 1, self.NC, 3, self.H, self.D), dtype=r0.torch_dtype,
+                           device=self.pool.device)
+
+    def new_out(self):
+        import torch
+        r0 = self.rounds[0]
+        return torch.zeros((self.n, self.S + 1, self.NC, self.H, self.D), dtype=r0.torch_dtype,
+                           device=self.pool.device)
+
+    def publish(self, mask, layer, qkv, stream=None):
+        check(lib.wf_group_publish(self.group, mask, layer, _ptr(qkv), _stream_handle(stream)),
+              "wf_group_publish")
+
+    def publish_proj(self, mask, layer, x, w_qkv, b_qkv=None, norm_q=None, norm_k=None, stream=None):
+        tmp = None
+        if norm_q is not None:
+            import torch
+            if self._qk_tmp is None:
+                self._qk_tmp = torch.empty(self.n * self.rounds[0].sizes.qk_norm_tmp, dtype=torch.uint8,
+                                           device=self.pool.device)
+            tmp = self._qk_tmp
+        check(lib.wf_group_proj_publish(self.group, mask, layer, _ptr(x), _ptr(w_qkv), _ptr(b_qkv),
+                                        _ptr(norm_q), _ptr(norm_k), _ptr(tmp), _stream_handle(stream)),
+              "wf_group_proj_publish")
+
+    def attention(self, mask, layer, out, kernel=WF_ATTN_AUTO, stream=None):
+        check(lib.wf_group_attention(self.group, mask, layer, _ptr(out), kernel, _stream_handle(stream)),
+              "wf_group_attention")
+
+    def close(self):
+        if getattr(self, "group", None):
+            lib.wf_group_destroy(self.group)
+            self.group = None
+        for r in getattr(self, "rounds", []):
+            r.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Dit:
     """A DiT model bound to a Round: device weights (torch bf16 tensors, kept
     alive here), the workspace, and ``round(z_new, eps, x0_out, chunk_out)``
@@ -373,7 +473,7 @@ class Dit:
         self._layers = (wf_dit_layer * L)()
         names = [("qkv_w", "qkv_w"), ("qkv_b", "qkv_b"), ("o_w", "o_w"), ("o_b", "o_b"),
                  ("ffn1_w", "f1_w"), ("ffn1_b", "f1_b"), ("ffn2_w", "f2_w"), ("ffn2_b", "f2_b"),
-                 ("modulation", "mod")]
+                 ("modulation", "mod"), ("norm_q", "nq"), ("norm_k", "nk")]
         for l in range(L):
             for cn, pn in names:
                 setattr(self._layers[l], cn, P[pn][l].data_ptr())

@@ -580,7 +580,7 @@ bool wf_attn_tc_supported(const WfGeom &g, int dtype) {
     return (dtype == WF_BF16 || dtype == WF_FP8) && g.D == HD;
 }
 
-cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out) {
+cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out, int n_req) {
     typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -605,12 +605,12 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
     const cuuint32_t box[3] = {f8 ? 128u : 64u, 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const cuuint64_t strides[2] = {(cuuint64_t)HD * es, (cuuint64_t)g.NC * HD * es};
-    cuuint64_t dq[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)(g.S + 1) * g.H};
+    cuuint64_t dq[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)n_req * (g.S + 1) * g.H};
     if (encode(&out->q, ty, 3, qbuf, dq, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    cuuint64_t dk[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)g.P * g.L * 2 * g.H};
+    cuuint64_t dk[3] = {(cuuint64_t)HD, (cuuint64_t)g.NC, (cuuint64_t)n_req * g.P * g.L * 2 * g.H};
     if (encode(&out->kv, ty, 3, pool, dk, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

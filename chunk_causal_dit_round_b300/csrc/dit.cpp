@@ -104,17 +104,22 @@ int wf_linear_e4m3(wf_plan_t p, const void *a8, long long a_rows, int lda, int r
 }
 
 int wf_qkv_proj_rope_publish(wf_plan_t p, int layer, const void *x, const void *w_qkv,
-                             const void *b_qkv, cudaStream_t stream) {
+                             const void *b_qkv, const void *norm_q, const void *norm_k,
+                             void *qk_tmp, cudaStream_t stream) {
     if (!p) return WF_EINVAL;
     if (!p->bound) return WF_EUNBOUND;
     if (p->k < 0) return WF_ENOROUND;
     if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
     if (!x || !w_qkv || !aligned16(x) || !aligned16(w_qkv) || (b_qkv && !aligned16(b_qkv)))
         return WF_EINVAL;
+    if ((norm_q == nullptr) != (norm_k == nullptr)) return WF_EINVAL;
+    if (norm_q && (!qk_tmp || !aligned16(norm_q) || !aligned16(norm_k) || !aligned16(qk_tmp)))
+        return WF_EINVAL;
     if (p->o.dtype != WF_BF16 && p->o.dtype != WF_FP8) return WF_EUNSUPPORTED;
     const int dim = p->H * p->D;
     if (dim % 64 || p->D % 32) return WF_EUNSUPPORTED;
-    return wf_publish_impl(p, layer, x, w_qkv, b_qkv, nullptr, stream);
+    return wf_publish_impl(p, layer, x, w_qkv, b_qkv, nullptr, stream, nullptr, norm_q, norm_k,
+                           qk_tmp);
 }
 
 int wf_dit_workspace_size(wf_plan_t p, int model_dim, int ffn_dim, int channels, int freq_dim,
@@ -154,8 +159,10 @@ int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_
     const int L = p->o.layers;
     for (int l = 0; l < L; ++l) {
         const wf_dit_layer &w = m->layers[l];
-        if (!w.qkv_w || !w.o_w || !w.ffn1_w || !w.ffn2_w || !w.modulation) return WF_EINVAL;
-        const void *all[] = {w.qkv_w, w.qkv_b, w.o_w, w.o_b, w.ffn1_w, w.ffn1_b, w.ffn2_w, w.ffn2_b};
+        if (!w.qkv_w || !w.o_w || !w.ffn1_w || !w.ffn2_w || !w.modulation || !w.norm_q || !w.norm_k)
+            return WF_EINVAL;
+        const void *all[] = {w.qkv_w, w.qkv_b, w.o_w, w.o_b, w.ffn1_w, w.ffn1_b, w.ffn2_w, w.ffn2_b,
+                             w.norm_q, w.norm_k};
         for (const void *q : all)
             if (q && !aligned16(q)) return WF_EINVAL;
     }
@@ -185,6 +192,7 @@ int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_
         const wf_dit_layer &w = m->layers[l];
         d.layers[l] = {B(w.qkv_w), B(w.qkv_b), B(w.o_w), B(w.o_b), B(w.ffn1_w),
                        B(w.ffn1_b), B(w.ffn2_w), B(w.ffn2_b), B(w.modulation),
+                       B(w.norm_q), B(w.norm_k),
                        nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     }
     const size_t latent = (size_t)d.C * p->g.gt * 4 * p->g.gh * p->g.gw;
@@ -259,8 +267,11 @@ int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_ou
         // P_{s,l}: x' = LN(x)(1 + scale_a) + shift_a; QKV projection, RoPE, publish
         if (wf_launch_ln_mod(d.x, act, r0, r1, dim, NC, mod, mod_ld, 0, dim, stream, f8) != cudaSuccess)
             return WF_ECUDA;
-        int rc = f8 ? wf_publish_impl(p, l, d.xa8, w.qkv_w8, w.qkv_b, nullptr, stream, w.qkv_s)
-                    : wf_publish_impl(p, l, d.xa, w.qkv_w, w.qkv_b, nullptr, stream);
+        // (q/k RMSNorm: the projection leaves unrotated q | k rows in hmid, free until FFN1)
+        int rc = f8 ? wf_publish_impl(p, l, d.xa8, w.qkv_w8, w.qkv_b, nullptr, stream, w.qkv_s,
+                                      w.nq, w.nk, d.hmid)
+                    : wf_publish_impl(p, l, d.xa, w.qkv_w, w.qkv_b, nullptr, stream, nullptr, w.nq,
+                                      w.nk, d.hmid);
         if (rc != WF_OK) return rc;
         // C_{s,l}: round attention (output over x', which is dead), then the rest of the block
         rc = wf_attention_impl(p, l, act, WF_ATTN_TC, stream, f8 ? 1 : 0);

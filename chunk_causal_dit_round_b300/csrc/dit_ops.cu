@@ -229,7 +229,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t wf_dit_workspace_bytes(int S, int NC, int dim, int ffn, int C, int freq, int L, size_t latent,
                               int linear_fp8) {
     const size_t rows = (size_t)(S + 1) * NC, B = S + 1;
-    size_t b = align256(rows * dim * 4) + align256(rows * dim * 2) + align256(rows * ffn * 2) +
+    const size_t hcols = ffn > 2 * dim ? ffn : 2 * dim;   // FFN hidden layer, or q | k rows
+    size_t b = align256(rows * dim * 4) + align256(rows * dim * 2) + align256(rows * hcols * 2) +
                align256(rows * 4 * C * 2) + align256(2 * B * latent * 4) +
                align256((size_t)L * B * 6 * dim * 4) + align256(B * 2 * dim * 4) +
                align256(B * (size_t)(freq + 9 * dim) * 4) + align256((size_t)L * sizeof(WfDitLayerDev)) +
@@ -249,7 +250,8 @@ void wf_dit_carve(WfDit *d, void *ws, int S, int NC, size_t latent) {
     auto take = [&](size_t bytes) { char *r = p; p += align256(bytes); return r; };
     d->x = reinterpret_cast<float *>(take(rows * d->dim * 4));
     d->xa = reinterpret_cast<__nv_bfloat16 *>(take(rows * d->dim * 2));
-    d->hmid = reinterpret_cast<__nv_bfloat16 *>(take(rows * d->ffn * 2));
+    const size_t hcols = d->ffn > 2 * d->dim ? d->ffn : 2 * d->dim;
+    d->hmid = reinterpret_cast<__nv_bfloat16 *>(take(rows * hcols * 2));
     d->patches = reinterpret_cast<__nv_bfloat16 *>(take(rows * 4 * d->C * 2));
     d->lat = reinterpret_cast<float *>(take(2 * B * latent * 4));
     d->modtab = reinterpret_cast<float *>(take((size_t)d->L * B * 6 * d->dim * 4));

@@ -268,7 +268,9 @@ struct Epi<WF_EPI_F32> {
 // K at the token's absolute (t, h, w); Q -> qbuf[slot][h][n][:], K/V ->
 // pool[dest page][layer][K|V][h][n][:]; the store of the anchor also keeps
 // its unrotated key on the raw-anchor page (App. B.3).  WF_FP8 plans store
-// e4m3 (Q and K times qk_scale, V times v_scale) instead of bf16.
+// e4m3 (Q and K times qk_scale, V times v_scale) instead of bf16.  With
+// qk_raw set, Q and K go out unrotated in bf16 for the q/k RMSNorm kernel
+// (which needs whole rows) and only V is published here.
 template <>
 struct Epi<WF_EPI_QKV_PUBLISH> {
     __device__ static void store32(__nv_bfloat16 *dst, const float (&v)[32]) {
@@ -315,10 +317,11 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
     };
     __device__ static Row row_info(const GemmParams &p, int row) {
         const WfGeom &g = p.g;
-        Row r;
+        Row r{};
         r.slot = row / g.NC;
         r.n = row - r.slot * g.NC;
-        r.ti = p.slot_task[r.slot];
+        r.ti = p.rd.task_of_slot[r.slot];
+        if (r.ti < 0) return r;                     // a slot without a task: skipped
         const int hw = g.gh * g.gw;
         const int f = r.n / hw, hh = (r.n / g.gw) % g.gh, ww = r.n - (r.n / g.gw) * g.gw;
         const int t = g.gt * p.rd.chunk[r.ti] + f;
@@ -336,13 +339,20 @@ struct Epi<WF_EPI_QKV_PUBLISH> {
         const int d0 = cc - h * g.D;                // 32 consecutive channels d0 .. d0 + 31
         const int slot = ri.slot, n = ri.n, ti = ri.ti;
         const size_t plane = (size_t)g.NC * g.D;
+        if (ti < 0) return;
+        if (part < 2 && p.qk_raw) {
+            // the block normalises q and k over the full width: leave the
+            // unrotated row for the q/k RMSNorm kernel
+            store32(p.qk_raw + ((size_t)slot * g.NC + n) * (2 * dim) + col, v);
+            return;
+        }
         if (part == 2) {
             size_t kvp = (((size_t)p.rd.dest[ti] * g.L + p.layer) * 2 + 1) * g.H + h;
             put(p, kvp * plane + (size_t)n * g.D + d0, v, g.v_scale);
             return;
         }
-        if (part == 1 && ti == p.rd.raw_copy_task) {
-            size_t rawp = (((size_t)g.raw_anchor_page * g.L + p.layer) * 2) * g.H + h;
+        if (part == 1 && p.rd.raw_page[ti] >= 0) {
+            size_t rawp = (((size_t)p.rd.raw_page[ti] * g.L + p.layer) * 2) * g.H + h;
             put(p, rawp * plane + (size_t)n * g.D + d0, v, g.qk_scale);
         }
         const float2 *tab = p.rope;

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(256) publish_kernel(const WfGeom g, const WfRo
     const unsigned nv = g.D / N;                  // vectors per (token, head) row
     const unsigned per_task = (unsigned)g.NC * g.H * nv;
     const unsigned n_task_items = per_task * rd.n_tasks;
-    const unsigned n_items = n_task_items + (rd.rerotate ? per_task : 0u);
+    const unsigned n_items = n_task_items + per_task * (unsigned)rd.n_rerot;
     const size_t plane = (size_t)g.NC * g.D;      // elements of one [NC][D] plane
     const int hw = g.gh * g.gw;
 
@@ -120,15 +120,15 @@ __global__ void __launch_bounds__(256) publish_kernel(const WfGeom g, const WfRo
             T *kdst = pool + kv_plane * plane + (size_t)n * g.D + d0;
             *reinterpret_cast<uint4 *>(kdst) = rope_vec<T>(k, d0, t, hh, ww, g, tab);
             *reinterpret_cast<uint4 *>(kdst + (size_t)g.H * plane) = vv;
-            if (ti == rd.raw_copy_task) {
-                size_t raw_plane = (((size_t)g.raw_anchor_page * g.L + layer) * 2) * g.H + h;
+            if (rd.raw_page[ti] >= 0) {
+                size_t raw_plane = (((size_t)rd.raw_page[ti] * g.L + layer) * 2) * g.H + h;
                 *reinterpret_cast<uint4 *>(pool + raw_plane * plane + (size_t)n * g.D + d0) = k;
             }
         } else {
-            // anchor re-rotation: unrotated copy -> anchor page 0 at the new position
-            int t = g.gt * rd.anchor_tpos + f;
-            size_t raw_plane = (((size_t)g.raw_anchor_page * g.L + layer) * 2) * g.H + h;
-            size_t anc_plane = (((size_t)0 * g.L + layer) * 2) * g.H + h;
+            // anchor re-rotation e = ti: unrotated copy -> anchor page at the new position
+            int t = g.gt * rd.rerot_tpos[ti] + f;
+            size_t raw_plane = (((size_t)rd.rerot_raw[ti] * g.L + layer) * 2) * g.H + h;
+            size_t anc_plane = (((size_t)rd.rerot_anchor[ti] * g.L + layer) * 2) * g.H + h;
             uint4 k = *reinterpret_cast<const uint4 *>(pool + raw_plane * plane + (size_t)n * g.D + d0);
             *reinterpret_cast<uint4 *>(pool + anc_plane * plane + (size_t)n * g.D + d0) =
                 rope_vec<T>(k, d0, t, hh, ww, g, tab);
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256) publish_fp8_kernel(const WfGeom g, const 
     const unsigned nv = g.D / 8;
     const unsigned per_task = (unsigned)g.NC * g.H * nv;
     const unsigned n_task_items = per_task * rd.n_tasks;
-    const unsigned n_items = n_task_items + (rd.rerotate ? per_task : 0u);
+    const unsigned n_items = n_task_items + per_task * (unsigned)rd.n_rerot;
     const size_t plane = (size_t)g.NC * g.D;
     const int hw = g.gh * g.gw;
     const float sqk = g.qk_scale, sv = g.v_scale;
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(256) publish_fp8_kernel(const WfGeom g, const 
             size_t kv_plane = (((size_t)rd.dest[ti] * g.L + layer) * 2) * g.H + h;
             uint8_t *kdst = pool + kv_plane * plane + (size_t)n * g.D + d0;
             *reinterpret_cast<uint2 *>(kdst + (size_t)g.H * plane) = e4m3x8(vv, sv);
-            if (ti == rd.raw_copy_task) {
-                size_t raw_plane = (((size_t)g.raw_anchor_page * g.L + layer) * 2) * g.H + h;
+            if (rd.raw_page[ti] >= 0) {
+                size_t raw_plane = (((size_t)rd.raw_page[ti] * g.L + layer) * 2) * g.H + h;
                 *reinterpret_cast<uint2 *>(pool + raw_plane * plane + (size_t)n * g.D + d0) = e4m3x8(k, sqk);
             }
             rope8(q, d0, t, hh, ww, g, tab);
@@ -226,9 +226,9 @@ __global__ void __launch_bounds__(256) publish_fp8_kernel(const WfGeom g, const 
                 e4m3x8(q, sqk);
             *reinterpret_cast<uint2 *>(kdst) = e4m3x8(k, sqk);
         } else {
-            int t = g.gt * rd.anchor_tpos + f;
-            size_t raw_plane = (((size_t)g.raw_anchor_page * g.L + layer) * 2) * g.H + h;
-            size_t anc_plane = (((size_t)0 * g.L + layer) * 2) * g.H + h;
+            int t = g.gt * rd.rerot_tpos[ti] + f;
+            size_t raw_plane = (((size_t)rd.rerot_raw[ti] * g.L + layer) * 2) * g.H + h;
+            size_t anc_plane = (((size_t)rd.rerot_anchor[ti] * g.L + layer) * 2) * g.H + h;
             float k[8];
             from_e4m3x8(*reinterpret_cast<const uint2 *>(pool + raw_plane * plane + (size_t)n * g.D + d0),
                         k, 1.f / sqk);
@@ -238,7 +238,128 @@ __global__ void __launch_bounds__(256) publish_fp8_kernel(const WfGeom g, const 
     }
 }
 
+// ---- q/k RMSNorm, RoPE and paged publication ---------------------------------
+// The standard Wan2.1 block normalises the projected q and k over the full
+// model width before RoPE ("Wave Forcing" App. D.2 keeps that architecture):
+// y = x / sqrt(mean(x^2) + 1e-6) * gain.  The QKV projection's epilogue sees
+// only 256 of a row's columns, so it leaves the unrotated q | k rows in bf16
+// and this kernel finishes them: one warp per (token row, q or k) reads the
+// row (16 bytes per lane per step, coalesced), reduces the sum of squares
+// with shuffles, then scales by the gain, rotates and stores Q into the
+// query workspace or K into its page (plus the normalised unrotated key of
+// the anchor when chunk 0 is stored).  HBM-bound: 2 dim bf16 read and 2 dim
+// elements written per token.  NV > 0 keeps the row in registers (dim =
+// 256 NV, up to 3072, where a warp still needs < 128 registers); NV = 0
+// handles any dim % 8 == 0 by reading the row twice (the second read hits
+// the caches).
+
+template <int NV, bool F8>
+__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const WfGeom g, const WfRoundDev rd,
+                                                           const WfQkNormArgs a) {
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    const int row = a.row_begin + (warp >> 1);
+    const int part = warp & 1;                        // 0: q, 1: k
+    if (row >= a.row_end) return;
+    const int dim = g.H * g.D;
+    const int nvec = dim / 8;
+    const __nv_bfloat16 *src = a.raw + (size_t)row * 2 * dim + (size_t)part * dim;
+    const __nv_bfloat16 *gain = part ? a.gk : a.gq;
+    float ss = 0.f;
+    uint4 u[NV > 0 ? NV : 1];
+    auto sumsq = [&](uint4 v) {
+        float x[8];
+        unpack(v, x, (__nv_bfloat16 *)nullptr);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+    };
+    if constexpr (NV > 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) u[i] = __ldg(reinterpret_cast<const uint4 *>(src) + lane + 32 * i);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) sumsq(u[i]);
+    } else {
+        for (int v = lane; v < nvec; v += 32) sumsq(__ldg(reinterpret_cast<const uint4 *>(src) + v));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rstd = rsqrtf(ss / (float)dim + 1e-6f);
+
+    const int slot = row / g.NC, n = row - slot * g.NC;
+    const int ti = rd.task_of_slot[slot];
+    if (ti < 0) return;                               // a slot without a task this round
+    const int hw = g.gh * g.gw;
+    const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n % g.gw;
+    const int t = g.gt * rd.chunk[ti] + f;
+    const size_t plane = (size_t)g.NC * g.D;
+    const int raw_page = part == 1 ? rd.raw_page[ti] : -1;
+    const size_t kplane = (((size_t)rd.dest[ti] * g.L + a.layer) * 2) * g.H;
+    const size_t rplane = (((size_t)(raw_page < 0 ? 0 : raw_page) * g.L + a.layer) * 2) * g.H;
+    auto emit = [&](uint4 in, int v) {
+        const int c = 8 * v;                          // channels c .. c + 7, one head
+        float x[8], w[8];
+        unpack(in, x, (__nv_bfloat16 *)nullptr);
+        unpack(__ldg(reinterpret_cast<const uint4 *>(gain) + v), w, (__nv_bfloat16 *)nullptr);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = x[i] * rstd * w[i];
+        const int h = c / g.D, d0 = c - h * g.D;
+        size_t dst;
+        if (part == 0) {
+            dst = ((size_t)slot * g.H + h) * plane + (size_t)n * g.D + d0;
+        } else {
+            dst = (kplane + h) * plane + (size_t)n * g.D + d0;
+            if (raw_page >= 0) {
+                const size_t raw = (rplane + h) * plane + (size_t)n * g.D + d0;
+                if constexpr (F8)
+                    *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.pool) + raw) = e4m3x8(x, g.qk_scale);
+                else
+                    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.pool) + raw) =
+                        pack(x, (__nv_bfloat16 *)nullptr);
+            }
+        }
+        rope8(x, d0, t, hh, ww, g, a.tab);
+        void *base = part == 0 ? a.qbuf : a.pool;
+        if constexpr (F8)
+            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(base) + dst) = e4m3x8(x, g.qk_scale);
+        else
+            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(base) + dst) =
+                pack(x, (__nv_bfloat16 *)nullptr);
+    };
+    if constexpr (NV > 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) emit(u[i], lane + 32 * i);
+    } else {
+        for (int v = lane; v < nvec; v += 32) emit(__ldg(reinterpret_cast<const uint4 *>(src) + v), v);
+    }
+}
+
+template <bool F8>
+cudaError_t launch_qk_norm(const WfGeom &g, const WfRoundDev &rd, const WfQkNormArgs &a, int blocks,
+                           cudaStream_t stream) {
+    const int dim = g.H * g.D;
+    const int nv = dim % 256 == 0 ? dim / 256 : 0;
+    switch (nv) {
+#define WF_QKN(NV) \
+    case NV: qk_norm_rope_kernel<NV, F8><<<blocks, 256, 0, stream>>>(g, rd, a); break;
+        WF_QKN(1) WF_QKN(2) WF_QKN(4) WF_QKN(6) WF_QKN(8) WF_QKN(12)
+#undef WF_QKN
+        default: qk_norm_rope_kernel<0, F8><<<blocks, 256, 0, stream>>>(g, rd, a); break;
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t wf_launch_qk_norm(const WfGeom &g, const WfRoundDev &rd, const WfQkNormArgs &a,
+                              cudaStream_t stream) {
+    if (g.D % 8 || (g.dtype != WF_BF16 && g.dtype != WF_FP8) || a.row_end <= a.row_begin)
+        return cudaErrorInvalidValue;
+    const long long warps = 2ll * (a.row_end - a.row_begin);
+    const long long blocks = (warps + 7) / 8;
+    if (blocks >= (1ll << 31)) return cudaErrorInvalidValue;
+    return g.dtype == WF_FP8 ? launch_qk_norm<true>(g, rd, a, (int)blocks, stream)
+                             : launch_qk_norm<false>(g, rd, a, (int)blocks, stream);
+}
 
 cudaError_t wf_launch_publish(const WfGeom &g, const WfRoundDev &rd, int layer, int dtype,
                               const void *qkv, void *qbuf, void *pool, const void *scratch,
@@ -249,7 +370,7 @@ cudaError_t wf_launch_publish(const WfGeom &g, const WfRoundDev &rd, int layer, 
     const int threads = 256;
     int nvec = dtype == WF_FP32 ? 4 : 8;
     if (g.D % nvec) return cudaErrorInvalidValue;
-    long long items = (long long)g.NC * g.H * (g.D / nvec) * (rd.n_tasks + (rd.rerotate ? 1 : 0));
+    long long items = (long long)g.NC * g.H * (g.D / nvec) * (rd.n_tasks + rd.n_rerot);
     if (items >= (1ll << 31)) return cudaErrorInvalidValue;
     long long want = (items + threads - 1) / threads;
     int blocks = (int)(want < (long long)sms * 8 ? want : (long long)sms * 8);

@@ -28,6 +28,11 @@ inline cudaError_t wf_once_per_device(std::atomic<unsigned long long> &done, F &
 }
 
 #define WF_MAX_TASKS (WF_MAX_STAGES + 1)
+// A round view may batch the tasks of up to WF_MAX_GROUP requests (a
+// wf_group): request r's slot s is global slot r (S+1) + s and its page p
+// global page r P + p.
+#define WF_MAX_GROUP WF_MAX_GROUP_PLANS
+#define WF_MAX_ROUND_TASKS (WF_MAX_GROUP * WF_MAX_TASKS)
 
 // Geometry of a plan, passed by value to every kernel.
 struct WfGeom {
@@ -42,18 +47,23 @@ struct WfGeom {
     float qk_scale, v_scale;   // e4m3 storage: Q, K (resp. V) multiplied by these before rounding
 };
 
-// One round as the kernels see it (host-built in wf_round_step).
+// One round as the kernels see it (host-built in wf_round_step; a group
+// concatenates the rounds of its requests with global slots and pages).
 struct WfRoundDev {
     int n_tasks;
-    int slot[WF_MAX_TASKS];        // q/out slot (== stage; S for the store)
-    int chunk[WF_MAX_TASKS];       // chunk index (temporal position of its own tokens)
-    int dest[WF_MAX_TASKS];        // page its K/V are published to
-    int n_ctx[WF_MAX_TASKS];       // chunks in its ordered context
-    int lpt[WF_MAX_TASKS];         // task indices, longest context first
-    uint8_t page[WF_MAX_TASKS][WF_MAX_CTX];  // ordered context page ids (Eq. 5)
-    int raw_copy_task;             // task whose K is also kept unrotated (store of the anchor), or -1
-    int rerotate;                  // publish launch re-rotates the anchor page
-    int anchor_tpos;               // temporal chunk position for the re-rotation
+    int slot[WF_MAX_ROUND_TASKS];        // q/out slot (request r, stage s: r (S+1) + s; S = store)
+    int chunk[WF_MAX_ROUND_TASKS];       // chunk index (temporal position of its own tokens)
+    int dest[WF_MAX_ROUND_TASKS];        // page its K/V are published to
+    int n_ctx[WF_MAX_ROUND_TASKS];       // chunks in its ordered context
+    int lpt[WF_MAX_ROUND_TASKS];         // task indices, longest context first
+    int raw_page[WF_MAX_ROUND_TASKS];    // page that also keeps its unrotated K (the store of
+                                         // an anchor chunk), or -1
+    int task_of_slot[WF_MAX_ROUND_TASKS];  // slot -> task index, -1 for an inactive slot
+    uint8_t page[WF_MAX_ROUND_TASKS][WF_MAX_CTX];  // ordered context page ids (Eq. 5)
+    // anchor re-rotations a publish launch performs: the anchor page, the
+    // page of its unrotated key, the temporal chunk position to rotate to
+    int n_rerot;
+    int rerot_anchor[WF_MAX_GROUP], rerot_raw[WF_MAX_GROUP], rerot_tpos[WF_MAX_GROUP];
 };
 
 // Scratch layout (bytes): control words first, then the RoPE tables.
@@ -70,6 +80,19 @@ cudaError_t wf_launch_publish(const WfGeom &g, const WfRoundDev &rd, int layer, 
                               const void *qkv, void *qbuf, void *pool, const void *scratch,
                               cudaStream_t stream);
 
+// q/k RMSNorm over the full width, RoPE and paged publication of rows
+// [row_begin, row_end) of raw = [rows][2 H D] unrotated bf16 q | k (the
+// QKV projection's epilogue output when the block normalises q and k).
+struct WfQkNormArgs {
+    int row_begin, row_end, layer;    // rows of inactive slots in the range are skipped
+    const __nv_bfloat16 *raw;
+    const __nv_bfloat16 *gq, *gk;     // [H D] gains of q and k
+    void *qbuf, *pool;
+    const float2 *tab;                // RoPE tables in scratch
+};
+cudaError_t wf_launch_qk_norm(const WfGeom &g, const WfRoundDev &rd, const WfQkNormArgs &a,
+                              cudaStream_t stream);
+
 cudaError_t wf_launch_attn_simt(const WfGeom &g, const WfRoundDev &rd, int layer, int dtype,
                                 const void *qbuf, const void *pool, void *out, cudaStream_t stream);
 
@@ -79,7 +102,9 @@ struct WfTmaps {
 };
 
 bool wf_attn_tc_supported(const WfGeom &g, int dtype);
-cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out);
+// Tensor maps over n_req consecutive requests' query workspaces and pools
+// (1 for a single plan).
+cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *out, int n_req = 1);
 cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
                               cudaStream_t stream, int out_e4m3 = 0);
@@ -111,11 +136,12 @@ struct GemmParams {
     uint32_t *status;            // plan scratch control words (timeouts), or null
     // QKV publication
     WfGeom g;
-    WfRoundDev rd;
+    WfRoundDev rd;               // rows of slots without a task are skipped
     int layer;
-    int slot_task[WF_MAX_TASKS]; // slot -> task index of rd
     __nv_bfloat16 *qbuf, *pool;
     const float2 *rope;
+    __nv_bfloat16 *qk_raw;       // non-null: Q/K columns stored unrotated here ([rows][2 dim]) for
+                                 // the q/k RMSNorm kernel, which rotates and publishes them
     // head + stage transition
     int channels;
     float sigma_next[WF_MAX_TASKS];  // per slot: warped sigma of the next stage (0: identity)
@@ -136,6 +162,7 @@ cudaError_t wf_launch_quant_rows(const void *w, int N, int K, void *w8, float *s
 // ---- DiT block pieces (dit_ops.cu) ------------------------------------------
 struct WfDitLayerDev {
     const __nv_bfloat16 *qkv_w, *qkv_b, *o_w, *o_b, *f1_w, *f1_b, *f2_w, *f2_b, *mod;
+    const __nv_bfloat16 *nq, *nk;   // q / k RMSNorm gains [dim]
     // e4m3 weights and per-output-channel scales (linear_fp8), in the workspace
     uint8_t *qkv_w8, *o_w8, *f1_w8, *f2_w8;
     float *qkv_s, *o_s, *f1_s, *f2_s;
@@ -153,7 +180,8 @@ struct WfDit {
     // workspace carve-up
     float *x;                    // [(S+1) N_C][dim] residual stream
     __nv_bfloat16 *xa;           // [(S+1) N_C][dim] normalised input / attention output
-    __nv_bfloat16 *hmid;         // [(S+1) N_C][ffn]
+    __nv_bfloat16 *hmid;         // [(S+1) N_C][max(ffn, 2 dim)]: FFN hidden layer; before the
+                                 // attention, the unrotated q | k rows the q/k RMSNorm reads
     __nv_bfloat16 *patches;      // [(S+1) N_C][4 C]
     float *lat;                  // [2][S+1][latent] slot inputs, double-buffered by round parity
     float *modtab;               // [L][S+1][6][dim]

@@ -130,7 +130,7 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
     WfRoundDev &rd = p->rd;
     std::memset(&rd, 0, sizeof(rd));
     rd.n_tasks = p->n_tasks;
-    rd.raw_copy_task = -1;
+    for (int i = 0; i < WF_MAX_ROUND_TASKS; ++i) rd.task_of_slot[i] = -1;
     for (int i = 0; i < p->n_tasks; ++i) {
         const HostTask &t = p->tasks[i];
         rd.slot[i] = t.stage;
@@ -138,30 +138,58 @@ void build_round(wf_plan_s *p, int store_chunk, int store_page) {
         rd.dest[i] = t.dest;
         rd.n_ctx[i] = t.n_ctx;
         for (int e = 0; e < t.n_ctx; ++e) rd.page[i][e] = (uint8_t)t.ctx[e].page;
-        if (t.stage == S && p->o.use_anchor && t.chunk == 0) rd.raw_copy_task = i;
+        // the store of the anchor chunk also keeps its unrotated key (App. B.3)
+        rd.raw_page[i] = (t.stage == S && p->o.use_anchor && t.chunk == 0) ? p->g.raw_anchor_page : -1;
+        rd.task_of_slot[t.stage] = i;
         rd.lpt[i] = i;
     }
     std::stable_sort(rd.lpt, rd.lpt + p->n_tasks,
                      [&](int a, int b) { return rd.n_ctx[a] > rd.n_ctx[b]; });
-    rd.anchor_tpos = p->anchor_tpos;
-    rd.rerotate = 0;
+    rd.n_rerot = 0;
 }
 
 }  // namespace
 
+namespace {
+// The round restricted to the tasks whose slot bit is set in mask (longest
+// context first, as in the full round).
+WfRoundDev subset_round(const WfRoundDev &rd, unsigned mask) {
+    WfRoundDev r = rd;
+    r.n_tasks = 0;
+    for (int i = 0; i < WF_MAX_ROUND_TASKS; ++i) r.task_of_slot[i] = -1;
+    for (int i = 0; i < rd.n_tasks; ++i) {
+        if (!((mask >> rd.slot[i]) & 1u)) continue;
+        const int o = r.n_tasks++;
+        r.slot[o] = rd.slot[i];
+        r.chunk[o] = rd.chunk[i];
+        r.dest[o] = rd.dest[i];
+        r.n_ctx[o] = rd.n_ctx[i];
+        r.raw_page[o] = rd.raw_page[i];
+        std::memcpy(r.page[o], rd.page[i], sizeof(rd.page[i]));
+        r.task_of_slot[r.slot[o]] = o;
+        r.lpt[o] = o;
+    }
+    std::stable_sort(r.lpt, r.lpt + r.n_tasks, [&](int a, int b) { return r.n_ctx[a] > r.n_ctx[b]; });
+    r.n_rerot = 0;
+    return r;
+}
+}  // namespace
+
 int wf_attention_impl(wf_plan_s *p, int layer, void *out, int kernel, cudaStream_t stream,
-                      int out_e4m3) {
+                      int out_e4m3, unsigned slot_mask) {
+    const WfRoundDev rd = slot_mask == ~0u ? p->rd : subset_round(p->rd, slot_mask);
+    if (rd.n_tasks == 0) return WF_OK;
     bool tc_ok = p->tmaps_ok && wf_attn_tc_supported(p->g, p->o.dtype);
     bool simt_ok = p->D % 32 == 0 && p->D <= 128 && p->o.dtype != WF_FP8 && !out_e4m3;
     if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
     cudaError_t e;
     if (kernel == WF_ATTN_TC) {
         if (!tc_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_tc(p->g, p->rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream,
+        e = wf_launch_attn_tc(p->g, rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream,
                               out_e4m3);
     } else {
         if (!simt_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_simt(p->g, p->rd, layer, p->o.dtype, p->qbuf, p->pool, out, stream);
+        e = wf_launch_attn_simt(p->g, rd, layer, p->o.dtype, p->qbuf, p->pool, out, stream);
     }
     return e == cudaSuccess ? WF_OK : WF_ECUDA;
 }
@@ -178,55 +206,107 @@ void wf_rebuild_round(wf_plan_s *p) {
 // Shared by wf_qkv_rope_publish (Q/K/V given) and the projection path
 // (x and W_qkv given): one launch publishes every active task; the anchor
 // key is re-rotated from its unrotated copy when the window moved.
-int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
-                    const void *qkv, cudaStream_t stream, const float *wscale) {
-    WfRoundDev rd = p->rd;
-    int new_rot = p->anchor_rot[layer];
-    bool rerotate = false;
-    if (rd.raw_copy_task >= 0) {
-        new_rot = 0;  // the store of chunk 0 writes the anchor at its own position
+void wf_anchor_update(const wf_plan_s *p, int layer, bool *rerotate, int *new_rot) {
+    *rerotate = false;
+    *new_rot = p->anchor_rot[layer];
+    bool stores_anchor = false;
+    for (int i = 0; i < p->rd.n_tasks; ++i) stores_anchor |= p->rd.raw_page[i] >= 0;
+    if (stores_anchor) {
+        *new_rot = 0;  // the store of chunk 0 writes the anchor at its own position
     } else if (p->anchor_tpos >= 0 && p->anchor_rot[layer] != p->anchor_tpos) {
-        rerotate = true;
-        new_rot = p->anchor_tpos;
+        *rerotate = true;
+        *new_rot = p->anchor_tpos;
     }
-    if (x) {
-        int lo, hi;
-        wf_active_range(p, &lo, &hi);
+}
+
+int wf_publish_launch(const WfPublishArgs &a, const WfRoundDev &rd, cudaStream_t stream) {
+    const WfGeom &g = a.g;
+    if (a.x) {
         GemmParams gp;
         std::memset(&gp, 0, sizeof(gp));
-        gp.row_begin = lo * p->NC;
-        gp.row_end = (hi + 1) * p->NC;
-        gp.N = 3 * p->H * p->D;
-        gp.K = p->H * p->D;
-        gp.bias = static_cast<const __nv_bfloat16 *>(b_qkv);
-        gp.status = static_cast<uint32_t *>(p->scratch);
-        gp.g = p->g;
+        gp.row_begin = a.row_begin;
+        gp.row_end = a.row_end;
+        gp.N = 3 * g.H * g.D;
+        gp.K = g.H * g.D;
+        gp.bias = static_cast<const __nv_bfloat16 *>(a.b_qkv);
+        gp.status = static_cast<uint32_t *>(a.scratch);
+        gp.g = g;
         gp.rd = rd;
-        gp.layer = layer;
-        for (int i = 0; i < WF_MAX_TASKS; ++i) gp.slot_task[i] = -1;
-        for (int i = 0; i < rd.n_tasks; ++i) gp.slot_task[rd.slot[i]] = i;
-        gp.qbuf = static_cast<__nv_bfloat16 *>(p->qbuf);
-        gp.pool = static_cast<__nv_bfloat16 *>(p->pool);
-        gp.rope = reinterpret_cast<const float2 *>(static_cast<const char *>(p->scratch) +
+        gp.rd.n_rerot = 0;
+        gp.layer = a.layer;
+        gp.qbuf = static_cast<__nv_bfloat16 *>(a.qbuf);
+        gp.pool = static_cast<__nv_bfloat16 *>(a.pool);
+        gp.rope = reinterpret_cast<const float2 *>(static_cast<const char *>(a.scratch) +
                                                    WF_SCRATCH_TABLES);
-        gp.wscale = wscale;
-        if (wf_launch_gemm(WF_EPI_QKV_PUBLISH, x, (long long)(p->S + 1) * p->NC, gp.K, w_qkv, gp,
-                           p->num_sms, stream, wscale != nullptr) != cudaSuccess)
+        gp.wscale = a.wscale;
+        gp.qk_raw = a.nq ? static_cast<__nv_bfloat16 *>(a.qk_tmp) : nullptr;
+        if (wf_launch_gemm(WF_EPI_QKV_PUBLISH, a.x, a.x_rows, gp.K, a.w_qkv, gp, a.num_sms, stream,
+                           a.wscale != nullptr) != cudaSuccess)
             return WF_ECUDA;
-        if (rerotate) {
+        if (a.nq) {
+            WfQkNormArgs n;
+            std::memset(&n, 0, sizeof(n));
+            n.row_begin = a.row_begin;
+            n.row_end = a.row_end;
+            n.layer = a.layer;
+            n.raw = gp.qk_raw;
+            n.gq = static_cast<const __nv_bfloat16 *>(a.nq);
+            n.gk = static_cast<const __nv_bfloat16 *>(a.nk);
+            n.qbuf = a.qbuf;
+            n.pool = a.pool;
+            n.tab = gp.rope;
+            if (wf_launch_qk_norm(g, gp.rd, n, stream) != cudaSuccess) return WF_ECUDA;
+        }
+        if (rd.n_rerot > 0) {
             WfRoundDev rr = rd;
             rr.n_tasks = 0;
-            rr.rerotate = 1;
-            if (wf_launch_publish(p->g, rr, layer, p->o.dtype, nullptr, p->qbuf, p->pool, p->scratch,
+            if (wf_launch_publish(g, rr, a.layer, g.dtype, nullptr, a.qbuf, a.pool, a.scratch,
                                   stream) != cudaSuccess)
                 return WF_ECUDA;
         }
-    } else {
-        rd.rerotate = rerotate ? 1 : 0;
-        if (wf_launch_publish(p->g, rd, layer, p->o.dtype, qkv, p->qbuf, p->pool, p->scratch,
-                              stream) != cudaSuccess)
-            return WF_ECUDA;
+    } else if (wf_launch_publish(g, rd, a.layer, g.dtype, a.qkv, a.qbuf, a.pool, a.scratch,
+                                 stream) != cudaSuccess) {
+        return WF_ECUDA;
     }
+    return WF_OK;
+}
+
+int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
+                    const void *qkv, cudaStream_t stream, const float *wscale, const void *nq,
+                    const void *nk, void *qk_tmp) {
+    bool rerotate;
+    int new_rot;
+    wf_anchor_update(p, layer, &rerotate, &new_rot);
+    WfRoundDev rd = p->rd;
+    if (rerotate) {
+        rd.n_rerot = 1;
+        rd.rerot_anchor[0] = 0;
+        rd.rerot_raw[0] = p->g.raw_anchor_page;
+        rd.rerot_tpos[0] = p->anchor_tpos;
+    }
+    int lo, hi;
+    wf_active_range(p, &lo, &hi);
+    WfPublishArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.g = p->g;
+    a.layer = layer;
+    a.row_begin = lo * p->NC;
+    a.row_end = (hi + 1) * p->NC;
+    a.x = x;
+    a.x_rows = (long long)(p->S + 1) * p->NC;
+    a.w_qkv = w_qkv;
+    a.b_qkv = b_qkv;
+    a.wscale = wscale;
+    a.nq = nq;
+    a.nk = nk;
+    a.qk_tmp = qk_tmp;
+    a.qkv = qkv;
+    a.qbuf = p->qbuf;
+    a.pool = p->pool;
+    a.scratch = p->scratch;
+    a.num_sms = p->num_sms;
+    const int rc = wf_publish_launch(a, rd, stream);
+    if (rc != WF_OK) return rc;
     p->anchor_rot[layer] = new_rot;
     p->published[layer] = p->k;
     return WF_OK;
@@ -361,6 +441,7 @@ int wf_plan_buffer_sizes(wf_plan_t p, wf_buffer_sizes *out) {
     if (!mul_ok(ptok, (size_t)p->P * p->o.layers, &a) || !mul_ok(a, 2, &b)) return WF_ERANGE;
     out->pool = b;
     out->scratch = WF_SCRATCH_TABLES + tables_bytes(p->g);
+    out->qk_norm_tmp = (size_t)p->NC * p->H * p->D * 2 * 2 * slots;
     out->n_pages = p->P;
     out->ring_pages = p->R;
     return WF_OK;
@@ -495,6 +576,19 @@ int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream
     if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
     if (p->published[layer] != p->k) return WF_EORDER;
     return wf_attention_impl(p, layer, out, kernel, stream);
+}
+
+int wf_round_attention_tasks(wf_plan_t p, int layer, void *out, int kernel, unsigned int slot_mask,
+                             cudaStream_t stream) {
+    if (!p) return WF_EINVAL;
+    if (!p->bound) return WF_EUNBOUND;
+    if (p->k < 0) return WF_ENOROUND;
+    if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
+    if (!out || ((uintptr_t)out & 15)) return WF_EINVAL;
+    if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
+    if (slot_mask >> (p->S + 1)) return WF_EINVAL;
+    if (p->published[layer] != p->k) return WF_EORDER;
+    return wf_attention_impl(p, layer, out, kernel, stream, 0, slot_mask);
 }
 
 int wf_round_attention_noalloc(wf_plan_t p, int layer, void *out, cudaStream_t stream) {

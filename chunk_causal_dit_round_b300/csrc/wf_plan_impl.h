@@ -74,11 +74,39 @@ void wf_rebuild_round(wf_plan_s *p);
 // Launch the QKV publication for `layer` of the current round: either the
 // projection GEMM (x != nullptr) or the given Q/K/V; the anchor re-rotation
 // when the window moved.  Returns a WF_* code.
+// Anchor bookkeeping of a plan's publication of `layer` in its current
+// round: whether its anchor page must be re-rotated from the unrotated copy
+// and the position the page holds afterwards (App. B.3).
+void wf_anchor_update(const wf_plan_s *p, int layer, bool *rerotate, int *new_rot);
+
+// The launches of one publication over a round view (a plan's or a
+// group's): the projection GEMM (x set; with gains, then the q/k RMSNorm
+// kernel) or the given-Q/K/V kernel, and rd's anchor re-rotations.
+struct WfPublishArgs {
+    WfGeom g;
+    int layer;
+    int row_begin, row_end;      // projection rows (slots without a task are skipped)
+    const void *x;               // [x_rows][dim] or null
+    long long x_rows;
+    const void *w_qkv, *b_qkv;
+    const float *wscale;         // e4m3 weights: per output channel scale, else null
+    const void *nq, *nk;         // q / k RMSNorm gains, or null
+    void *qk_tmp;
+    const void *qkv;             // given Q/K/V when x is null
+    void *qbuf, *pool, *scratch;
+    int num_sms;
+};
+int wf_publish_launch(const WfPublishArgs &a, const WfRoundDev &rd, cudaStream_t stream);
+
+// With gains nq / nk (projection path only) the projection leaves unrotated
+// q | k rows in qk_tmp and the q/k RMSNorm kernel publishes them.
 int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, const void *b_qkv,
-                    const void *qkv, cudaStream_t stream, const float *wscale = nullptr);
+                    const void *qkv, cudaStream_t stream, const float *wscale = nullptr,
+                    const void *nq = nullptr, const void *nk = nullptr, void *qk_tmp = nullptr);
 
 // Round attention of `layer` after the argument checks of wf_round_attention;
-// out_e4m3 writes O as e4m3 bytes (tensor-core kernel).  Returns a WF_* code.
+// out_e4m3 writes O as e4m3 bytes (tensor-core kernel); slot_mask selects the
+// tasks by slot (all by default).  Returns a WF_* code.
 int wf_attention_impl(wf_plan_s *p, int layer, void *out, int kernel, cudaStream_t stream,
-                      int out_e4m3 = 0);
+                      int out_e4m3 = 0, unsigned slot_mask = ~0u);
 

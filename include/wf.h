@@ -133,6 +133,8 @@ typedef struct wf_buffer_sizes {
     size_t scratch;  /* bytes of library scratch (RoPE tables, scheduler counters, status) */
     int n_pages;     /* P */
     int ring_pages;  /* R: clean-history ring incl. the live store page */
+    size_t qk_norm_tmp; /* bytes of the q | k workspace wf_qkv_proj_rope_publish needs when it
+                           normalises q and k: (S+1) N_C 2 H D bf16 */
 } wf_buffer_sizes;
 
 typedef struct wf_round_info {
@@ -212,6 +214,19 @@ int wf_qkv_rope_publish(wf_plan_t plan, int layer, const void *qkv, cudaStream_t
  * available for dtype/head_dim), WF_ECUDA. */
 int wf_round_attention(wf_plan_t plan, int layer, void *out, int kernel, cudaStream_t stream);
 
+/* Round attention of a subset of the round's tasks: as wf_round_attention,
+ * for the active tasks whose slot s has bit s set in slot_mask (other slots
+ * of out are not written).  Each task's result does not depend on which
+ * other tasks share the launch (every (task, head, query tile) unit reads
+ * only its own context, in a fixed order), so launching the tasks one at a
+ * time -- e.g. the store, then stages S-1 .. 0, the sequential replay of
+ * "Wave Forcing" App. B.6 Proposition 1 -- gives bit-identical outputs to
+ * the batched launch.  Lets a caller run the store pass first or split a
+ * round over streams.  A mask selecting no active task launches nothing.
+ * Errors: as wf_round_attention, plus WF_EINVAL (bits above slot S set). */
+int wf_round_attention_tasks(wf_plan_t plan, int layer, void *out, int kernel,
+                             unsigned int slot_mask, cudaStream_t stream);
+
 /* Round attention without caller-provided scratch.  The paper has no
  * counterpart: this is a library convenience.
  *
@@ -245,6 +260,58 @@ int wf_round_attention(wf_plan_t plan, int layer, void *out, int kernel, cudaStr
  * and WF_ECUDA (symbol lookup, memset or launch failed). */
 #define WF_NOALLOC_SCRATCH_BYTES 256
 int wf_round_attention_noalloc(wf_plan_t plan, int layer, void *out, cudaStream_t stream);
+
+/* ---- several requests batched into one round ------------------------------
+ * "Wave Forcing" names serving concurrent streams with batching as the next
+ * step (Sec. 8 Future Work; App. E).  A group batches the current rounds of
+ * up to WF_MAX_GROUP_PLANS independent requests into single launches.
+ *
+ * Each member plan keeps its own schedule, page ring and anchor and is
+ * advanced with wf_round_step as before: members may start at different
+ * times and finish on their own.  A group call takes plan_mask (bit r:
+ * member r takes part; a member that has not entered a round yet or has
+ * finished is left out) and concatenates the selected members' rounds: the
+ * tasks of member r use slot r (S+1) + s and page r P + p of the group's
+ * buffers, so one launch serves all of them and every member gets exactly
+ * what its own wf_qkv_rope_publish / wf_round_attention would compute.
+ *
+ * wf_group_create: plans[0 .. n-1] (1 <= n <= WF_MAX_GROUP_PLANS), distinct,
+ *   bound, of one shape (every plan option that fixes the buffers' layout or
+ *   bytes equal: S, N_C, H, D, W, n_chunks, layers, grid, dtype, RoPE, e4m3
+ *   scales), on one device, whose pools and query workspaces are consecutive
+ *   slices of one allocation: plan r's pool at plan 0's pool + r * pool
+ *   bytes, its query workspace at plan 0's + r * qbuf bytes
+ *   (wf_plan_buffer_sizes).  n * n_pages <= 256.  The group keeps the
+ *   pointers: the plans must outlive it and stay bound to those buffers.
+ *   Group launches use plan 0's scratch (RoPE tables, scheduler counters,
+ *   status): read timeouts with wf_sync_status(plans[0]) and do not overlap
+ *   them with plan 0's own launches.  Errors: WF_EINVAL (null, duplicate,
+ *   shape or layout mismatch), WF_ERANGE (n, page ids), WF_EUNBOUND,
+ *   WF_ECUDA (tensor maps).
+ * wf_group_publish: as wf_qkv_rope_publish for every selected member, one
+ *   launch (plus the members' anchor re-rotations in the same launch);
+ *   qkv [n][S+1][N_C][3][H][D].
+ * wf_group_proj_publish: as wf_qkv_proj_rope_publish for every selected
+ *   member, one projection GEMM over their rows; x [n][S+1][N_C][dim];
+ *   qk_tmp (with the q/k RMSNorm gains) n * wf_buffer_sizes.qk_norm_tmp
+ *   bytes.
+ * wf_group_attention: as wf_round_attention for every selected member, one
+ *   launch; out [n][S+1][N_C][H][D].  WF_EORDER when a selected member has
+ *   not published this layer in its current round.
+ * Errors of the launching calls: as their single-plan counterparts, plus
+ *   WF_EINVAL (empty mask or bits beyond n), WF_ENOROUND (a selected member
+ *   has no current round). */
+#define WF_MAX_GROUP_PLANS 8
+typedef struct wf_group_s *wf_group_t;
+int wf_group_create(const wf_plan_t *plans, int n, wf_group_t *out);
+int wf_group_publish(wf_group_t group, unsigned int plan_mask, int layer, const void *qkv,
+                     cudaStream_t stream);
+int wf_group_proj_publish(wf_group_t group, unsigned int plan_mask, int layer, const void *x,
+                          const void *w_qkv, const void *b_qkv, const void *norm_q,
+                          const void *norm_k, void *qk_tmp, cudaStream_t stream);
+int wf_group_attention(wf_group_t group, unsigned int plan_mask, int layer, void *out, int kernel,
+                       cudaStream_t stream);
+void wf_group_destroy(wf_group_t group);
 
 /* ---- linear layers on the tensor cores -------------------------------------
  * out = epilogue(A W^T + bias) for rows row_begin .. row_end-1 of A.
@@ -301,10 +368,20 @@ int wf_linear_e4m3(wf_plan_t plan, const void *a8, long long a_rows, int lda, in
  *   w_qkv  bf16 [3 dim][dim]: rows 0..dim-1 produce Q, then K, then V; head h
  *          of each part is rows h*head_dim .. h*head_dim + head_dim - 1
  *   b_qkv  bf16 [3 dim] or NULL
+ *   norm_q, norm_k  bf16 [dim] gains of the standard Wan2.1 block's q/k
+ *          RMSNorm (App. D.2 keeps that architecture), or both NULL for no
+ *          normalisation: q <- q / sqrt(mean(q^2) + 1e-6) * norm_q over the
+ *          full width (all heads of a token), likewise k, before RoPE.  The
+ *          projection then writes the unrotated q | k rows (bf16) to
+ *   qk_tmp  device workspace of wf_buffer_sizes.qk_norm_tmp bytes (16-byte
+ *          aligned; ignored without norms), and a second, memory-bound
+ *          launch normalises, rotates and publishes them
  * bf16 or WF_FP8 plans (e4m3 pages), dim % 64 == 0, head_dim % 32 == 0.
- * Errors: as wf_qkv_rope_publish, plus WF_EUNSUPPORTED. */
+ * Errors: as wf_qkv_rope_publish, plus WF_EUNSUPPORTED; WF_EINVAL when only
+ * one gain is given or qk_tmp is missing. */
 int wf_qkv_proj_rope_publish(wf_plan_t plan, int layer, const void *x, const void *w_qkv,
-                             const void *b_qkv, cudaStream_t stream);
+                             const void *b_qkv, const void *norm_q, const void *norm_k,
+                             void *qk_tmp, cudaStream_t stream);
 
 /* ---- the chunk-wise causal DiT round --------------------------------------
  * Weights of one transformer block (device pointers, bf16, linear weights
@@ -315,13 +392,15 @@ typedef struct wf_dit_layer {
     const void *ffn1_w, *ffn1_b;   /* [ffn][dim], [ffn] */
     const void *ffn2_w, *ffn2_b;   /* [dim][ffn], [dim] */
     const void *modulation;        /* [6][dim]: shift, scale, gate of attention, then of FFN */
+    const void *norm_q, *norm_k;   /* [dim], [dim]: gains of the q / k RMSNorm (required) */
 } wf_dit_layer;
 
 /* A Wan2.1-style DiT without text cross-attention (the pages omit text
  * conditioning, Sec. 2).  The block, as this library computes it:
  *   (shift_a, scale_a, gate_a, shift_f, scale_f, gate_f) = modulation + e0(t)
  *   x' = LN(x)(1 + scale_a) + shift_a   (LayerNorm eps 1e-6, no affine)
- *   Q,K,V = x' W_qkv^T + b; RoPE on Q, K; x += gate_a (Attn W_o^T + b_o)
+ *   Q,K,V = x' W_qkv^T + b; Q = RMSNorm(Q) norm_q, K = RMSNorm(K) norm_k
+ *   (over the full width, eps 1e-6); RoPE on Q, K; x += gate_a (Attn W_o^T + b_o)
  *   x += gate_f (GELU_tanh((LN(x)(1 + scale_f) + shift_f) W_1^T + b_1) W_2^T + b_2)
  * with the timestep embedding e(t) = W_t2 SiLU(W_t1 sinusoid(t) + b) + b,
  * e0 = W_tp SiLU(e) + b_tp; patch embedding of (1,2,2) patches of C

@@ -184,12 +184,39 @@ def test_dit_entry_points_validate_before_any_cuda_call():
         assert wf.lib.wf_dit_bind(h, None, ctypes.c_void_p(256), None) == wf.WF_EINVAL
         assert wf.lib.wf_dit_round(h, None, None, None, None, None) == wf.WF_EUNBOUND
         p = ctypes.c_void_p(256)
-        assert wf.lib.wf_qkv_proj_rope_publish(h, 0, p, p, None, None) == wf.WF_EUNBOUND
+        assert wf.lib.wf_qkv_proj_rope_publish(h, 0, p, p, None, None, None, None, None) == wf.WF_EUNBOUND
         assert wf.lib.wf_linear(h, p, 128, 64, 0, 128, p, None, 64, 64, wf.WF_EPI_F32, p, 64,
                                 None, 0, 1, None) == wf.WF_EUNBOUND
         assert wf.lib.wf_linear(None, p, 128, 64, 0, 128, p, None, 64, 64, wf.WF_EPI_F32, p, 64,
                                 None, 0, 1, None) == wf.WF_EINVAL
     finally:
+        wf.lib.wf_plan_destroy(h)
+
+
+def test_group_entry_points_validate_on_the_host():
+    """wf_group_create refuses unbound plans, bad counts and null
+    arguments before any CUDA call; the launching calls refuse a null group."""
+    plans = []
+    for _ in range(2):
+        rc, h = _plan(2, 48, 1, 32, 1, n_chunks=4, grid_h=4, grid_w=4)
+        assert rc == wf.WF_OK
+        plans.append(h)
+    arr = (ctypes.c_void_p * 2)(plans[0].value, plans[1].value)
+    g = ctypes.c_void_p()
+    assert wf.lib.wf_group_create(arr, 2, ctypes.byref(g)) == wf.WF_EUNBOUND
+    assert wf.lib.wf_group_create(arr, 0, ctypes.byref(g)) == wf.WF_ERANGE
+    assert wf.lib.wf_group_create(arr, wf.WF_MAX_GROUP_PLANS + 1, ctypes.byref(g)) == wf.WF_ERANGE
+    assert wf.lib.wf_group_create(None, 2, ctypes.byref(g)) == wf.WF_EINVAL
+    assert wf.lib.wf_group_create(arr, 2, None) == wf.WF_EINVAL
+    dup = (ctypes.c_void_p * 2)(plans[0].value, plans[0].value)
+    assert wf.lib.wf_group_create(dup, 2, ctypes.byref(g)) == wf.WF_EINVAL
+    assert g.value is None
+    p = ctypes.c_void_p(256)
+    assert wf.lib.wf_group_attention(None, 1, 0, p, wf.WF_ATTN_TC, None) == wf.WF_EINVAL
+    assert wf.lib.wf_group_publish(None, 1, 0, p, None) == wf.WF_EINVAL
+    assert wf.lib.wf_group_proj_publish(None, 1, 0, p, p, None, None, None, None, None) == wf.WF_EINVAL
+    wf.lib.wf_group_destroy(None)
+    for h in plans:
         wf.lib.wf_plan_destroy(h)
 
 

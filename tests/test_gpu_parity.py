@@ -58,7 +58,7 @@ SMALL = Geom(grid_t=3, grid_h=10, grid_w=10, heads=2, head_dim=128)   # 300 toke
 
 
 @pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
-@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(2, 6, -1),
+@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3), sch.Cfg(2, 6, -1),
                                  sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE),
                                  sch.Cfg(2, 5, 2, use_anchor=False),
                                  sch.Cfg(4, 10, 3, mask=sch.MASK_RF),
@@ -116,7 +116,8 @@ def test_bf16_request_custom_rope_split():
     assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
-@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3)] + DEGENERATE + STORE_EXTRA, ids=str)
+@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3)] + DEGENERATE + STORE_EXTRA,
+                         ids=str)
 @pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 def test_visibility_fingerprint(kernel, cfg):
     """Q = 0 makes softmax uniform over the visible keys; V one-hot in the
@@ -198,6 +199,54 @@ def test_tc_deterministic_and_matches_simt():
         assert torch.equal(a, b)
         d = (a.float() - c.float()).abs() / c.float().abs().clamp(min=1.0)
         assert d.max().item() <= 2e-2 and d.mean().item() <= 2e-3
+    assert r.sync_status() == wf.WF_OK
+
+
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
+@pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3), sch.Cfg(3, 7, 1, mask=sch.MASK_RF)],
+                         ids=str)
+def test_batched_launch_equals_per_task_replay(cfg, kernel):
+    """App. B.6 Proposition 1 on the GPU: one batched launch over the round's
+    tasks gives bit-identical outputs to launching the same kernel once per
+    task in the sequential replay order (store, then stages S-1 .. 0), every
+    round of the request."""
+    geom = SMALL
+    r = make_round(cfg, geom, wf.WF_BF16)
+    _, traw = raw_fn(29, geom, torch.bfloat16, qk_scale=2.0)
+    batched, replay = r.new_out(), r.new_out()
+    for k in range(sch.n_rounds(cfg)):
+        info = r.step()
+        r.publish(0, fill_qkv(r, info, traw, 0))
+        batched.fill_(float("nan"))
+        replay.fill_(float("nan"))
+        r.attention(0, batched, kernel)
+        stages = sorted((info.task_stage[i] for i in range(info.n_tasks)), reverse=True)
+        for s in stages:
+            r.attention_tasks(0, replay, 1 << s, kernel)
+        torch.cuda.synchronize()
+        for s in stages:
+            assert torch.equal(batched[s], replay[s]), (k, s)
+            assert torch.isfinite(batched[s]).all()
+        # slots that are not active in this round are left untouched
+        for s in set(range(cfg.S + 1)) - set(stages):
+            assert torch.isnan(replay[s]).all()
+    assert r.sync_status() == wf.WF_OK
+
+
+def test_task_subset_rejects_bad_masks():
+    cfg = sch.Cfg(2, 4, 1)
+    r = make_round(cfg, SMALL, wf.WF_BF16)
+    info = r.step()
+    out = r.new_out()
+    fn = wf.lib.wf_round_attention_tasks
+    assert fn(r.plan, 0, out.data_ptr(), wf.WF_ATTN_TC, 1, None) == wf.WF_EORDER
+    r.publish(0, fill_qkv(r, info, raw_fn(1, SMALL, torch.bfloat16)[1], 0))
+    assert fn(r.plan, 0, out.data_ptr(), wf.WF_ATTN_TC, 1 << (cfg.S + 1), None) == wf.WF_EINVAL
+    assert fn(r.plan, 0, out.data_ptr(), 7, 1, None) == wf.WF_EINVAL
+    assert fn(r.plan, 1, out.data_ptr(), wf.WF_ATTN_TC, 1, None) == wf.WF_ERANGE
+    # round 0 has only stage 0: a mask of inactive slots launches nothing
+    assert fn(r.plan, 0, out.data_ptr(), wf.WF_ATTN_TC, 0b110, None) == wf.WF_OK
+    torch.cuda.synchronize()
     assert r.sync_status() == wf.WF_OK
 
 
