@@ -49,7 +49,7 @@ UNIT = "TFLOP/s"
 # again.
 ATTN_TC_SOURCES = ("chunk_causal_dit_round_b300/csrc/attn_tc.cu",
                    "chunk_causal_dit_round_b300/csrc/wf_ptx.cuh")
-ATTN_TC_TRAFFIC = {"bf16": (1.2571e9, "0" * 16), "e4m3": (6.061e8, "0" * 16)}
+ATTN_TC_TRAFFIC = {"bf16": (1.2591e9, "4bc1dbc751bd96d4"), "e4m3": (6.117e8, "4bc1dbc751bd96d4")}
 
 
 def _sources_sha16(paths):
@@ -214,6 +214,9 @@ STREAM_SHAPES = {
     # chunk (3 latent frames) and a one-latent-frame chunk
     "chunk4680": dict(grid=(3, 30, 52), desc="3 latent frames x 30 x 52 patches"),
     "chunk1560": dict(grid=(1, 30, 52), desc="1 latent frame x 30 x 52 patches"),
+    # a quarter-size frame (240 x 416 video): one request's round has 120
+    # work units, fewer than the SMs
+    "chunk390": dict(grid=(1, 15, 26), desc="1 latent frame x 15 x 26 patches"),
 }
 
 
@@ -239,7 +242,7 @@ def run_streams(args, rank, world, counts=(1, 2, 4, 8), steps=10, warmup=3):
         NC = math.prod(shp["grid"])
         rows = []
         for R in counts:
-            grp = wf.Group(R, S, NC, H, D, W, n_chunks=k_steady + warmup + steps + 2, grid=shp["grid"],
+            grp = wf.Group(R, S, NC, H, D, W, n_chunks=k_steady + warmup + 400, grid=shp["grid"],
                            dtype=wf.WF_BF16, device=dev)
             g = torch.Generator(device=dev)
             g.manual_seed(99 + R)
@@ -262,22 +265,31 @@ def run_streams(args, rank, world, counts=(1, 2, 4, 8), steps=10, warmup=3):
             for i in range(k_steady + warmup):
                 one(i)
             torch.cuda.synchronize()
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(steps)]
-            flops = 0.0
-            for j in range(steps):
-                evs[j][0].record(stream)
-                flops += one(j)
-                evs[j][1].record(stream)
+            # time at least ~0.3 s per row so the clock sampler sees it
+            t0 = time.perf_counter()
+            one(0)
             torch.cuda.synchronize()
+            n_t = max(steps, int(0.3 / max(time.perf_counter() - t0, 1e-4)))
+            n_t = min(n_t, grp.rounds[0].n_left())
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_t)]
+            flops = 0.0
+            with ClockSampler(dev.index) as clk:
+                torch.cuda.synchronize()
+                for j in range(n_t):
+                    evs[j][0].record(stream)
+                    flops += one(j)
+                    evs[j][1].record(stream)
+                torch.cuda.synchronize()
             st = grp.rounds[0].sync_status()
             if st != wf.WF_OK:
                 raise RuntimeError(f"device status {st}")
             per = [a.elapsed_time(b) for a, b in evs]
             ms, = max_over_ranks([sum(per)], world, dev)
-            rows.append({"requests": R, "chunks_per_s": round(world * R * steps / (ms * 1e-3), 2),
-                         "round_ms": round(ms / steps, 4),
-                         "attn_tflops": round(flops / (ms * 1e-3) / 1e12, 1)})
+            rows.append({"requests": R, "chunks_per_s": round(world * R * n_t / (ms * 1e-3), 2),
+                         "round_ms": round(ms / n_t, 4), "rounds": n_t,
+                         "attn_tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                         "clocks": clk.summary()})
             grp.close()
             del grp, qkvs, o
             torch.cuda.empty_cache()
@@ -286,8 +298,56 @@ def run_streams(args, rank, world, counts=(1, 2, 4, 8), steps=10, warmup=3):
             r_["vs_one_request"] = round(r_["chunks_per_s"] / base1, 3)
         out[name] = {"chunk_tokens": NC, "desc": shp["desc"], "rows": rows}
     return {"workload": "batched requests, Wan2.1-1.3B attention layer (publish + attention per round)",
-            "unit": "chunks/s", "steady_rounds_timed": steps, "shapes": out,
-            "gpu_launches_per_round": 2}
+            "unit": "chunks/s", "shapes": out, "gpu_launches_per_round": 2}
+
+
+def measure_peaks(n=8192, seconds=4.0):
+    """The dense GEMM peaks of this GPU for the 8-bit rooflines, measured as
+    the bf16 denominator is: a library GEMM (cuBLASLt through torch) at
+    n^3, the best of 10 launches (burst) and back-to-back launches for
+    ``seconds`` (sustained), for e4m3 (torch._scaled_mm, unit scales, bf16
+    out) and bf16.  A denominator measurement, not a workload of this
+    library."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    one = torch.ones((), device=dev)
+    a8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+    b8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+    ab = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    bb = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    fns = {"e4m3": lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one,
+                                            out_dtype=torch.bfloat16),
+           "bf16": lambda: ab @ bb}
+    res = {}
+    for name, fn in fns.items():
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        with ClockSampler(dev.index) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0, count = time.time(), 0
+            e0.record()
+            while time.time() - t0 < seconds:
+                for _ in range(20):
+                    fn()
+                count += 20
+                torch.cuda.synchronize()
+            e1.record()
+            torch.cuda.synchronize()
+        res[name] = {"burst_tflops": round(2 * n ** 3 / (best * 1e-3) / 1e12, 1),
+                     "sustained_tflops": round(2 * n ** 3 * count / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
+                     "clocks_sustained": clk.summary()}
+    return {"workload": f"library dense GEMM {n}^3 (cuBLASLt through torch)", "peaks": res}
 
 
 def max_over_ranks(values, world, device="cpu"):
@@ -943,7 +1003,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="wan13_attn",
                     choices=sorted(CONFIGS) + sorted(DIT_CONFIGS) + sorted(QKV_ATTN_CONFIGS)
-                    + ["streams"])
+                    + ["streams", "peaks"])
     ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
@@ -964,6 +1024,10 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    if args.config == "peaks":
+        if rank == 0:
+            print(json.dumps(measure_peaks()), flush=True)
+        return
     if args.config == "streams":
         d = run_streams(args, rank, world, steps=args.steps, warmup=args.warmup)
         if rank == 0:
@@ -984,12 +1048,12 @@ def main():
         # the other workloads of the measurement plan, each with its clocks and
         # roofline: the 1.3B DiT (bf16 and 8-bit), the 5-step long rollout and
         # the 14B-scale QKV + attention stack
+        res["streams"] = run_streams(args, rank, world)
         res["dit"] = run_dit(args, "dit13", rank, world, steps=args.dit_steps, warmup=3)
         res["dit_w8a8"] = run_dit(args, "dit13_w8a8", rank, world, steps=args.dit_steps, warmup=3)
         res["dit_s5"] = run_dit(args, "dit13_s5", rank, world, steps=args.dit_steps, warmup=3)
         res["qkv_attn14b"] = run_qkv_attn(args, "qkv_attn14b", rank, world,
                                           steps=max(5, args.dit_steps // 2), warmup=3)
-        res["streams"] = run_streams(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()

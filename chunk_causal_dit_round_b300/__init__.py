@@ -202,6 +202,7 @@ class Round:
             o.rope_split[0], o.rope_split[1], o.rope_split[2] = rope_split
         self.S, self.NC, self.H, self.D = S, chunk_tokens, heads, head_dim
         self.dtype = dtype
+        self.n_chunks, self.schedule = n_chunks, schedule
         h = ctypes.c_void_p()
         check(lib.wf_plan(S, chunk_tokens, heads, head_dim, history, ctypes.byref(o),
                           ctypes.byref(h)), "wf_plan")
@@ -249,6 +250,12 @@ class Round:
         check(rc, "wf_round_step")
         self.info = info
         return info
+
+    def n_left(self):
+        """Rounds this request still has after the current one."""
+        total = self.n_chunks * (self.S + 1) if self.schedule == WF_SCHED_SEQUENTIAL \
+            else self.n_chunks + self.S
+        return total - 1 - (self.info.k if self.info is not None else -1)
 
     def page_table(self):
         cap = 4096

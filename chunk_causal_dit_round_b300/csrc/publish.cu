@@ -253,8 +253,11 @@ __global__ void __launch_bounds__(256) publish_fp8_kernel(const WfGeom g, const 
 // handles any dim % 8 == 0 by reading the row twice (the second read hits
 // the caches).
 
+// Three 256-thread blocks per SM: the kernel is latency-bound at two (one
+// warp's loads are in flight only until it starts computing), and the
+// register cap this sets (85) costs at most a few bytes of spill.
 template <int NV, bool F8>
-__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const WfGeom g, const WfRoundDev rd,
+__global__ void __launch_bounds__(256, 3) qk_norm_rope_kernel(const WfGeom g, const WfRoundDev rd,
                                                            const WfQkNormArgs a) {
     const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;

@@ -413,17 +413,26 @@ def test_qkv_publish_sampled_rows(width):
 
 # ---- 8-bit attention inside the DiT round ------------------------------------------
 
-FP8_REL, FP8_MEAN = 4e-2, 1.5e-2     # the e4m3 bars of tests/test_gpu_fp8.py
+# 8-bit bars (tests/derive_fp8_bars.py).  Benchmark weights (std 0.02): the
+# emulated e4m3 rounding of P moves the predictions by max <= 0.0064, so max
+# 0.05 (a mask mistake at this flat attention moves them by only ~0.025:
+# the sharp variant below is the one that separates mistakes).  Sharp
+# weights (std 0.05): rounding spread max 0.094 / mean 0.011 / rel 0.017
+# (e4m3 linears and attention), planted mask mistake 0.46 / 0.071 / 0.117.
+FP8_REL, FP8_MEAN, FP8_MAX = 4e-2, 1.5e-2, 5e-2
+FP8_SHARP = (0.15, 0.02, 0.035)
 
 
-def test_dit_request_fp8_attention():
+@pytest.mark.parametrize("std", [0.02, 0.05], ids=["bench-init", "sharp"])
+def test_dit_request_fp8_attention(std):
     """A WF_FP8 plan runs the same DiT round with e4m3 Q/K/V pages (written by
     the QKV epilogue) and e4m3 attention; checked against the oracle with
     the same e4m3 storage."""
     cfg = sch.Cfg(4, 6, 3)
-    mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=0.02, seed=13,
+    mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=std, seed=13,
                                 steps=[1000.0, 750.0, 500.0, 250.0], fp8=(4.0, 4.0))
-    assert np.isfinite(mx) and mean <= FP8_MEAN and rel <= FP8_REL, (mx, mean, rel)
+    bars = (FP8_MAX, FP8_MEAN, FP8_REL) if std == 0.02 else FP8_SHARP
+    assert mx <= bars[0] and mean <= bars[1] and rel <= bars[2], (mx, mean, rel)
 
 
 def test_qkv_projection_publish_fp8():
@@ -470,12 +479,14 @@ def test_qkv_projection_publish_fp8():
 
 
 
+@pytest.mark.parametrize("std", [0.02, 0.05], ids=["bench-init", "sharp"])
 @pytest.mark.parametrize("fp8", [None, (4.0, 4.0)], ids=["bf16-attention", "e4m3-attention"])
-def test_dit_request_e4m3_linears(fp8):
+def test_dit_request_e4m3_linears(fp8, std):
     """The block's linear layers in e4m3 (per-channel weight scales, e4m3 LN
     output, attention output and FFN hidden layer), with bf16 or e4m3
     attention, against the oracle with the same e4m3 rounding points."""
     cfg = sch.Cfg(4, 6, 3)
-    mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=0.02, seed=15,
+    mx, mean, rel = run_request(cfg, GRID, DIMS.heads, DIMS, std=std, seed=15,
                                 steps=[1000.0, 750.0, 500.0, 250.0], fp8=fp8, linear_fp8=True)
-    assert np.isfinite(mx) and mean <= FP8_MEAN and rel <= FP8_REL, (mx, mean, rel)
+    bars = (FP8_MAX, FP8_MEAN, FP8_REL) if std == 0.02 else FP8_SHARP
+    assert mx <= bars[0] and mean <= bars[1] and rel <= bars[2], (mx, mean, rel)

@@ -13,9 +13,13 @@ oracle with the same e4m3 storage (oracle.round.Fp8).
   nearest: up to 2^-4 relative, about 3.6% RMS per element, unbiased), which
   averages over the keys a row attends to.  Sharp inputs (few dominant keys
   per row) measured relative L2 2.4% and mean |O - O_ref| / max(1, |O_ref|)
-  0.0076; bars: relative L2 <= 4e-2, mean <= 1.5e-2.  The benchmark's
-  near-uniform rows keep the bf16 bars.  Masks and pages are checked exactly
-  by the fingerprint, so the looser bars hide no bookkeeping error."""
+  0.0076; bars: relative L2 <= 4e-2, mean <= 1.5e-2, max 0.25.  The
+  max bar comes from tests/derive_fp8_bars.py: the oracle with that e4m3
+  rounding of P emulated differs from the plain oracle by max 0.053-0.074
+  on these requests, and a planted mask mistake (reverse edges) by max
+  3.7-4.9.  The benchmark's near-uniform rows keep the bf16 bars.  Masks
+  and pages are checked exactly by the fingerprint, so the looser bars hide
+  no bookkeeping error."""
 
 import numpy as np
 import pytest
@@ -30,7 +34,7 @@ from oracle.round import Fp8, Geom, e4m3, round_attention
 pytestmark = pytest.mark.gpu
 
 SMALL = Geom(grid_t=3, grid_h=10, grid_w=10, heads=2, head_dim=128)   # 300 tokens: 2 tiles + 44
-REL, MEAN = 4e-2, 1.5e-2
+REL, MEAN, MAX = 4e-2, 1.5e-2, 0.25
 
 
 def test_fp8_publish_placement():
@@ -117,7 +121,7 @@ def _request(cfg, geom, seed, qk_raw_scale, v_raw_scale, scales, err):
                                  sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE)], ids=str)
 def test_fp8_request_sharp_inputs(cfg):
     mx, mean, rel = _request(cfg, SMALL, 7, 2.0, 1.0, (4.0, 4.0), scaled_errors)
-    assert np.isfinite(mx) and mean <= MEAN and rel <= REL, (mx, mean, rel)
+    assert mx <= MAX and mean <= MEAN and rel <= REL, (mx, mean, rel)
 
 
 def test_fp8_request_bench_distribution():
@@ -129,7 +133,10 @@ def test_fp8_request_bench_distribution():
 def test_fp8_wan_shape_sampled_rows():
     """8-bit attention at the Wan2.1-1.3B shape (S = 4, 4680-token chunks,
     12 x 128, W = 3) in a steady round with anchor re-rotation, against the
-    oracle with the same e4m3 storage on sampled query rows of 3 heads."""
+    oracle with the same e4m3 storage on sampled query rows of 3 heads.
+    Absolute bars max 3.5e-3, mean 7e-4 (tests/derive_fp8_bars.py: the
+    emulated e4m3 rounding of P moves these rows by max 7e-4, mean 1.5e-4;
+    a planted mask mistake by max 0.0118, mean 0.0028)."""
     cfg = sch.Cfg(4, 14, 3)
     geom = Geom(3, 30, 52, 12, 128)
     heads = [0, 5, 11]
@@ -151,5 +158,5 @@ def test_fp8_wan_shape_sampled_rows():
     for t, o in zip(sch.round_tasks(cfg, k_check), ref):
         g = out[t.stage][rows][:, heads].float().cpu().numpy()
         mx, mean, rel = errors(g, o)
-        assert mean <= MEAN and rel <= REL, (t.stage, mx, mean, rel)
+        assert mx <= 3.5e-3 and mean <= 7e-4 and rel <= REL, (t.stage, mx, mean, rel)
     r.close()
