@@ -634,12 +634,15 @@ def run_ours(args, rank, world):
         del x
     out = r.new_out()
 
+    kernel = {"auto": wf.WF_ATTN_AUTO, "tc": wf.WF_ATTN_TC, "tc_split": wf.WF_ATTN_TC_SPLIT,
+              "simt": wf.WF_ATTN_SIMT}[getattr(args, "attn_kernel", "auto")]
+
     def step(i, qkv=None):
         info = r.step()
         if info is None:
             raise RuntimeError("request exhausted")
         r.publish(0, qkv if qkv is not None else qkvs[i % n_in], stream)
-        r.attention(0, out, wf.WF_ATTN_AUTO, stream)
+        r.attention(0, out, kernel, stream)
         return info
 
     # fill the pipeline (untimed): rounds 0 .. k_steady-1
@@ -666,7 +669,7 @@ def run_ours(args, rank, world):
             ev_pub[i].record(stream)
             r.publish(0, qkvs[i % n_in], stream)
             ev_attn[i][0].record(stream)
-            r.attention(0, out, wf.WF_ATTN_AUTO, stream)
+            r.attention(0, out, kernel, stream)
             ev_attn[i][1].record(stream)
             flops += info.attn_flops
         t1.record(stream)
@@ -714,7 +717,7 @@ def run_ours(args, rank, world):
             stream.wait_event(d2h_done[b])                # round i-2's output is home
         info = r.step()
         r.publish(0, dev_in[b], stream)
-        r.attention(0, dev_out[b], wf.WF_ATTN_AUTO, stream)
+        r.attention(0, dev_out[b], kernel, stream)
         comp_done[b].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(comp_done[b])
@@ -1008,6 +1011,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "tc", "tc_split", "simt"],
+                    help="attention kernel of the attention-layer workload (default: the library's choice)")
     ap.add_argument("--dit-steps", type=int, default=20,
                     help="steady chunks timed per DiT leg of the default line (14B leg: half)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -66,10 +66,14 @@ def test_fp8_publish_placement():
     r.close()
 
 
+TC_KERNELS = [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT]
+
+
+@pytest.mark.parametrize("kernel", TC_KERNELS)
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(3, 7, 1, mask=sch.MASK_RF),
                                  sch.Cfg(2, 4, 1, sequential=True), sch.Cfg(1, 4, 1), sch.Cfg(3, 1, -1),
                                  sch.Cfg(3, 7, 0), sch.Cfg(2, 6, 0, use_anchor=False)], ids=str)
-def test_fp8_visibility_fingerprint(cfg):
+def test_fp8_visibility_fingerprint(cfg, kernel):
     geom = SMALL
     r = make_round(cfg, geom, wf.WF_FP8, fp8_scales=(2.0, 1.0))
     out = r.new_out()
@@ -83,7 +87,7 @@ def test_fp8_visibility_fingerprint(cfg):
             qkv[s, :, 2, :, c] = 1.0
             qkv[s, :, 2, :, 64 + s] = 1.0
         r.publish(0, qkv)
-        r.attention(0, out, wf.WF_ATTN_TC)
+        r.attention(0, out, kernel)
         torch.cuda.synchronize()
         for t in sch.round_tasks(cfg, k):
             want = np.zeros(geom.head_dim)
@@ -97,7 +101,7 @@ def test_fp8_visibility_fingerprint(cfg):
     r.close()
 
 
-def _request(cfg, geom, seed, qk_raw_scale, v_raw_scale, scales, err):
+def _request(cfg, geom, seed, qk_raw_scale, v_raw_scale, scales, err, kernel=wf.WF_ATTN_TC):
     r = make_round(cfg, geom, wf.WF_FP8, fp8_scales=scales)
     raw, traw = raw_fn(seed, geom, torch.bfloat16, qk_raw_scale, v_raw_scale)
     out = r.new_out()
@@ -106,7 +110,7 @@ def _request(cfg, geom, seed, qk_raw_scale, v_raw_scale, scales, err):
         info = r.step()
         r.publish(0, fill_qkv(r, info, traw, 0))
         out.zero_()
-        r.attention(0, out, wf.WF_ATTN_TC)
+        r.attention(0, out, kernel)
         torch.cuda.synchronize()
         ref = round_attention(cfg, geom, k, 0, raw, qk_dtype=Fp8(*scales))
         for t, o in zip(sch.round_tasks(cfg, k), ref):
@@ -117,20 +121,23 @@ def _request(cfg, geom, seed, qk_raw_scale, v_raw_scale, scales, err):
     return worst
 
 
+@pytest.mark.parametrize("kernel", TC_KERNELS)
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(2, 6, -1),
                                  sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE)], ids=str)
-def test_fp8_request_sharp_inputs(cfg):
-    mx, mean, rel = _request(cfg, SMALL, 7, 2.0, 1.0, (4.0, 4.0), scaled_errors)
+def test_fp8_request_sharp_inputs(cfg, kernel):
+    mx, mean, rel = _request(cfg, SMALL, 7, 2.0, 1.0, (4.0, 4.0), scaled_errors, kernel)
     assert mx <= MAX and mean <= MEAN and rel <= REL, (mx, mean, rel)
 
 
-def test_fp8_request_bench_distribution():
+@pytest.mark.parametrize("kernel", TC_KERNELS)
+def test_fp8_request_bench_distribution(kernel):
     s = 1.0 / np.sqrt(128)
-    mx, mean, rel = _request(sch.Cfg(4, 9, 3), SMALL, 3, s, s, (8.0, 8.0), errors)
+    mx, mean, rel = _request(sch.Cfg(4, 9, 3), SMALL, 3, s, s, (8.0, 8.0), errors, kernel)
     assert mx <= 2e-2 and mean <= 2e-3 and rel <= REL, (mx, mean, rel)
 
 
-def test_fp8_wan_shape_sampled_rows():
+@pytest.mark.parametrize("kernel", TC_KERNELS)
+def test_fp8_wan_shape_sampled_rows(kernel):
     """8-bit attention at the Wan2.1-1.3B shape (S = 4, 4680-token chunks,
     12 x 128, W = 3) in a steady round with anchor re-rotation, against the
     oracle with the same e4m3 storage on sampled query rows of 3 heads.
@@ -149,7 +156,7 @@ def test_fp8_wan_shape_sampled_rows():
     for k in range(k_check + 1):
         info = r.step()
         r.publish(0, fill_qkv(r, info, traw, 0))
-    r.attention(0, out, wf.WF_ATTN_TC)
+    r.attention(0, out, kernel)
     torch.cuda.synchronize()
     assert r.sync_status() == wf.WF_OK
     rows = [0, 1, 127, 128, 2000, 4607, 4608, 4650, 4679]

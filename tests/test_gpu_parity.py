@@ -57,7 +57,7 @@ def _run_request(cfg, geom, dtype, kernel, seed, qk_scale=1.0, v_scale=1.0, roun
 SMALL = Geom(grid_t=3, grid_h=10, grid_w=10, heads=2, head_dim=128)   # 300 tokens: 2 tiles + 44
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3), sch.Cfg(2, 6, -1),
                                  sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE),
                                  sch.Cfg(2, 5, 2, use_anchor=False),
@@ -69,7 +69,7 @@ def test_bf16_request_all_rounds(cfg, kernel):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
 def test_bf16_bench_distribution(kernel):
     # the benchmark's distribution: Q/K/V ~ N(0,1)/sqrt(128)
     cfg = sch.Cfg(4, 9, 3)
@@ -99,9 +99,10 @@ STORE_EXTRA = [sch.Cfg(4, 10, 2, store_extra=4), sch.Cfg(2, 7, 0, store_extra=2)
                sch.Cfg(3, 8, 1, mask=sch.MASK_RF, store_extra=2)]
 
 
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
 @pytest.mark.parametrize("cfg", DEGENERATE + STORE_EXTRA, ids=str)
-def test_bf16_degenerate_requests(cfg):
-    mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, wf.WF_ATTN_TC, seed=17, qk_scale=2.0,
+def test_bf16_degenerate_requests(cfg, kernel):
+    mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, kernel, seed=17, qk_scale=2.0,
                                  err=scaled_errors)
     assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
@@ -118,7 +119,7 @@ def test_bf16_request_custom_rope_split():
 
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3)] + DEGENERATE + STORE_EXTRA,
                          ids=str)
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
 def test_visibility_fingerprint(kernel, cfg):
     """Q = 0 makes softmax uniform over the visible keys; V one-hot in the
     producing (chunk, stage) gives O = share of each visible chunk, exactly
@@ -183,17 +184,18 @@ def test_publish_placement_and_rope():
             assert np.all(np.abs(ag - aref) <= 2 ** -8 * np.abs(aref) + 1e-6), k
 
 
-def test_tc_deterministic_and_matches_simt():
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+def test_tc_deterministic_and_matches_simt(kernel):
     cfg = sch.Cfg(4, 12, 3)
-    geom = Geom(3, 16, 20, 3, 128)   # 960 tokens: 7.5 tiles
+    geom = Geom(3, 16, 20, 3, 128)   # 960 tokens: 7.5 tiles of 128, 12 of 80
     r = make_round(cfg, geom, wf.WF_BF16)
     _, traw = raw_fn(11, geom, torch.bfloat16, qk_scale=2.0)
     a, b, c = r.new_out(), r.new_out(), r.new_out()
     for k in range(sch.n_rounds(cfg)):
         info = r.step()
         r.publish(0, fill_qkv(r, info, traw, 0))
-        r.attention(0, a, wf.WF_ATTN_TC)
-        r.attention(0, b, wf.WF_ATTN_TC)
+        r.attention(0, a, kernel)
+        r.attention(0, b, kernel)
         r.attention(0, c, wf.WF_ATTN_SIMT)
         torch.cuda.synchronize()
         assert torch.equal(a, b)
@@ -202,7 +204,7 @@ def test_tc_deterministic_and_matches_simt():
     assert r.sync_status() == wf.WF_OK
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3), sch.Cfg(3, 7, 1, mask=sch.MASK_RF)],
                          ids=str)
 def test_batched_launch_equals_per_task_replay(cfg, kernel):
@@ -250,10 +252,12 @@ def test_task_subset_rejects_bad_masks():
     assert r.sync_status() == wf.WF_OK
 
 
-def test_wan_shape_sampled_rows():
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+def test_wan_shape_sampled_rows(kernel):
     """Wan2.1-1.3B attention layer (S=4, 4680-token chunks, 12 x 128, W=3) in
-    a steady round with anchor re-rotation, TC kernel, against the oracle on
-    sampled query rows (first, last and the ragged tail tile) of 3 heads."""
+    a steady round with anchor re-rotation, tensor-core kernels, against the
+    oracle on sampled query rows (first, last and the ragged tail tile) of 3
+    heads."""
     cfg = sch.Cfg(4, 14, 3)
     geom = Geom(3, 30, 52, 12, 128)
     heads = [0, 5, 11]
@@ -265,7 +269,7 @@ def test_wan_shape_sampled_rows():
     for k in range(k_check + 1):
         info = r.step()
         r.publish(0, fill_qkv(r, info, traw, 0))
-    r.attention(0, out, wf.WF_ATTN_TC)
+    r.attention(0, out, kernel)
     torch.cuda.synchronize()
     assert r.sync_status() == wf.WF_OK
     rows = [0, 1, 127, 128, 2000, 4607, 4608, 4650, 4679]
@@ -277,7 +281,7 @@ def test_wan_shape_sampled_rows():
         assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (t.stage, mx, mean, rel)
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
 def test_bf16_extreme_scores(kernel):
     """Scores spread over thousands (Q, K ~ N(0, 8^2)): most exp2 arguments
     fall far below -126 and the softmax rows are near one-hot.  No output may
@@ -291,10 +295,12 @@ def test_bf16_extreme_scores(kernel):
     assert np.isfinite(mx) and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
-def test_14b_shape_sampled_rows():
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+def test_14b_shape_sampled_rows(kernel):
     """14B-scale attention layer (40 heads x 128, S = 4, 4680-token chunks,
-    W = 3) in a steady round with anchor re-rotation, TC kernel, against the
-    oracle on sampled query rows of 3 heads (first, middle, last)."""
+    W = 3) in a steady round with anchor re-rotation, tensor-core kernels,
+    against the oracle on sampled query rows of 3 heads (first, middle,
+    last)."""
     cfg = sch.Cfg(4, 12, 3)
     geom = Geom(3, 30, 52, 40, 128)
     heads = [0, 19, 39]
@@ -306,7 +312,7 @@ def test_14b_shape_sampled_rows():
     for k in range(k_check + 1):
         info = r.step()
         r.publish(0, fill_qkv(r, info, traw, 0))
-    r.attention(0, out, wf.WF_ATTN_TC)
+    r.attention(0, out, kernel)
     torch.cuda.synchronize()
     assert r.sync_status() == wf.WF_OK
     rows = [0, 127, 128, 2345, 4607, 4608, 4679]
