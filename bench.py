@@ -634,7 +634,7 @@ def run_ours(args, rank, world):
         del x
     out = r.new_out()
 
-    kernel = {"auto": wf.WF_ATTN_AUTO, "tc": wf.WF_ATTN_TC, "tc_split": wf.WF_ATTN_TC_SPLIT,
+    kernel = {"auto": wf.WF_ATTN_AUTO, "tc": wf.WF_ATTN_TC,
               "simt": wf.WF_ATTN_SIMT}[getattr(args, "attn_kernel", "auto")]
 
     def step(i, qkv=None):
@@ -1011,7 +1011,7 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "tc", "tc_split", "simt"],
+    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "tc", "simt"],
                     help="attention kernel of the attention-layer workload (default: the library's choice)")
     ap.add_argument("--dit-steps", type=int, default=20,
                     help="steady chunks timed per DiT leg of the default line (14B leg: half)")

@@ -43,7 +43,6 @@ WF_MAX_GROUP_PLANS = 8
 WF_ATTN_AUTO = 0
 WF_ATTN_TC = 1
 WF_ATTN_SIMT = 2
-WF_ATTN_TC_SPLIT = 3
 WF_EPI_BF16 = 0
 WF_EPI_F32 = 1
 WF_EPI_GELU_BF16 = 2

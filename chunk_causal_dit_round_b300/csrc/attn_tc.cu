@@ -615,11 +615,6 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const cuuint32_t box2[3] = {f8 ? 128u : 64u, (cuuint32_t)wf_attn_tc2_keys(g.dtype), 1};
-    if (encode(&out->kv2, ty, 3, pool, dk, strides, box2, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
     return cudaSuccess;
 }
 

@@ -208,7 +208,7 @@ int wf_group_attention(wf_group_t gr, unsigned int plan_mask, int layer, void *o
     wf_plan_s *p0 = gr->plans[0];
     if (layer < 0 || layer >= p0->o.layers) return WF_ERANGE;
     if (!out || !aligned16(out)) return WF_EINVAL;
-    if (kernel < WF_ATTN_AUTO || kernel > WF_ATTN_TC_SPLIT) return WF_EINVAL;
+    if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
     for (int r = 0; r < gr->n; ++r) {
         if (!((plan_mask >> r) & 1u)) continue;
         const wf_plan_s *p = gr->plans[r];
@@ -226,9 +226,6 @@ int wf_group_attention(wf_group_t gr, unsigned int plan_mask, int layer, void *o
     if (kernel == WF_ATTN_TC) {
         if (!tc_ok) return WF_EUNSUPPORTED;
         e = wf_launch_attn_tc(p0->g, rd, layer, gr->tmaps, out, p0->scratch, p0->num_sms, stream);
-    } else if (kernel == WF_ATTN_TC_SPLIT) {
-        if (!tc_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_tc2(p0->g, rd, layer, gr->tmaps, out, p0->scratch, p0->num_sms, stream);
     } else {
         if (!simt_ok) return WF_EUNSUPPORTED;
         e = wf_launch_attn_simt(p0->g, rd, layer, p0->o.dtype, p0->qbuf, p0->pool, out, stream);

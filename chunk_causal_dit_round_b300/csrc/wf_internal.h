@@ -99,7 +99,6 @@ cudaError_t wf_launch_attn_simt(const WfGeom &g, const WfRoundDev &rd, int layer
 struct WfTmaps {
     CUtensorMap q;     // qbuf  [S+1][H][NC][128] bf16, box 64 x 128 x 1, 128B swizzle
     CUtensorMap kv;    // pool  [P*L*2*H][NC][128] bf16, same box
-    CUtensorMap kv2;   // pool, box 64 x wf_attn_tc2_keys x 1 (the split-P kernel's key tiles)
 };
 
 bool wf_attn_tc_supported(const WfGeom &g, int dtype);
@@ -109,13 +108,6 @@ cudaError_t wf_encode_tmaps(const WfGeom &g, void *qbuf, void *pool, WfTmaps *ou
 cudaError_t wf_launch_attn_tc(const WfGeom &g, const WfRoundDev &rd, int layer,
                               const WfTmaps &maps, void *out, void *scratch, int num_sms,
                               cudaStream_t stream, int out_e4m3 = 0);
-
-// The tensor-core kernel with S and P apart in tensor memory (attn_tc2.cu):
-// key tiles of wf_attn_tc2_keys(dtype) keys (80 bf16, 96 e4m3).
-int wf_attn_tc2_keys(int dtype);
-cudaError_t wf_launch_attn_tc2(const WfGeom &g, const WfRoundDev &rd, int layer, const WfTmaps &maps,
-                               void *out, void *scratch, int num_sms, cudaStream_t stream,
-                               int out_e4m3 = 0);
 
 // Variant of wf_launch_attn_tc whose scheduler counters live in a static
 // device block inside the library; status_scratch receives the status and

@@ -187,10 +187,6 @@ int wf_attention_impl(wf_plan_s *p, int layer, void *out, int kernel, cudaStream
         if (!tc_ok) return WF_EUNSUPPORTED;
         e = wf_launch_attn_tc(p->g, rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream,
                               out_e4m3);
-    } else if (kernel == WF_ATTN_TC_SPLIT) {
-        if (!tc_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_tc2(p->g, rd, layer, p->tmaps, out, p->scratch, p->num_sms, stream,
-                               out_e4m3);
     } else {
         if (!simt_ok) return WF_EUNSUPPORTED;
         e = wf_launch_attn_simt(p->g, rd, layer, p->o.dtype, p->qbuf, p->pool, out, stream);
@@ -577,7 +573,7 @@ int wf_round_attention(wf_plan_t p, int layer, void *out, int kernel, cudaStream
     if (p->k < 0) return WF_ENOROUND;
     if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
     if (!out || ((uintptr_t)out & 15)) return WF_EINVAL;
-    if (kernel < WF_ATTN_AUTO || kernel > WF_ATTN_TC_SPLIT) return WF_EINVAL;
+    if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
     if (p->published[layer] != p->k) return WF_EORDER;
     return wf_attention_impl(p, layer, out, kernel, stream);
 }
@@ -589,7 +585,7 @@ int wf_round_attention_tasks(wf_plan_t p, int layer, void *out, int kernel, unsi
     if (p->k < 0) return WF_ENOROUND;
     if (layer < 0 || layer >= p->o.layers) return WF_ERANGE;
     if (!out || ((uintptr_t)out & 15)) return WF_EINVAL;
-    if (kernel < WF_ATTN_AUTO || kernel > WF_ATTN_TC_SPLIT) return WF_EINVAL;
+    if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
     if (slot_mask >> (p->S + 1)) return WF_EINVAL;
     if (p->published[layer] != p->k) return WF_EORDER;
     return wf_attention_impl(p, layer, out, kernel, stream, 0, slot_mask);

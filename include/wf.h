@@ -90,10 +90,6 @@ typedef struct CUstream_st *cudaStream_t; /* identical to CUDA's own typedef */
 #define WF_ATTN_AUTO 0    /* tensor-core kernel when supported, else the SIMT kernel */
 #define WF_ATTN_TC   1    /* tcgen05/TMEM/TMA kernel (bf16, head_dim 128) */
 #define WF_ATTN_SIMT 2    /* CUDA-core kernel (fp32 or bf16, head_dim 32..128, %32) */
-#define WF_ATTN_TC_SPLIT 3 /* tcgen05 kernel with the probabilities P kept apart from the scores
-                              in tensor memory (80-key bf16 / 96-key e4m3 tiles): the next
-                              Q K^T is issued as soon as the softmax has read S (bf16 or e4m3,
-                              head_dim 128) */
 
 #define WF_EPI_BF16           0 /* out bf16 = acc + bias */
 #define WF_EPI_F32            1 /* out f32  = acc + bias */

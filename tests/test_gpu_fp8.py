@@ -66,7 +66,7 @@ def test_fp8_publish_placement():
     r.close()
 
 
-TC_KERNELS = [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT]
+TC_KERNELS = [wf.WF_ATTN_TC]
 
 
 @pytest.mark.parametrize("kernel", TC_KERNELS)

@@ -61,7 +61,7 @@ def drive(grp, cfg, starts, on_round):
     assert all(k == sch.n_rounds(cfg) - 1 for k in ks)
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 @pytest.mark.parametrize("starts", [(0, 3), (0, 2, 5)], ids=["two", "three"])
 def test_group_requests_match_oracle(starts, kernel):
     cfg = sch.Cfg(4, 8, 2)

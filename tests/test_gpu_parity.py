@@ -57,7 +57,7 @@ def _run_request(cfg, geom, dtype, kernel, seed, qk_scale=1.0, v_scale=1.0, roun
 SMALL = Geom(grid_t=3, grid_h=10, grid_w=10, heads=2, head_dim=128)   # 300 tokens: 2 tiles + 44
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3), sch.Cfg(2, 6, -1),
                                  sch.Cfg(3, 7, 1, anchor_mode=sch.ANCHOR_ABSOLUTE),
                                  sch.Cfg(2, 5, 2, use_anchor=False),
@@ -69,7 +69,7 @@ def test_bf16_request_all_rounds(cfg, kernel):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 def test_bf16_bench_distribution(kernel):
     # the benchmark's distribution: Q/K/V ~ N(0,1)/sqrt(128)
     cfg = sch.Cfg(4, 9, 3)
@@ -99,7 +99,7 @@ STORE_EXTRA = [sch.Cfg(4, 10, 2, store_extra=4), sch.Cfg(2, 7, 0, store_extra=2)
                sch.Cfg(3, 8, 1, mask=sch.MASK_RF, store_extra=2)]
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC])
 @pytest.mark.parametrize("cfg", DEGENERATE + STORE_EXTRA, ids=str)
 def test_bf16_degenerate_requests(cfg, kernel):
     mx, mean, rel = _run_request(cfg, SMALL, wf.WF_BF16, kernel, seed=17, qk_scale=2.0,
@@ -119,7 +119,7 @@ def test_bf16_request_custom_rope_split():
 
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3)] + DEGENERATE + STORE_EXTRA,
                          ids=str)
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 def test_visibility_fingerprint(kernel, cfg):
     """Q = 0 makes softmax uniform over the visible keys; V one-hot in the
     producing (chunk, stage) gives O = share of each visible chunk, exactly
@@ -184,7 +184,7 @@ def test_publish_placement_and_rope():
             assert np.all(np.abs(ag - aref) <= 2 ** -8 * np.abs(aref) + 1e-6), k
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC])
 def test_tc_deterministic_and_matches_simt(kernel):
     cfg = sch.Cfg(4, 12, 3)
     geom = Geom(3, 16, 20, 3, 128)   # 960 tokens: 7.5 tiles of 128, 12 of 80
@@ -204,7 +204,7 @@ def test_tc_deterministic_and_matches_simt(kernel):
     assert r.sync_status() == wf.WF_OK
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 @pytest.mark.parametrize("cfg", [sch.Cfg(4, 10, 3), sch.Cfg(5, 12, 3), sch.Cfg(3, 7, 1, mask=sch.MASK_RF)],
                          ids=str)
 def test_batched_launch_equals_per_task_replay(cfg, kernel):
@@ -252,7 +252,7 @@ def test_task_subset_rejects_bad_masks():
     assert r.sync_status() == wf.WF_OK
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC])
 def test_wan_shape_sampled_rows(kernel):
     """Wan2.1-1.3B attention layer (S=4, 4680-token chunks, 12 x 128, W=3) in
     a steady round with anchor re-rotation, tensor-core kernels, against the
@@ -281,7 +281,7 @@ def test_wan_shape_sampled_rows(kernel):
         assert mx <= BF16_MAX and mean <= BF16_MEAN and rel <= BF16_REL, (t.stage, mx, mean, rel)
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_SIMT])
 def test_bf16_extreme_scores(kernel):
     """Scores spread over thousands (Q, K ~ N(0, 8^2)): most exp2 arguments
     fall far below -126 and the softmax rows are near one-hot.  No output may
@@ -295,7 +295,7 @@ def test_bf16_extreme_scores(kernel):
     assert np.isfinite(mx) and mean <= BF16_MEAN and rel <= BF16_REL, (mx, mean, rel)
 
 
-@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC, wf.WF_ATTN_TC_SPLIT])
+@pytest.mark.parametrize("kernel", [wf.WF_ATTN_TC])
 def test_14b_shape_sampled_rows(kernel):
     """14B-scale attention layer (40 heads x 128, S = 4, 4680-token chunks,
     W = 3) in a steady round with anchor re-rotation, tensor-core kernels,
