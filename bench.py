@@ -684,35 +684,64 @@ def run_ours(args, rank, world):
 
     # ---- timed: end to end through the C ABI with host buffers ------------
     # Every round's Q/K/V go up from pinned host memory and its output comes
-    # back.  Two device buffers each way and two copy streams: round i+1's
-    # upload and round i-1's readback overlap round i's kernels.
+    # back.  Two device buffers each way; each upload is split over two copy
+    # streams (one copy engine alone does not fill the host link) and a third
+    # stream reads the outputs back: round i+1's upload and round i-1's
+    # readback overlap round i's kernels.
     host_in = torch.empty_like(qkvs[0], device="cpu").pin_memory()
     host_in.copy_(qkvs[0].cpu())
     host_out = [torch.empty(out.shape, dtype=out.dtype, device="cpu").pin_memory() for _ in range(2)]
     dev_in = [torch.empty_like(qkvs[0]) for _ in range(2)]
     dev_out = [r.new_out() for _ in range(2)]
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ups, down = [torch.cuda.Stream(), torch.cuda.Stream()], torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    h2d_done = [[ev(), ev()], [ev(), ev()]]        # [buffer][copy stream]
+    comp_done, d2h_done = [ev(), ev()], [ev(), ev()]
+    flat_in = host_in.view(-1)
+    half = flat_in.numel() // 2
+
+    def upload(nb):
+        for u, (lo, hi) in enumerate(((0, half), (half, flat_in.numel()))):
+            with torch.cuda.stream(ups[u]):
+                dev_in[nb].view(-1)[lo:hi].copy_(flat_in[lo:hi], non_blocking=True)
+                h2d_done[nb][u].record(ups[u])
+
+    # the host link's rate for one copy of this size, one and two streams
+    link = {}
+    for n_str in (1, 2):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        l0.record(stream)
+        for u in range(n_str):
+            ups[u].wait_stream(stream)
+        if n_str == 1:
+            with torch.cuda.stream(ups[0]):
+                dev_in[0].copy_(host_in, non_blocking=True)
+        else:
+            upload(0)
+        for u in range(n_str):
+            stream.wait_stream(ups[u])
+        l1.record(stream)
+        torch.cuda.synchronize()
+        link[n_str] = host_in.numel() * host_in.element_size() / (l0.elapsed_time(l1) * 1e-3) / 1e9
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_flops = 0.0
     torch.cuda.synchronize()
     e0.record(stream)
-    up.wait_stream(stream)
+    for u in ups:
+        u.wait_stream(stream)
     down.wait_stream(stream)
-    with torch.cuda.stream(up):
-        dev_in[0].copy_(host_in, non_blocking=True)
-        h2d_done[0].record(up)
+    upload(0)
     for i in range(e2e_steps):
         b = i % 2
         if i + 1 < e2e_steps:
             nb = (i + 1) % 2
-            with torch.cuda.stream(up):
-                if i >= 1:
-                    up.wait_event(comp_done[nb])          # round i-1 has read dev_in[nb]
-                dev_in[nb].copy_(host_in, non_blocking=True)
-                h2d_done[nb].record(up)
-        stream.wait_event(h2d_done[b])
+            if i >= 1:
+                for u in ups:
+                    u.wait_event(comp_done[nb])          # round i-1 has read dev_in[nb]
+            upload(nb)
+        for u in range(2):
+            stream.wait_event(h2d_done[b][u])
         if i >= 2:
             stream.wait_event(d2h_done[b])                # round i-2's output is home
         info = r.step()
@@ -768,7 +797,8 @@ def run_ours(args, rank, world):
         "e2e": {"value": round(world * e2e_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
                 "d2h_bytes_per_step": host_out[0].numel() * host_out[0].element_size(),
-                "ms_per_step": round(e2e_ms / max(1, e2e_steps), 4), "steps": e2e_steps},
+                "ms_per_step": round(e2e_ms / max(1, e2e_steps), 4), "steps": e2e_steps,
+                "h2d_link_gbs": {"one_stream": round(link[1], 1), "two_streams": round(link[2], 1)}},
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel",
                      "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
