@@ -59,7 +59,8 @@ SYMBOLS = ["wf_plan_opts_default", "wf_plan", "wf_plan_buffer_sizes", "wf_bind",
            "wf_dit_round", "wf_selftest_timeout", "wf_plan_state_size", "wf_plan_export_state",
            "wf_plan_import_state", "wf_quantize_weight_e4m3", "wf_linear_e4m3",
            "wf_group_create", "wf_group_publish", "wf_group_proj_publish", "wf_group_attention",
-           "wf_group_destroy"]
+           "wf_group_destroy", "wf_group_dit_workspace_size", "wf_group_dit_bind",
+           "wf_group_dit_round"]
 
 
 class wf_plan_opts(ctypes.Structure):
@@ -140,6 +141,9 @@ def _load():
         "wf_group_proj_publish": (I, [P, ctypes.c_uint, I, VP, VP, VP, VP, VP, VP, VP]),
         "wf_group_attention": (I, [P, ctypes.c_uint, I, VP, I, VP]),
         "wf_group_destroy": (None, [P]),
+        "wf_group_dit_workspace_size": (I, [P, I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]),
+        "wf_group_dit_bind": (I, [P, ctypes.POINTER(wf_dit_model), VP, VP]),
+        "wf_group_dit_round": (I, [P, ctypes.c_uint, VP, VP, VP, VP, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -454,20 +458,15 @@ class Group:
             pass
 
 
-class Dit:
-    """A DiT model bound to a Round: device weights (torch bf16 tensors, kept
-    alive here), the workspace, and ``round(z_new, eps, x0_out, chunk_out)``
-    launching wf_dit_round for the round the plan is in."""
+class _DitModel:
+    """The wf_dit_model of a parameter dict (torch bf16 tensors, copied to
+    `dev` and kept alive here)."""
 
-    def __init__(self, rnd: Round, params: dict, *, ffn, channels=16, freq=256, timesteps,
-                 shift=5.0, context_noise=0.0, linear_fp8=False, stream=None):
-        import torch
-        self.r = rnd
-        dev = rnd.pool.device
+    def __init__(self, dev, dim, params: dict, *, ffn, channels, freq, timesteps, shift,
+                 context_noise, linear_fp8):
         self.params = {k: ([t.to(dev).contiguous() for t in v] if isinstance(v, list)
                            else v.to(dev).contiguous()) for k, v in params.items()}
         P = self.params
-        dim = rnd.H * rnd.D
         L = len(P["qkv_w"])
         m = wf_dit_model()
         m.model_dim, m.ffn_dim, m.channels, m.freq_dim = dim, ffn, channels, freq
@@ -487,13 +486,57 @@ class Dit:
         m.layers = self._layers
         m.linear_fp8 = int(linear_fp8)
         self.model = m
+        self.dims = (dim, ffn, channels, freq, int(linear_fp8))
+
+
+class Dit:
+    """A DiT model bound to a Round: device weights (torch bf16 tensors, kept
+    alive here), the workspace, and ``round(z_new, eps, x0_out, chunk_out)``
+    launching wf_dit_round for the round the plan is in."""
+
+    def __init__(self, rnd: Round, params: dict, *, ffn, channels=16, freq=256, timesteps,
+                 shift=5.0, context_noise=0.0, linear_fp8=False, stream=None):
+        import torch
+        self.r = rnd
+        dev = rnd.pool.device
+        md = _DitModel(dev, rnd.H * rnd.D, params, ffn=ffn, channels=channels, freq=freq,
+                       timesteps=timesteps, shift=shift, context_noise=context_noise,
+                       linear_fp8=linear_fp8)
+        self._md, self.params, self.model = md, md.params, md.model
         nbytes = ctypes.c_size_t()
-        check(lib.wf_dit_workspace_size(rnd.plan, dim, ffn, channels, freq, int(linear_fp8),
-                                         ctypes.byref(nbytes)), "wf_dit_workspace_size")
+        check(lib.wf_dit_workspace_size(rnd.plan, *md.dims, ctypes.byref(nbytes)),
+              "wf_dit_workspace_size")
         self.workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
-        check(lib.wf_dit_bind(rnd.plan, ctypes.byref(m), _ptr(self.workspace),
+        check(lib.wf_dit_bind(rnd.plan, ctypes.byref(md.model), _ptr(self.workspace),
                               _stream_handle(stream)), "wf_dit_bind")
 
     def round(self, z_new, eps, x0_out=None, chunk_out=None, stream=None):
         check(lib.wf_dit_round(self.r.plan, _ptr(z_new), _ptr(eps), _ptr(x0_out), _ptr(chunk_out),
                                _stream_handle(stream)), "wf_dit_round")
+
+
+class GroupDit:
+    """A DiT model bound to a Group (wf_group_dit_bind); ``round(mask, z_new,
+    eps, x0_out, chunk_out)`` runs the DiT round of the selected members, each
+    already stepped into its round.  z_new [n][latent], eps [n][S][latent],
+    x0_out [n][S+1][latent], chunk_out [n][latent]."""
+
+    def __init__(self, grp: Group, params: dict, *, ffn, channels=16, freq=256, timesteps,
+                 shift=5.0, context_noise=0.0, linear_fp8=False, stream=None):
+        import torch
+        self.g = grp
+        dev = grp.pool.device
+        md = _DitModel(dev, grp.H * grp.D, params, ffn=ffn, channels=channels, freq=freq,
+                       timesteps=timesteps, shift=shift, context_noise=context_noise,
+                       linear_fp8=linear_fp8)
+        self._md, self.params, self.model = md, md.params, md.model
+        nbytes = ctypes.c_size_t()
+        check(lib.wf_group_dit_workspace_size(grp.group, *md.dims, ctypes.byref(nbytes)),
+              "wf_group_dit_workspace_size")
+        self.workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        check(lib.wf_group_dit_bind(grp.group, ctypes.byref(md.model), _ptr(self.workspace),
+                                    _stream_handle(stream)), "wf_group_dit_bind")
+
+    def round(self, mask, z_new, eps, x0_out=None, chunk_out=None, stream=None):
+        check(lib.wf_group_dit_round(self.g.group, mask, _ptr(z_new), _ptr(eps), _ptr(x0_out),
+                                     _ptr(chunk_out), _stream_handle(stream)), "wf_group_dit_round")

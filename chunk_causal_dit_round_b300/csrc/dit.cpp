@@ -10,6 +10,7 @@
 // layer, and C_{s,l} before P_{s,l+1}.
 
 #include <cmath>
+#include <functional>
 #include <cstring>
 #include <new>
 
@@ -37,6 +38,190 @@ GemmParams base_params(wf_plan_s *p, int row_begin, int row_end, int N, int K, c
 }
 
 }  // namespace
+
+// Binding shared by a plan (n_req = 1) and a group of n_req plans of p's
+// shape: the activations and tables are sized for n_req (S+1) slots, the
+// modulation and head tables written once per request.
+int wf_dit_bind_impl(WfDit *dp, const wf_plan_s *p, const wf_dit_model *m, void *workspace,
+                     int n_req, cudaStream_t stream) {
+    if ((p->o.dtype != WF_BF16 && p->o.dtype != WF_FP8) || p->D != 128) return WF_EUNSUPPORTED;
+    if ((uintptr_t)workspace & 255) return WF_EINVAL;
+    size_t need;
+    int rc = wf_dit_workspace_size(const_cast<wf_plan_s *>(p), m->model_dim, m->ffn_dim, m->channels,
+                                   m->freq_dim, m->linear_fp8, &need);
+    if (rc != WF_OK) return rc;
+    if (!(m->shift > 0.0) || !std::isfinite(m->shift) || !(m->context_noise >= 0.0) ||
+        !(m->context_noise <= 1000.0))
+        return WF_EINVAL;
+    for (int s = 0; s < p->S; ++s)
+        if (!(m->timesteps[s] > 0.0 && m->timesteps[s] <= 1000.0) ||
+            (s > 0 && !(m->timesteps[s] < m->timesteps[s - 1])))
+            return WF_EINVAL;
+    const void *ptrs[] = {m->patch_w, m->t1_w, m->t1_b, m->t2_w, m->t2_b, m->tp_w, m->tp_b,
+                          m->head_w, m->head_mod, m->layers};
+    for (const void *q : ptrs)
+        if (!q) return WF_EINVAL;
+    const int L = p->o.layers;
+    for (int l = 0; l < L; ++l) {
+        const wf_dit_layer &w = m->layers[l];
+        if (!w.qkv_w || !w.o_w || !w.ffn1_w || !w.ffn2_w || !w.modulation || !w.norm_q || !w.norm_k)
+            return WF_EINVAL;
+        const void *all[] = {w.qkv_w, w.qkv_b, w.o_w, w.o_b, w.ffn1_w, w.ffn1_b, w.ffn2_w, w.ffn2_b,
+                             w.norm_q, w.norm_k};
+        for (const void *q : all)
+            if (q && !aligned16(q)) return WF_EINVAL;
+    }
+    WfDit &d = *dp;
+    delete[] d.layers;
+    d.layers = nullptr;
+    d.dim = m->model_dim;
+    d.ffn = m->ffn_dim;
+    d.C = m->channels;
+    d.freq = m->freq_dim;
+    d.L = L;
+    d.linear_fp8 = m->linear_fp8;
+    d.shift = m->shift;
+    d.context_noise = m->context_noise;
+    for (int s = 0; s < p->S; ++s) d.nu[s] = m->timesteps[s];
+    d.nu[p->S] = 0.0;
+    auto B = [](const void *q) { return static_cast<const __nv_bfloat16 *>(q); };
+    d.patch_w = B(m->patch_w); d.patch_b = B(m->patch_b);
+    d.t1_w = B(m->t1_w); d.t1_b = B(m->t1_b);
+    d.t2_w = B(m->t2_w); d.t2_b = B(m->t2_b);
+    d.tp_w = B(m->tp_w); d.tp_b = B(m->tp_b);
+    d.head_w = B(m->head_w); d.head_b = B(m->head_b); d.head_mod = B(m->head_mod);
+    d.layers = new (std::nothrow) WfDitLayerDev[L];
+    if (!d.layers) return WF_ENOMEM;
+    for (int l = 0; l < L; ++l) {
+        const wf_dit_layer &w = m->layers[l];
+        d.layers[l] = {B(w.qkv_w), B(w.qkv_b), B(w.o_w), B(w.o_b), B(w.ffn1_w),
+                       B(w.ffn1_b), B(w.ffn2_w), B(w.ffn2_b), B(w.modulation),
+                       B(w.norm_q), B(w.norm_k),
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    }
+    const size_t latent = (size_t)d.C * p->g.gt * 4 * p->g.gh * p->g.gw;
+    const int slots = n_req * (p->S + 1);
+    wf_dit_carve(&d, workspace, slots - 1, p->NC, latent);
+    // model timestep per stage slot: warped nu_s for stage s, warped context_noise for the store
+    float tm[WF_MAX_TASKS];
+    for (int s = 0; s < p->S; ++s) tm[s] = (float)(1000.0 * warp_sigma(d.nu[s], d.shift));
+    tm[p->S] = (float)(1000.0 * warp_sigma(d.context_noise, d.shift));
+    if (cudaMemcpy(d.tmodel, tm, sizeof(float) * (p->S + 1), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(d.layers_dev, d.layers, sizeof(WfDitLayerDev) * L, cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+        return WF_ECUDA;
+    if (cudaMemsetAsync(d.lat, 0, 2 * (size_t)slots * latent * 4, stream) != cudaSuccess)
+        return WF_ECUDA;
+    if (wf_launch_time_embedding(d, p->S, n_req, stream) != cudaSuccess) return WF_ECUDA;
+    if (d.linear_fp8) {
+        const int dm = d.dim, f = d.ffn;
+        for (int l = 0; l < L; ++l) {
+            const WfDitLayerDev &w = d.layers[l];
+            if (wf_launch_quant_rows(w.qkv_w, 3 * dm, dm, w.qkv_w8, w.qkv_s, stream) != cudaSuccess ||
+                wf_launch_quant_rows(w.o_w, dm, dm, w.o_w8, w.o_s, stream) != cudaSuccess ||
+                wf_launch_quant_rows(w.f1_w, f, dm, w.f1_w8, w.f1_s, stream) != cudaSuccess ||
+                wf_launch_quant_rows(w.f2_w, dm, f, w.f2_w8, w.f2_s, stream) != cudaSuccess)
+                return WF_ECUDA;
+        }
+    }
+    return WF_OK;
+}
+
+// One DiT forward over the rows [r0, r1) of n_slots slot-indexed buffers
+// (a plan's S+1 slots, or a group's n (S+1)), every layer's publication and
+// attention through the given callbacks, then the head and the stage
+// transition into each request's next-round slot buffers.
+int wf_dit_pass(const WfDitPass &a, cudaStream_t stream) {
+    WfDit &d = *a.d;
+    const WfGeom &g = *a.g;
+    const int NC = g.NC, S = g.S;
+    const int dim = d.dim, mod_ld = 6 * dim;
+    const long long rows = (long long)a.n_slots * NC;
+    auto params = [&](int N, int K, const void *bias) {
+        GemmParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        gp.row_begin = a.r0;
+        gp.row_end = a.r1;
+        gp.N = N;
+        gp.K = K;
+        gp.bias = static_cast<const __nv_bfloat16 *>(bias);
+        gp.status = a.status;
+        return gp;
+    };
+    // patch embedding of every active task's input latent
+    if (wf_launch_patchify(g, d.C, a.src, a.lo, a.hi, d.patches, stream) != cudaSuccess) return WF_ECUDA;
+    GemmParams gp = params(dim, 4 * d.C, d.patch_b);
+    gp.out = d.x;
+    gp.ldo = dim;
+    if (wf_launch_gemm(WF_EPI_F32, d.patches, rows, 4 * d.C, d.patch_w, gp, a.num_sms, stream) !=
+        cudaSuccess)
+        return WF_ECUDA;
+
+    const bool f8 = d.linear_fp8 != 0;
+    for (int l = 0; l < d.L; ++l) {
+        const WfDitLayerDev &w = d.layers[l];
+        const float *mod = d.modtab + (size_t)l * a.n_slots * mod_ld;
+        // activations of the linear layers: bf16, or e4m3 with e4m3 weights
+        void *act = f8 ? static_cast<void *>(d.xa8) : static_cast<void *>(d.xa);
+        // P_{s,l}: x' = LN(x)(1 + scale_a) + shift_a; QKV projection, q/k RMSNorm, RoPE, publish
+        if (wf_launch_ln_mod(d.x, act, a.r0, a.r1, dim, NC, mod, mod_ld, 0, dim, stream, f8) != cudaSuccess)
+            return WF_ECUDA;
+        int rc = a.publish(l, act, w, f8);
+        if (rc != WF_OK) return rc;
+        // C_{s,l}: round attention (output over x', which is dead), then the rest of the block
+        rc = a.attend(l, act, f8);
+        if (rc != WF_OK) return rc;
+        gp = params(dim, dim, w.o_b);
+        gp.out = d.x;
+        gp.ldo = dim;
+        gp.gate = mod + 2 * dim;
+        gp.gate_ld = mod_ld;
+        gp.rows_per_group = NC;
+        gp.wscale = w.o_s;
+        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, act, rows, dim, f8 ? (const void *)w.o_w8 : w.o_w, gp,
+                           a.num_sms, stream, f8) != cudaSuccess)
+            return WF_ECUDA;
+        if (wf_launch_ln_mod(d.x, act, a.r0, a.r1, dim, NC, mod, mod_ld, 3 * dim, 4 * dim, stream, f8) !=
+            cudaSuccess)
+            return WF_ECUDA;
+        gp = params(d.ffn, dim, w.f1_b);
+        gp.out = f8 ? static_cast<void *>(d.h8) : static_cast<void *>(d.hmid);
+        gp.ldo = d.ffn;
+        gp.wscale = w.f1_s;
+        if (wf_launch_gemm(f8 ? WF_EPI_GELU_E4M3 : WF_EPI_GELU_BF16, act, rows, dim,
+                           f8 ? (const void *)w.f1_w8 : w.f1_w, gp, a.num_sms, stream, f8) != cudaSuccess)
+            return WF_ECUDA;
+        gp = params(dim, d.ffn, w.f2_b);
+        gp.out = d.x;
+        gp.ldo = dim;
+        gp.gate = mod + 5 * dim;
+        gp.gate_ld = mod_ld;
+        gp.rows_per_group = NC;
+        gp.wscale = w.f2_s;
+        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, f8 ? static_cast<const void *>(d.h8) : d.hmid, rows,
+                           d.ffn, f8 ? (const void *)w.f2_w8 : w.f2_w, gp, a.num_sms, stream, f8) !=
+            cudaSuccess)
+            return WF_ECUDA;
+    }
+
+    // head and stage transition (Eq. 1) into next round's slot inputs
+    if (wf_launch_ln_mod(d.x, d.xa, a.r0, a.r1, dim, NC, d.headtab, 2 * dim, 0, dim, stream) !=
+        cudaSuccess)
+        return WF_ECUDA;
+    gp = params(4 * d.C, dim, d.head_b);
+    gp.g = g;
+    gp.rd = *a.rd;
+    gp.channels = d.C;
+    for (int s = 0; s <= S; ++s)
+        gp.sigma_next[s] = s < S ? (float)warp_sigma(d.nu[s + 1], d.shift) : 0.f;
+    gp.eps = a.eps;
+    for (int m = 0; m < WF_MAX_GROUP; ++m) gp.z_next[m] = a.z_next[m];
+    gp.x0_out = a.x0_out;
+    gp.chunk_out = a.chunk_out;
+    if (wf_launch_gemm(WF_EPI_HEAD, d.xa, rows, dim, d.head_w, gp, a.num_sms, stream) != cudaSuccess)
+        return WF_ECUDA;
+    return WF_OK;
+}
 
 extern "C" {
 
@@ -139,86 +324,9 @@ int wf_dit_workspace_size(wf_plan_t p, int model_dim, int ffn_dim, int channels,
 int wf_dit_bind(wf_plan_t p, const wf_dit_model *m, void *workspace, cudaStream_t stream) {
     if (!p || !m || !workspace) return WF_EINVAL;
     if (!p->bound) return WF_EUNBOUND;
-    if ((p->o.dtype != WF_BF16 && p->o.dtype != WF_FP8) || p->D != 128) return WF_EUNSUPPORTED;
-    if ((uintptr_t)workspace & 255) return WF_EINVAL;
-    size_t need;
-    int rc = wf_dit_workspace_size(p, m->model_dim, m->ffn_dim, m->channels, m->freq_dim,
-                                   m->linear_fp8, &need);
-    if (rc != WF_OK) return rc;
-    if (!(m->shift > 0.0) || !std::isfinite(m->shift) || !(m->context_noise >= 0.0) ||
-        !(m->context_noise <= 1000.0))
-        return WF_EINVAL;
-    for (int s = 0; s < p->S; ++s)
-        if (!(m->timesteps[s] > 0.0 && m->timesteps[s] <= 1000.0) ||
-            (s > 0 && !(m->timesteps[s] < m->timesteps[s - 1])))
-            return WF_EINVAL;
-    const void *ptrs[] = {m->patch_w, m->t1_w, m->t1_b, m->t2_w, m->t2_b, m->tp_w, m->tp_b,
-                          m->head_w, m->head_mod, m->layers};
-    for (const void *q : ptrs)
-        if (!q) return WF_EINVAL;
-    const int L = p->o.layers;
-    for (int l = 0; l < L; ++l) {
-        const wf_dit_layer &w = m->layers[l];
-        if (!w.qkv_w || !w.o_w || !w.ffn1_w || !w.ffn2_w || !w.modulation || !w.norm_q || !w.norm_k)
-            return WF_EINVAL;
-        const void *all[] = {w.qkv_w, w.qkv_b, w.o_w, w.o_b, w.ffn1_w, w.ffn1_b, w.ffn2_w, w.ffn2_b,
-                             w.norm_q, w.norm_k};
-        for (const void *q : all)
-            if (q && !aligned16(q)) return WF_EINVAL;
-    }
-    WfDit &d = p->dit;
-    delete[] d.layers;
-    d.layers = nullptr;
     p->dit_bound = false;
-    d.dim = m->model_dim;
-    d.ffn = m->ffn_dim;
-    d.C = m->channels;
-    d.freq = m->freq_dim;
-    d.L = L;
-    d.linear_fp8 = m->linear_fp8;
-    d.shift = m->shift;
-    d.context_noise = m->context_noise;
-    for (int s = 0; s < p->S; ++s) d.nu[s] = m->timesteps[s];
-    d.nu[p->S] = 0.0;
-    auto B = [](const void *q) { return static_cast<const __nv_bfloat16 *>(q); };
-    d.patch_w = B(m->patch_w); d.patch_b = B(m->patch_b);
-    d.t1_w = B(m->t1_w); d.t1_b = B(m->t1_b);
-    d.t2_w = B(m->t2_w); d.t2_b = B(m->t2_b);
-    d.tp_w = B(m->tp_w); d.tp_b = B(m->tp_b);
-    d.head_w = B(m->head_w); d.head_b = B(m->head_b); d.head_mod = B(m->head_mod);
-    d.layers = new (std::nothrow) WfDitLayerDev[L];
-    if (!d.layers) return WF_ENOMEM;
-    for (int l = 0; l < L; ++l) {
-        const wf_dit_layer &w = m->layers[l];
-        d.layers[l] = {B(w.qkv_w), B(w.qkv_b), B(w.o_w), B(w.o_b), B(w.ffn1_w),
-                       B(w.ffn1_b), B(w.ffn2_w), B(w.ffn2_b), B(w.modulation),
-                       B(w.norm_q), B(w.norm_k),
-                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-    }
-    const size_t latent = (size_t)d.C * p->g.gt * 4 * p->g.gh * p->g.gw;
-    wf_dit_carve(&d, workspace, p->S, p->NC, latent);
-    // model timestep per slot: warped nu_s for stage s, warped context_noise for the store
-    float tm[WF_MAX_TASKS];
-    for (int s = 0; s < p->S; ++s) tm[s] = (float)(1000.0 * warp_sigma(d.nu[s], d.shift));
-    tm[p->S] = (float)(1000.0 * warp_sigma(d.context_noise, d.shift));
-    if (cudaMemcpy(d.tmodel, tm, sizeof(float) * (p->S + 1), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemcpy(d.layers_dev, d.layers, sizeof(WfDitLayerDev) * L, cudaMemcpyHostToDevice) !=
-            cudaSuccess)
-        return WF_ECUDA;
-    if (cudaMemsetAsync(d.lat, 0, 2 * (size_t)(p->S + 1) * latent * 4, stream) != cudaSuccess)
-        return WF_ECUDA;
-    if (wf_launch_time_embedding(d, p->S, stream) != cudaSuccess) return WF_ECUDA;
-    if (d.linear_fp8) {
-        const int dm = d.dim, f = d.ffn;
-        for (int l = 0; l < L; ++l) {
-            const WfDitLayerDev &w = d.layers[l];
-            if (wf_launch_quant_rows(w.qkv_w, 3 * dm, dm, w.qkv_w8, w.qkv_s, stream) != cudaSuccess ||
-                wf_launch_quant_rows(w.o_w, dm, dm, w.o_w8, w.o_s, stream) != cudaSuccess ||
-                wf_launch_quant_rows(w.f1_w, f, dm, w.f1_w8, w.f1_s, stream) != cudaSuccess ||
-                wf_launch_quant_rows(w.f2_w, dm, f, w.f2_w8, w.f2_s, stream) != cudaSuccess)
-                return WF_ECUDA;
-        }
-    }
+    const int rc = wf_dit_bind_impl(&p->dit, p, m, workspace, 1, stream);
+    if (rc != WF_OK) return rc;
     p->dit_bound = true;
     return WF_OK;
 }
@@ -239,92 +347,39 @@ int wf_dit_round(wf_plan_t p, const float *z_new, const float *eps, float *x0_ou
     WfDit &d = p->dit;
     int lo, hi;
     wf_active_range(p, &lo, &hi);
-    const int r0 = lo * NC, r1 = (hi + 1) * NC;
-    const long long rows = (long long)(S + 1) * NC;
     const size_t latent = d.latent;
     float *lat_cur = d.lat + (size_t)(k & 1) * (S + 1) * latent;
     float *lat_next = d.lat + (size_t)((k + 1) & 1) * (S + 1) * latent;
-    const int dim = d.dim, mod_ld = 6 * dim;
 
-    // patch embedding of every active task's input latent
-    const float *src[WF_MAX_TASKS];
-    src[0] = z_new;
-    for (int s = 1; s <= S; ++s) src[s] = lat_cur + (size_t)s * latent;
-    if (wf_launch_patchify(p->g, d.C, src, lo, hi, d.patches, stream) != cudaSuccess) return WF_ECUDA;
-    GemmParams gp = base_params(p, r0, r1, dim, 4 * d.C, d.patch_b);
-    gp.out = d.x;
-    gp.ldo = dim;
-    if (wf_launch_gemm(WF_EPI_F32, d.patches, rows, 4 * d.C, d.patch_w, gp, p->num_sms, stream) !=
-        cudaSuccess)
-        return WF_ECUDA;
-
-    const bool f8 = d.linear_fp8 != 0;
-    for (int l = 0; l < d.L; ++l) {
-        const WfDitLayerDev &w = d.layers[l];
-        const float *mod = d.modtab + (size_t)l * (S + 1) * mod_ld;
-        // activations of the linear layers: bf16, or e4m3 with e4m3 weights
-        void *act = f8 ? static_cast<void *>(d.xa8) : static_cast<void *>(d.xa);
-        // P_{s,l}: x' = LN(x)(1 + scale_a) + shift_a; QKV projection, RoPE, publish
-        if (wf_launch_ln_mod(d.x, act, r0, r1, dim, NC, mod, mod_ld, 0, dim, stream, f8) != cudaSuccess)
-            return WF_ECUDA;
+    WfDitPass a;
+    a.d = &d;
+    a.g = &p->g;
+    a.n_slots = S + 1;
+    a.lo = lo;
+    a.hi = hi;
+    a.r0 = lo * NC;
+    a.r1 = (hi + 1) * NC;
+    a.rd = &p->rd;
+    a.status = static_cast<uint32_t *>(p->scratch);
+    a.num_sms = p->num_sms;
+    for (int i = 0; i < WF_MAX_ROUND_TASKS; ++i) a.src[i] = nullptr;
+    a.src[0] = z_new;
+    for (int s = 1; s <= S; ++s) a.src[s] = lat_cur + (size_t)s * latent;
+    for (int m = 0; m < WF_MAX_GROUP; ++m) a.z_next[m] = m == 0 ? lat_next : nullptr;
+    a.eps = eps;
+    a.x0_out = x0_out;
+    a.chunk_out = chunk_out;
+    a.publish = [&](int l, const void *act, const WfDitLayerDev &w, bool f8) {
         // (q/k RMSNorm: the projection leaves unrotated q | k rows in hmid, free until FFN1)
-        int rc = f8 ? wf_publish_impl(p, l, d.xa8, w.qkv_w8, w.qkv_b, nullptr, stream, w.qkv_s,
-                                      w.nq, w.nk, d.hmid)
-                    : wf_publish_impl(p, l, d.xa, w.qkv_w, w.qkv_b, nullptr, stream, nullptr, w.nq,
-                                      w.nk, d.hmid);
-        if (rc != WF_OK) return rc;
-        // C_{s,l}: round attention (output over x', which is dead), then the rest of the block
-        rc = wf_attention_impl(p, l, act, WF_ATTN_TC, stream, f8 ? 1 : 0);
-        if (rc != WF_OK) return rc;
-        gp = base_params(p, r0, r1, dim, dim, w.o_b);
-        gp.out = d.x;
-        gp.ldo = dim;
-        gp.gate = mod + 2 * dim;
-        gp.gate_ld = mod_ld;
-        gp.rows_per_group = NC;
-        gp.wscale = w.o_s;
-        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, act, rows, dim, f8 ? (const void *)w.o_w8 : w.o_w, gp,
-                           p->num_sms, stream, f8) != cudaSuccess)
-            return WF_ECUDA;
-        if (wf_launch_ln_mod(d.x, act, r0, r1, dim, NC, mod, mod_ld, 3 * dim, 4 * dim, stream, f8) !=
-            cudaSuccess)
-            return WF_ECUDA;
-        gp = base_params(p, r0, r1, d.ffn, dim, w.f1_b);
-        gp.out = f8 ? static_cast<void *>(d.h8) : static_cast<void *>(d.hmid);
-        gp.ldo = d.ffn;
-        gp.wscale = w.f1_s;
-        if (wf_launch_gemm(f8 ? WF_EPI_GELU_E4M3 : WF_EPI_GELU_BF16, act, rows, dim,
-                           f8 ? (const void *)w.f1_w8 : w.f1_w, gp, p->num_sms, stream, f8) != cudaSuccess)
-            return WF_ECUDA;
-        gp = base_params(p, r0, r1, dim, d.ffn, w.f2_b);
-        gp.out = d.x;
-        gp.ldo = dim;
-        gp.gate = mod + 5 * dim;
-        gp.gate_ld = mod_ld;
-        gp.rows_per_group = NC;
-        gp.wscale = w.f2_s;
-        if (wf_launch_gemm(WF_EPI_GATED_RESIDUAL, f8 ? static_cast<const void *>(d.h8) : d.hmid, rows,
-                           d.ffn, f8 ? (const void *)w.f2_w8 : w.f2_w, gp, p->num_sms, stream, f8) !=
-            cudaSuccess)
-            return WF_ECUDA;
-    }
-
-    // head and stage transition (Eq. 1) into next round's slot inputs
-    if (wf_launch_ln_mod(d.x, d.xa, r0, r1, dim, NC, d.headtab, 2 * dim, 0, dim, stream) !=
-        cudaSuccess)
-        return WF_ECUDA;
-    gp = base_params(p, r0, r1, 4 * d.C, dim, d.head_b);
-    gp.g = p->g;
-    gp.channels = d.C;
-    for (int s = 0; s <= S; ++s)
-        gp.sigma_next[s] = s < S ? (float)warp_sigma(d.nu[s + 1], d.shift) : 0.f;
-    gp.eps = eps;
-    gp.z_next = lat_next;
-    gp.x0_out = x0_out;
-    gp.chunk_out = chunk_out;
-    if (wf_launch_gemm(WF_EPI_HEAD, d.xa, rows, dim, d.head_w, gp, p->num_sms, stream) != cudaSuccess)
-        return WF_ECUDA;
-    return WF_OK;
+        return f8 ? wf_publish_impl(p, l, act, w.qkv_w8, w.qkv_b, nullptr, stream, w.qkv_s, w.nq, w.nk,
+                                    d.hmid)
+                  : wf_publish_impl(p, l, act, w.qkv_w, w.qkv_b, nullptr, stream, nullptr, w.nq, w.nk,
+                                    d.hmid);
+    };
+    a.attend = [&](int l, void *act, bool f8) {
+        return wf_attention_impl(p, l, act, WF_ATTN_TC, stream, f8 ? 1 : 0);
+    };
+    return wf_dit_pass(a, stream);
 }
 
 }  // extern "C"

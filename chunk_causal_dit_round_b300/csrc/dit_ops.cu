@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256) ln_mod_reg_kernel(const float *__restrict
 // Row n of slot s: features (channel c, row offset q, column offset r) of the
 // 2 x 2 patch of token (f, h, w); one thread per (token, channel).
 struct SlotSrc {
-    const float *p[WF_MAX_TASKS];
+    const float *p[WF_MAX_ROUND_TASKS];   // per (global) slot
 };
 
 __global__ void __launch_bounds__(256) patchify_kernel(const WfGeom g, int C, SlotSrc src, int lo,
@@ -143,9 +143,12 @@ __global__ void __launch_bounds__(256) patchify_kernel(const WfGeom g, int C, Sl
         const int n = (int)(tok % g.NC);
         const int hw = g.gh * g.gw;
         const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n % g.gw;
-        const float *z = src.p[slot] + (size_t)c * cstride + ((size_t)f * Hl + 2 * hh) * Wl + 2 * ww;
-        const float2 top = *reinterpret_cast<const float2 *>(z);
-        const float2 bot = *reinterpret_cast<const float2 *>(z + Wl);
+        float2 top = make_float2(0.f, 0.f), bot = top;     // a slot without a task: zero patches
+        if (src.p[slot]) {
+            const float *z = src.p[slot] + (size_t)c * cstride + ((size_t)f * Hl + 2 * hh) * Wl + 2 * ww;
+            top = *reinterpret_cast<const float2 *>(z);
+            bot = *reinterpret_cast<const float2 *>(z + Wl);
+        }
         __nv_bfloat162 a = __floats2bfloat162_rn(top.x, top.y), b = __floats2bfloat162_rn(bot.x, bot.y);
         uint2 w = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
         *reinterpret_cast<uint2 *>(patches + ((size_t)slot * g.NC + n) * 4 * C + 4 * c) = w;
@@ -197,27 +200,30 @@ __global__ void __launch_bounds__(256) gemv_kernel(const __nv_bfloat16 *__restri
     }
 }
 
-// modtab[l][b][i][:] = mod_l[i][:] + e0[b][i][:];  headtab[b][i][:] = head_mod[i][:] + e[b][:]
-__global__ void tables_kernel(const WfDitLayerDev *layers, int L, int B, int dim,
+// modtab[l][b][i][:] = mod_l[i][:] + e0[b % B][i][:];  headtab[b][i][:] = head_mod[i][:] + e[b % B][:]
+// for b < B_out: the tables of the B stage slots, written once per request of
+// a group (B_out = n B; slot b of the group is stage b % B).
+__global__ void tables_kernel(const WfDitLayerDev *layers, int L, int B, int B_out, int dim,
                               const float *temb, int temb_ld, int e_off, int e0_off,
                               const __nv_bfloat16 *head_mod, float *modtab, float *headtab) {
-    const long long n_mod = (long long)L * B * 6 * dim;
-    const long long n_head = (long long)B * 2 * dim;
+    const long long n_mod = (long long)L * B_out * 6 * dim;
+    const long long n_head = (long long)B_out * 2 * dim;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_mod + n_head;
          i += (long long)gridDim.x * blockDim.x) {
         if (i < n_mod) {
             const int c = (int)(i % dim);
             const int r = (int)((i / dim) % 6);
-            const int b = (int)((i / (6LL * dim)) % B);
-            const int l = (int)(i / (6LL * dim * B));
+            const int b = (int)((i / (6LL * dim)) % B_out);
+            const int l = (int)(i / (6LL * dim * B_out));
             modtab[i] = __bfloat162float(layers[l].mod[r * dim + c]) +
-                        temb[(size_t)b * temb_ld + e0_off + r * dim + c];
+                        temb[(size_t)(b % B) * temb_ld + e0_off + r * dim + c];
         } else {
             const long long j = i - n_mod;
             const int c = (int)(j % dim);
             const int r = (int)((j / dim) % 2);
             const int b = (int)(j / (2LL * dim));
-            headtab[j] = __bfloat162float(head_mod[r * dim + c]) + temb[(size_t)b * temb_ld + e_off + c];
+            headtab[j] = __bfloat162float(head_mod[r * dim + c]) +
+                         temb[(size_t)(b % B) * temb_ld + e_off + c];
         }
     }
 }
@@ -310,6 +316,7 @@ cudaError_t wf_launch_ln_mod(const float *x, void *out, int row_begin, int row_e
 
 cudaError_t wf_launch_patchify(const WfGeom &g, int C, const float *const *src, int lo, int hi,
                                __nv_bfloat16 *patches, cudaStream_t stream) {
+    if (lo < 0 || hi >= WF_MAX_ROUND_TASKS || hi < lo) return cudaErrorInvalidValue;
     SlotSrc s{};
     for (int i = lo; i <= hi; ++i) s.p[i] = src[i];
     const long long total = (long long)(hi - lo + 1) * g.NC * C;
@@ -320,7 +327,7 @@ cudaError_t wf_launch_patchify(const WfGeom &g, int C, const float *const *src, 
     return cudaGetLastError();
 }
 
-cudaError_t wf_launch_time_embedding(const WfDit &d, int S, cudaStream_t stream) {
+cudaError_t wf_launch_time_embedding(const WfDit &d, int S, int n_req, cudaStream_t stream) {
     // temb row b: [sinusoid (freq) | h1 (dim) | e (dim) | e0 (6 dim)]
     const int B = S + 1, dim = d.dim;
     const int ld = d.freq + 9 * dim;
@@ -335,7 +342,7 @@ cudaError_t wf_launch_time_embedding(const WfDit &d, int S, cudaStream_t stream)
     gemv(d.t1_w, d.t1_b, 0, o_h1, dim, d.freq, 0);
     gemv(d.t2_w, d.t2_b, o_h1, o_e, dim, dim, 1);
     gemv(d.tp_w, d.tp_b, o_e, o_e0, 6 * dim, dim, 1);
-    tables_kernel<<<148 * 4, 256, 0, stream>>>(d.layers_dev, d.L, B, dim, T, ld, o_e, o_e0,
+    tables_kernel<<<148 * 4, 256, 0, stream>>>(d.layers_dev, d.L, B, n_req * B, dim, T, ld, o_e, o_e0,
                                                d.head_mod, d.modtab, d.headtab);
     return cudaGetLastError();
 }

@@ -387,8 +387,11 @@ template <>
 struct Epi<WF_EPI_HEAD> {
     __device__ static void apply(const GemmParams &p, int row, int col, float (&v)[32]) {
         const WfGeom &g = p.g;
-        const int slot = row / g.NC;
-        const int n = row - slot * g.NC;
+        const int gslot = row / g.NC;               // request m, stage slot `slot`
+        if (p.rd.task_of_slot[gslot] < 0) return;   // no task in this slot this round
+        const int m = gslot / (g.S + 1);
+        const int slot = gslot - m * (g.S + 1);
+        const int n = row - gslot * g.NC;
         const int hw = g.gh * g.gw;
         const int f = n / hw, hh = (n / g.gw) % g.gh, ww = n - (n / g.gw) * g.gw;
         const int C = p.channels;
@@ -396,10 +399,10 @@ struct Epi<WF_EPI_HEAD> {
         const size_t cstride = (size_t)g.gt * Hl * Wl;
         const size_t lat = (size_t)C * cstride;
         const float sg = p.sigma_next[slot];
-        float *x0 = p.x0_out ? p.x0_out + (size_t)slot * lat : nullptr;
-        float *zn = slot < g.S ? p.z_next + (size_t)(slot + 1) * lat : nullptr;
-        const float *eps = (slot < g.S && sg != 0.f) ? p.eps + (size_t)slot * lat : nullptr;
-        float *emit = (slot == g.S - 1) ? p.chunk_out : nullptr;
+        float *x0 = p.x0_out ? p.x0_out + (size_t)gslot * lat : nullptr;
+        float *zn = slot < g.S ? p.z_next[m] + (size_t)(slot + 1) * lat : nullptr;
+        const float *eps = (slot < g.S && sg != 0.f) ? p.eps + ((size_t)m * g.S + slot) * lat : nullptr;
+        float *emit = (slot == g.S - 1 && p.chunk_out) ? p.chunk_out + (size_t)m * lat : nullptr;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int j = col + i;              // feature index (q, r, c)

@@ -23,6 +23,12 @@ struct wf_group_s {
     wf_plan_s *plans[WF_MAX_GROUP] = {};
     bool tmaps_ok = false;
     WfTmaps tmaps;   // over the n consecutive query workspaces and pools
+    // DiT model of the group (wf_group_dit_bind): activations for n (S+1)
+    // slots; member r's latent slot inputs at lat + r * 2 (S+1) latent,
+    // double-buffered by that member's own round parity
+    bool dit_bound = false;
+    WfDit dit{};
+    ~wf_group_s() { delete[] dit.layers; }
 };
 
 namespace {
@@ -72,7 +78,7 @@ int check_mask(const wf_group_s *gr, unsigned mask) {
 // else the given qkv), with each plan's anchor re-rotation.
 int group_publish(wf_group_s *gr, unsigned mask, int layer, const void *x, const void *w_qkv,
                   const void *b_qkv, const void *nq, const void *nk, void *qk_tmp, const void *qkv,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const float *wscale = nullptr) {
     wf_plan_s *p0 = gr->plans[0];
     if (layer < 0 || layer >= p0->o.layers) return WF_ERANGE;
     WfRoundDev rd;
@@ -107,6 +113,7 @@ int group_publish(wf_group_s *gr, unsigned mask, int layer, const void *x, const
         a.x_rows = (long long)gr->n * (p0->S + 1) * p0->NC;
         a.w_qkv = w_qkv;
         a.b_qkv = b_qkv;
+        a.wscale = wscale;
         a.nq = nq;
         a.nk = nk;
         a.qk_tmp = qk_tmp;
@@ -128,6 +135,36 @@ int group_publish(wf_group_s *gr, unsigned mask, int layer, const void *x, const
         gr->plans[r]->published[layer] = gr->plans[r]->k;
     }
     return WF_OK;
+}
+
+// Round attention of the selected members' current rounds, one launch
+// (out_e4m3: O as e4m3 bytes, tensor-core kernel only).
+int group_attention(wf_group_s *gr, unsigned mask, int layer, void *out, int kernel,
+                    cudaStream_t stream, int out_e4m3) {
+    wf_plan_s *p0 = gr->plans[0];
+    for (int r = 0; r < gr->n; ++r) {
+        if (!((mask >> r) & 1u)) continue;
+        const wf_plan_s *p = gr->plans[r];
+        if (p->k < 0) return WF_ENOROUND;
+        if (p->published[layer] != p->k) return WF_EORDER;
+    }
+    WfRoundDev rd;
+    int rc = group_round(gr, mask, &rd);
+    if (rc != WF_OK) return rc;
+    if (rd.n_tasks == 0) return WF_OK;
+    const bool tc_ok = gr->tmaps_ok && wf_attn_tc_supported(p0->g, p0->o.dtype);
+    const bool simt_ok = p0->D % 32 == 0 && p0->D <= 128 && p0->o.dtype != WF_FP8 && !out_e4m3;
+    if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
+    cudaError_t e;
+    if (kernel == WF_ATTN_TC) {
+        if (!tc_ok) return WF_EUNSUPPORTED;
+        e = wf_launch_attn_tc(p0->g, rd, layer, gr->tmaps, out, p0->scratch, p0->num_sms, stream,
+                              out_e4m3);
+    } else {
+        if (!simt_ok) return WF_EUNSUPPORTED;
+        e = wf_launch_attn_simt(p0->g, rd, layer, p0->o.dtype, p0->qbuf, p0->pool, out, stream);
+    }
+    return e == cudaSuccess ? WF_OK : WF_ECUDA;
 }
 
 }  // namespace
@@ -205,32 +242,97 @@ int wf_group_attention(wf_group_t gr, unsigned int plan_mask, int layer, void *o
     if (!gr) return WF_EINVAL;
     int rc = check_mask(gr, plan_mask);
     if (rc != WF_OK) return rc;
-    wf_plan_s *p0 = gr->plans[0];
-    if (layer < 0 || layer >= p0->o.layers) return WF_ERANGE;
+    if (layer < 0 || layer >= gr->plans[0]->o.layers) return WF_ERANGE;
     if (!out || !aligned16(out)) return WF_EINVAL;
     if (kernel != WF_ATTN_AUTO && kernel != WF_ATTN_TC && kernel != WF_ATTN_SIMT) return WF_EINVAL;
-    for (int r = 0; r < gr->n; ++r) {
-        if (!((plan_mask >> r) & 1u)) continue;
-        const wf_plan_s *p = gr->plans[r];
-        if (p->k < 0) return WF_ENOROUND;
-        if (p->published[layer] != p->k) return WF_EORDER;
-    }
+    return group_attention(gr, plan_mask, layer, out, kernel, stream, 0);
+}
+
+int wf_group_dit_workspace_size(wf_group_t gr, int model_dim, int ffn_dim, int channels,
+                                int freq_dim, int linear_fp8, size_t *bytes) {
+    if (!gr || !bytes) return WF_EINVAL;
+    wf_plan_s *p0 = gr->plans[0];
+    size_t one;
+    const int rc = wf_dit_workspace_size(p0, model_dim, ffn_dim, channels, freq_dim, linear_fp8, &one);
+    if (rc != WF_OK) return rc;
+    const size_t latent = (size_t)channels * p0->g.gt * 4 * p0->g.gh * p0->g.gw;
+    *bytes = wf_dit_workspace_bytes(gr->n * (p0->S + 1) - 1, p0->NC, model_dim, ffn_dim, channels,
+                                    freq_dim, p0->o.layers, latent, linear_fp8);
+    return WF_OK;
+}
+
+int wf_group_dit_bind(wf_group_t gr, const wf_dit_model *m, void *workspace, cudaStream_t stream) {
+    if (!gr || !m || !workspace) return WF_EINVAL;
+    gr->dit_bound = false;
+    const int rc = wf_dit_bind_impl(&gr->dit, gr->plans[0], m, workspace, gr->n, stream);
+    if (rc != WF_OK) return rc;
+    gr->dit_bound = true;
+    return WF_OK;
+}
+
+int wf_group_dit_round(wf_group_t gr, unsigned int plan_mask, const float *z_new, const float *eps,
+                       float *x0_out, float *chunk_out, cudaStream_t stream) {
+    if (!gr) return WF_EINVAL;
+    int rc = check_mask(gr, plan_mask);
+    if (rc != WF_OK) return rc;
+    if (!gr->dit_bound) return WF_EUNBOUND;
+    wf_plan_s *p0 = gr->plans[0];
+    const int S = p0->S, NC = p0->NC, slots = S + 1;
     WfRoundDev rd;
     rc = group_round(gr, plan_mask, &rd);
     if (rc != WF_OK) return rc;
     if (rd.n_tasks == 0) return WF_OK;
-    const bool tc_ok = gr->tmaps_ok && wf_attn_tc_supported(p0->g, p0->o.dtype);
-    const bool simt_ok = p0->D % 32 == 0 && p0->D <= 128 && p0->o.dtype != WF_FP8;
-    if (kernel == WF_ATTN_AUTO) kernel = tc_ok ? WF_ATTN_TC : WF_ATTN_SIMT;
-    cudaError_t e;
-    if (kernel == WF_ATTN_TC) {
-        if (!tc_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_tc(p0->g, rd, layer, gr->tmaps, out, p0->scratch, p0->num_sms, stream);
-    } else {
-        if (!simt_ok) return WF_EUNSUPPORTED;
-        e = wf_launch_attn_simt(p0->g, rd, layer, p0->o.dtype, p0->qbuf, p0->pool, out, stream);
+    bool new_chunk = false;                      // a task at stage 0 reads z_new
+    int lo = WF_MAX_ROUND_TASKS, hi = -1;
+    for (int i = 0; i < rd.n_tasks; ++i) {
+        new_chunk |= rd.slot[i] % slots == 0;
+        lo = std::min(lo, rd.slot[i]);
+        hi = std::max(hi, rd.slot[i]);
     }
-    return e == cudaSuccess ? WF_OK : WF_ECUDA;
+    if (new_chunk && (!z_new || ((uintptr_t)z_new & 7))) return WF_EINVAL;
+    if (S > 1 && (!eps || !aligned16(eps))) return WF_EINVAL;
+    if ((x0_out && !aligned16(x0_out)) || (chunk_out && ((uintptr_t)chunk_out & 3)))
+        return WF_EINVAL;
+    WfDit &d = gr->dit;
+    const size_t latent = d.latent;
+
+    WfDitPass a;
+    a.d = &d;
+    a.g = &p0->g;
+    a.n_slots = gr->n * slots;
+    a.lo = lo;
+    a.hi = hi;
+    a.r0 = lo * NC;
+    a.r1 = (hi + 1) * NC;
+    a.rd = &rd;
+    a.status = static_cast<uint32_t *>(p0->scratch);
+    a.num_sms = p0->num_sms;
+    for (int i = 0; i < WF_MAX_ROUND_TASKS; ++i) a.src[i] = nullptr;
+    for (int r = 0; r < WF_MAX_GROUP; ++r) a.z_next[r] = nullptr;
+    for (int r = 0; r < gr->n; ++r) {
+        if (!((plan_mask >> r) & 1u)) continue;
+        const int k = gr->plans[r]->k;
+        float *own = d.lat + (size_t)r * 2 * slots * latent;
+        const float *cur = own + (size_t)(k & 1) * slots * latent;
+        a.z_next[r] = own + (size_t)((k + 1) & 1) * slots * latent;
+        for (int s = 0; s <= S; ++s) {
+            const int gs = r * slots + s;
+            if (rd.task_of_slot[gs] < 0) continue;
+            a.src[gs] = s == 0 ? z_new + (size_t)r * latent : cur + (size_t)s * latent;
+        }
+    }
+    a.eps = eps;
+    a.x0_out = x0_out;
+    a.chunk_out = chunk_out;
+    a.publish = [&](int l, const void *act, const WfDitLayerDev &w, bool f8) {
+        // (q/k RMSNorm: the projection leaves unrotated q | k rows in hmid, free until FFN1)
+        return group_publish(gr, plan_mask, l, act, f8 ? (const void *)w.qkv_w8 : w.qkv_w, w.qkv_b,
+                             w.nq, w.nk, d.hmid, nullptr, stream, f8 ? w.qkv_s : nullptr);
+    };
+    a.attend = [&](int l, void *act, bool f8) {
+        return group_attention(gr, plan_mask, l, act, WF_ATTN_TC, stream, f8 ? 1 : 0);
+    };
+    return wf_dit_pass(a, stream);
 }
 
 void wf_group_destroy(wf_group_t gr) { delete gr; }

@@ -144,11 +144,12 @@ struct GemmParams {
                                  // the q/k RMSNorm kernel, which rotates and publishes them
     // head + stage transition
     int channels;
-    float sigma_next[WF_MAX_TASKS];  // per slot: warped sigma of the next stage (0: identity)
-    const float *eps;            // [S][latent] transition draws, or null
-    float *z_next;               // [S+1][latent] next round's slot inputs
-    float *x0_out;               // [S+1][latent] predictions, or null
-    float *chunk_out;            // [latent] emitted clean chunk, or null
+    float sigma_next[WF_MAX_TASKS];  // per stage slot: warped sigma of the next stage (0: identity)
+    // request m of a group owns global slots m (S+1) .. m (S+1) + S (m = 0 for one plan)
+    const float *eps;            // [n][S][latent] transition draws, or null
+    float *z_next[WF_MAX_GROUP]; // per request: [S+1][latent] next round's slot inputs
+    float *x0_out;               // [n][S+1][latent] predictions, or null
+    float *chunk_out;            // [n][latent] emitted clean chunks, or null
 };
 
 int wf_gemm_bn_for(int epi);
@@ -201,7 +202,9 @@ cudaError_t wf_launch_ln_mod(const float *x, void *out, int row_begin, int row_e
                              cudaStream_t stream, bool out_e4m3 = false);
 cudaError_t wf_launch_patchify(const WfGeom &g, int C, const float *const *src, int lo, int hi,
                                __nv_bfloat16 *patches, cudaStream_t stream);
-cudaError_t wf_launch_time_embedding(const WfDit &d, int S, cudaStream_t stream);
+// Timestep embeddings of the S+1 stage slots and the modulation / head
+// tables, written once per request of a group (n_req = 1 for one plan).
+cudaError_t wf_launch_time_embedding(const WfDit &d, int S, int n_req, cudaStream_t stream);
 
 // ---- failure-detection self-test (selftest.cu) --------------------------------
 cudaError_t wf_launch_wait_probe(void *scratch, uint64_t limit_ns, cudaStream_t stream);

@@ -2,6 +2,7 @@
 // request), shared by the host files of the library.  Not part of the C ABI.
 #pragma once
 
+#include <functional>
 #include <deque>
 #include <utility>
 #include <vector>
@@ -109,4 +110,33 @@ int wf_publish_impl(wf_plan_s *p, int layer, const void *x, const void *w_qkv, c
 // tasks by slot (all by default).  Returns a WF_* code.
 int wf_attention_impl(wf_plan_s *p, int layer, void *out, int kernel, cudaStream_t stream,
                       int out_e4m3 = 0, unsigned slot_mask = ~0u);
+
+// ---- one DiT forward over slot-indexed buffers (dit.cpp) ---------------------
+// Binding of the DiT model's pointers and tables for n_req requests of p's
+// shape (a plan: n_req = 1; a group: its member count), activations carved
+// for n_req (S+1) slots of `workspace`.  Returns a WF_* code.
+int wf_dit_bind_impl(WfDit *d, const wf_plan_s *p, const wf_dit_model *m, void *workspace,
+                     int n_req, cudaStream_t stream);
+
+// What one DiT forward needs besides the model: the round view (global
+// slots; request m owns slots m (S+1) .. m (S+1) + S), the rows it covers,
+// the per-slot inputs, the per-request outputs and the layer steps that
+// differ between a plan and a group (publication and attention).
+struct WfDitPass {
+    WfDit *d;
+    const WfGeom *g;
+    int n_slots;                              // slot rows of the activation buffers
+    int lo, hi;                               // first / last slot with a task
+    int r0, r1;                               // rows [lo NC, (hi+1) NC)
+    const WfRoundDev *rd;
+    uint32_t *status;
+    int num_sms;
+    const float *src[WF_MAX_ROUND_TASKS];     // per slot: input latent (null: no task)
+    float *z_next[WF_MAX_GROUP];              // per request: next round's slot inputs
+    const float *eps;
+    float *x0_out, *chunk_out;
+    std::function<int(int layer, const void *act, const WfDitLayerDev &w, bool f8)> publish;
+    std::function<int(int layer, void *act, bool f8)> attend;
+};
+int wf_dit_pass(const WfDitPass &a, cudaStream_t stream);
 

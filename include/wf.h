@@ -465,6 +465,42 @@ int wf_dit_bind(wf_plan_t plan, const wf_dit_model *model, void *workspace, cuda
 int wf_dit_round(wf_plan_t plan, const float *z_new, const float *eps, float *x0_out,
                  float *chunk_out, cudaStream_t stream);
 
+/* ---- whole DiT rounds of a group -------------------------------------------
+ * The DiT round of every selected member of a group (wf_group_create) in one
+ * pass: one patch embedding, per layer one projection + publication, one
+ * attention launch, the output projection and the FFN over all selected
+ * members' tasks, then one head.  Each member computes exactly what its own
+ * wf_dit_round computes (same kernels, global slots as in the group calls).
+ * The group keeps its own DiT state: the members' latent slot inputs live
+ * in the group workspace, double-buffered by each member's round parity, so
+ * a member advanced by group rounds is not also run by wf_dit_round.
+ *
+ * wf_group_dit_workspace_size: bytes of the group's DiT workspace (the
+ *   single-plan workspace with n (S+1) slots).  Errors: as
+ *   wf_dit_workspace_size.
+ * wf_group_dit_bind: as wf_dit_bind for the group (model checked against
+ *   member 0; workspace 256-byte aligned, caller-owned; modulation tables
+ *   written once per member; latent buffers cleared).  The weight pointers
+ *   are kept.
+ * wf_group_dit_round: members in plan_mask, each already entered into its
+ *   current round with wf_round_step.  Request r's arguments sit at
+ *   r times the single-plan sizes:
+ *     z_new      float [n][latent]: member r's fresh chunk, read when member r
+ *                has a stage-0 task
+ *     eps        float [n][S][latent] (may be NULL when S == 1)
+ *     x0_out     float [n][S+1][latent] or NULL (rows of active slots written)
+ *     chunk_out  float [n][latent] or NULL (row r written when member r has a
+ *                stage-(S-1) task)
+ *   Launches use member 0's scratch (wf_sync_status(plans[0])).  Errors:
+ *   WF_EINVAL (mask, pointers), WF_EUNBOUND (no wf_group_dit_bind),
+ *   WF_ENOROUND, WF_ECUDA. */
+int wf_group_dit_workspace_size(wf_group_t group, int model_dim, int ffn_dim, int channels,
+                                int freq_dim, int linear_fp8, size_t *bytes);
+int wf_group_dit_bind(wf_group_t group, const wf_dit_model *model, void *workspace,
+                      cudaStream_t stream);
+int wf_group_dit_round(wf_group_t group, unsigned int plan_mask, const float *z_new,
+                       const float *eps, float *x0_out, float *chunk_out, cudaStream_t stream);
+
 /* Read and clear the device status word in scratch (synchronises stream).
  * Returns WF_OK, WF_ETIMEOUT if a kernel's bounded wait gave up, or WF_ECUDA. */
 int wf_sync_status(wf_plan_t plan, cudaStream_t stream);

@@ -215,6 +215,10 @@ def test_group_entry_points_validate_on_the_host():
     assert wf.lib.wf_group_attention(None, 1, 0, p, wf.WF_ATTN_TC, None) == wf.WF_EINVAL
     assert wf.lib.wf_group_publish(None, 1, 0, p, None) == wf.WF_EINVAL
     assert wf.lib.wf_group_proj_publish(None, 1, 0, p, p, None, None, None, None, None) == wf.WF_EINVAL
+    n = ctypes.c_size_t()
+    assert wf.lib.wf_group_dit_workspace_size(None, 256, 512, 16, 256, 0, ctypes.byref(n)) == wf.WF_EINVAL
+    assert wf.lib.wf_group_dit_bind(None, None, p, None) == wf.WF_EINVAL
+    assert wf.lib.wf_group_dit_round(None, 1, p, p, None, None, None) == wf.WF_EINVAL
     wf.lib.wf_group_destroy(None)
     for h in plans:
         wf.lib.wf_plan_destroy(h)
