@@ -371,6 +371,102 @@ def _sustained_peak():
     return 1400.0, "fallback"
 
 
+def _dit_params(g, dev, dim, ffn, L, C):
+    """Random-init Wan2.1-shaped DiT weights, bf16 ~ N(0, 0.02); q / k
+    RMSNorm gains 1 + N(0, 0.02^2)."""
+    import torch
+
+    def rnd(*shape, std=0.02):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    P = {"patch_w": rnd(dim, 4 * C), "patch_b": rnd(dim), "t1_w": rnd(dim, 256), "t1_b": rnd(dim),
+         "t2_w": rnd(dim, dim), "t2_b": rnd(dim), "tp_w": rnd(6 * dim, dim), "tp_b": rnd(6 * dim),
+         "head_w": rnd(4 * C, dim), "head_b": rnd(4 * C), "head_mod": rnd(2, dim)}
+    for k_, shp in (("qkv_w", (3 * dim, dim)), ("qkv_b", (3 * dim,)), ("o_w", (dim, dim)),
+                    ("o_b", (dim,)), ("f1_w", (ffn, dim)), ("f1_b", (ffn,)), ("f2_w", (dim, ffn)),
+                    ("f2_b", (dim,)), ("mod", (6, dim))):
+        P[k_] = [rnd(*shp) for _ in range(L)]
+    for k_ in ("nq", "nk"):
+        P[k_] = [(1 + rnd(dim).float()).to(torch.bfloat16) for _ in range(L)]
+    return P
+
+
+def run_dit_streams(args, rank, world, counts=(1, 2, 4, 8), steps=10, warmup=3):
+    """Several requests batched into whole DiT rounds (wf_group_dit_round):
+    R requests of the random-init Wan2.1-1.3B-shaped DiT (dit13's model, S = 4,
+    30 blocks), each steady round one group DiT pass over all R (S+1) tasks;
+    every request completes one chunk per round, so chunks/s = R / round time.
+    At small chunks one request's GEMMs and attention fill a fraction of the
+    SMs; batching recovers it."""
+    import torch
+    import chunk_causal_dit_round_b300 as wf
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = DIT_CONFIGS["dit13"]
+    S, W, H, D, dim, ffn = cfg["S"], cfg["history"], cfg["heads"], cfg["head_dim"], cfg["dim"], cfg["ffn"]
+    L = getattr(args, "layers", None) or cfg["layers"]
+    C = 16
+    k_steady = S + W + 2
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321 + rank)
+    P = _dit_params(g, dev, dim, ffn, L, C)
+    out = {}
+    for name in ("chunk390", "chunk1560"):
+        shp = STREAM_SHAPES[name]
+        NC = math.prod(shp["grid"])
+        latent = C * shp["grid"][0] * 4 * shp["grid"][1] * shp["grid"][2]
+        rows = []
+        for R in counts:
+            grp = wf.Group(R, S, NC, H, D, W, n_chunks=k_steady + warmup + 400, layers=L,
+                           grid=shp["grid"], dtype=wf.WF_BF16, device=dev)
+            model = wf.GroupDit(grp, P, ffn=ffn, channels=C, freq=256, timesteps=cfg["steps"])
+            z = torch.randn((R, latent), generator=g, device=dev)
+            eps = torch.randn((R, S, latent), generator=g, device=dev)
+            chunk = torch.empty((R, latent), device=dev)
+            mask = (1 << R) - 1
+
+            def one():
+                for r in grp.rounds:
+                    r.step()
+                model.round(mask, z, eps, None, chunk, stream)
+
+            for _ in range(k_steady + warmup):
+                one()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            one()
+            torch.cuda.synchronize()
+            n_t = max(steps, int(0.3 / max(time.perf_counter() - t0, 1e-4)))
+            n_t = min(n_t, grp.rounds[0].n_left())
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with ClockSampler(dev.index) as clk:
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(n_t):
+                    one()
+                e1.record(stream)
+                torch.cuda.synchronize()
+            st = grp.rounds[0].sync_status()
+            if st != wf.WF_OK:
+                raise RuntimeError(f"device status {st}")
+            ms, = max_over_ranks([e0.elapsed_time(e1)], world, dev)
+            rows.append({"requests": R, "chunks_per_s": round(world * R * n_t / (ms * 1e-3), 2),
+                         "round_ms": round(ms / n_t, 3), "rounds": n_t, "clocks": clk.summary()})
+            del model
+            grp.close()
+            del grp, z, eps, chunk
+            torch.cuda.empty_cache()
+        base1 = rows[0]["chunks_per_s"]
+        for r_ in rows:
+            r_["vs_one_request"] = round(r_["chunks_per_s"] / base1, 3)
+        out[name] = {"chunk_tokens": NC, "desc": shp["desc"], "rows": rows}
+    return {"workload": f"batched requests, whole DiT rounds ({cfg['desc']}; chunk size as listed)",
+            "layers": L, "unit": "chunks/s", "shapes": out,
+            "gpu_launches_per_round": 4 + 8 * L}
+
+
 def run_dit(args, name, rank, world, steps=None, warmup=None):
     """Steady wavefront rounds of the whole DiT forward (wf_dit_round): per
     layer LN + modulation, QKV projection + RoPE + paged publish, round
@@ -399,19 +495,7 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
                  schedule=wf.WF_SCHED_SEQUENTIAL if seq else wf.WF_SCHED_WAVEFRONT)
     g = torch.Generator(device=dev)
     g.manual_seed(4321 + rank)
-
-    def rnd(*shape, std=0.02):
-        return (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
-
-    P = {"patch_w": rnd(dim, 4 * C), "patch_b": rnd(dim), "t1_w": rnd(dim, 256), "t1_b": rnd(dim),
-         "t2_w": rnd(dim, dim), "t2_b": rnd(dim), "tp_w": rnd(6 * dim, dim), "tp_b": rnd(6 * dim),
-         "head_w": rnd(4 * C, dim), "head_b": rnd(4 * C), "head_mod": rnd(2, dim)}
-    for k_, shp in (("qkv_w", (3 * dim, dim)), ("qkv_b", (3 * dim,)), ("o_w", (dim, dim)),
-                    ("o_b", (dim,)), ("f1_w", (ffn, dim)), ("f1_b", (ffn,)), ("f2_w", (dim, ffn)),
-                    ("f2_b", (dim,)), ("mod", (6, dim))):
-        P[k_] = [rnd(*shp) for _ in range(L)]
-    for k_ in ("nq", "nk"):          # q / k RMSNorm gains: 1 + N(0, 0.02^2)
-        P[k_] = [(1 + rnd(dim).float()).to(torch.bfloat16) for _ in range(L)]
+    P = _dit_params(g, dev, dim, ffn, L, C)
     model = wf.Dit(r, P, ffn=ffn, channels=C, freq=256, timesteps=cfg["steps"],
                    linear_fp8=cfg.get("linear_fp8", False))
     latent = C * cfg["grid"][0] * 4 * cfg["grid"][1] * cfg["grid"][2]
@@ -1036,7 +1120,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="wan13_attn",
                     choices=sorted(CONFIGS) + sorted(DIT_CONFIGS) + sorted(QKV_ATTN_CONFIGS)
-                    + ["streams", "peaks"])
+                    + ["streams", "dit_streams", "peaks"])
     ap.add_argument("--no-dit", action="store_true", help="skip the DiT round measurement")
     ap.add_argument("--layers", type=int, default=None,
                     help="DiT configs: override the block count (smaller profiling captures only)")
@@ -1063,8 +1147,9 @@ def main():
         if rank == 0:
             print(json.dumps(measure_peaks()), flush=True)
         return
-    if args.config == "streams":
-        d = run_streams(args, rank, world, steps=args.steps, warmup=args.warmup)
+    if args.config in ("streams", "dit_streams"):
+        fn = run_streams if args.config == "streams" else run_dit_streams
+        d = fn(args, rank, world, steps=args.steps, warmup=args.warmup)
         if rank == 0:
             print(json.dumps(d), flush=True)
         if world > 1:
