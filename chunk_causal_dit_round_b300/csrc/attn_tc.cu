@@ -27,15 +27,6 @@
 //    when it grows by more than 2^8, and O is rescaled in TMEM only then.
 //  * TMEM (512 columns): S0 | S1 | O0 | O1, P aliasing the first 64 columns of S.
 //
-// Row-split variant (576 threads): each tile's softmax is spread over two
-// warpgroups, warps 0-7 taking key columns 0-63 of S (and output columns
-// 0-63 of O) and warps 8-15 columns 64-127, so a tile's chain of TMEM
-// loads, exponentials and P stores is half as long; the two threads of a
-// row trade their partial row max (and at the end their partial sums)
-// through shared memory under a 64-thread mbarrier.  Warp 16 is the TMA
-// producer and warp 17 the MMA issuer.  No register split: 96 registers a
-// thread (five warps on a sub-partition's 16K registers).
-//
 // Every wait is bounded (%globaltimer); on a timeout the kernel records it in
 // the scratch status word, drains its own copies and MMAs, frees TMEM and
 // returns.
@@ -43,7 +34,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "wf_internal.h"
@@ -57,14 +47,7 @@ constexpr int BM = 128;             // query rows per tile
 constexpr int BN = 128;             // keys per tile
 constexpr int HD = 128;             // head dim
 constexpr int NST = 4;              // K/V ring stages
-
-// Threads and the producer / MMA warps of the two variants (RS: row-split).
-template <bool RS> struct Roles {
-    static constexpr int THREADS = RS ? 576 : 384;
-    static constexpr int SOFTMAX_WARPS = RS ? 16 : 8;
-    static constexpr int PRODUCER = SOFTMAX_WARPS;      // TMA producer warp
-    static constexpr int MMA = SOFTMAX_WARPS + 1;       // MMA issuer warp (owns TMEM)
-};
+constexpr int NUM_THREADS = 384;
 
 // Shared-memory layout of one CTA.  bf16: a 128 x 128 tile is two 64-column
 // halves of 128-byte rows (16 KB each); e4m3: one block of 128-byte rows.
@@ -85,14 +68,12 @@ constexpr int B_SFULL = B_KVEMPTY + NST;
 constexpr int B_PFULL = B_SFULL + 2;
 constexpr int B_ODONE = B_PFULL + 2;
 constexpr int B_DRAIN = B_ODONE + 2;
-constexpr int B_XCH = B_DRAIN + 1;     // row-split: per (tile, lane quarter) exchange of a row's halves
-constexpr int NBARS = B_XCH + 8;
+constexpr int NBARS = B_DRAIN + 1;
 
 template <bool F8>
 struct LayMisc {
     static constexpr uint32_t MISC = Lay<F8>::BAR + ((NBARS * 8 + 63) / 64) * 64;
-    static constexpr uint32_t XCH = MISC + 64;            // [2 parity][2 tile][2 half][128 rows] floats
-    static constexpr uint32_t ALLOC = XCH + 4096 + 1024;  // + alignment slack
+    static constexpr uint32_t ALLOC = MISC + 64 + 1024;   // + alignment slack
 };
 
 constexpr uint64_t WAIT_NS = 1000000000ull;  // 1 s
@@ -106,10 +87,6 @@ constexpr int REGS_SOFTMAX = 224;
 constexpr int REGS_AUX = 56;
 static_assert(8 * (REGS_SOFTMAX - LAUNCH_REGS) <= 4 * (LAUNCH_REGS - REGS_AUX),
               "register split exceeds the launch pool");
-static_assert(Roles<false>::THREADS * LAUNCH_REGS <= 65536, "launch registers exceed the SM");
-// the row-split variant runs without a split, at the launch bound's cap
-constexpr int LAUNCH_REGS_RS = 112;
-static_assert(Roles<true>::THREADS * LAUNCH_REGS_RS <= 65536, "launch registers exceed the SM");
 
 struct TcParams {
     int layer;
@@ -433,171 +410,8 @@ __device__ void softmax_tile(const Ctx<F8> &c, uint32_t tmem, const WfGeom &g, c
     }
 }
 
-// Softmax of tile X split over two warpgroups: half hf owns key columns
-// [64 hf, 64 hf + 64) of S and output columns [64 hf, 64 hf + 64) of O for
-// all 128 rows.  The two threads of a row trade partial values through
-// shared memory (xch, double-buffered by exchange parity) under a 64-thread
-// mbarrier per (tile, lane quarter) and take identical decisions from them:
-// the row max (fmaxf of the same two values), the rescaling, the row sum.
 template <bool F8>
-__device__ void softmax_half(const Ctx<F8> &c, uint32_t tmem, float *xch, const WfGeom &g,
-                             const WfRoundDev &rd, const TcParams &p, int X, int hf, int ti, int h,
-                             int qp, int n, uint32_t it_base, uint32_t unit_iter, uint32_t &xc) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + X * 128;
-    const uint32_t tO = tmem + lane_off + 256 + X * 128 + hf * 64;
-    const int xb = B_XCH + X * 4 + wq;
-    const float sl2 = p.sl2;
-    float m_run = -INFINITY, l_run = 0.f;
-    // this row's partner value of exchange xc; false when a wait gave up
-    auto exchange = [&](float v, float &other) -> bool {
-        const uint32_t par = xc & 1;
-        float *e = xch + (par * 2 + X) * 256 + row;
-        e[hf * 128] = v;
-        tc_fence_before();
-        mbar_arrive(c.bar(xb));
-        const bool ok = c.wait(xb, par, 14 + X);
-        ++xc;
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        tc_fence_after();
-        other = e[(hf ^ 1) * 128];
-        return true;
-    };
-
-    for (int j = 0; j < n; ++j) {
-        bool ok = c.wait(B_SFULL + X, (it_base + j) & 1, 10 + X);
-        if (!__all_sync(0xffffffffu, ok)) return;
-        tc_fence_after();
-        uint32_t r[2][32];
-        tmem_ld32(tS + hf * 64, r[0]);
-        tmem_ld32(tS + hf * 64 + 32, r[1]);
-        tmem_wait_ld(r[0]);
-        tmem_wait_ld(r[1]);
-        const int t = j % p.tpc;
-        const int valid = g.NC - t * BN - hf * 64;   // valid keys among this half's 64
-        if (valid < 64) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (q * 32 + i >= valid) r[q][i] = __float_as_uint(-INFINITY);
-        }
-        // partial row max: 4 independent chains of 3-input max over 16 scores each
-        float pm[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const uint32_t *v = &r[a >> 1][(a & 1) * 16];
-            float m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-            for (int i = 3; i < 15; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-            pm[a] = fmaxf(m, __uint_as_float(v[15]));
-        }
-        const float mh = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-        float mo;
-        if (!exchange(mh, mo)) return;
-        const float mnew = fmaxf(mh, mo) * sl2;
-        float alpha = 1.f;
-        if (mnew > m_run + 8.f) {
-            alpha = ex2(m_run - mnew);
-            m_run = mnew;
-        }
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t negm2 = f2_pack(-m_run, -m_run);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        // P over S (both halves' S loads completed before the exchange), one
-        // 32-key quarter at a time: 16 bf16 pairs (16 columns) or 8 e4m3
-        // quads; stored before the O rescale so that P and O are never live
-        // together
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                uint64_t x = f2_fma(f2_pack(__uint_as_float(r[q][2 * i]), __uint_as_float(r[q][2 * i + 1])),
-                                    sl2x2, negm2);
-                float a0, a1;
-                f2_unpack(x, a0, a1);
-                const float p0 = ex2(a0), p1 = ex2(a1);
-                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                if constexpr (F8) {
-                    const uint32_t hw = pack_e4m3x2(p0, p1);
-                    uint32_t &w = pk[(q & 1) * 8 + (i >> 1)];
-                    w = (i & 1) ? (w | (hw << 16)) : hw;
-                } else {
-                    pk[i] = pack_bf16(p0, p1);
-                }
-            }
-            if constexpr (F8) {
-                if (q == 1) tmem_st16(tS + hf * 16, pk);
-            } else {
-                tmem_st16(tS + hf * 32 + q * 16, pk);
-            }
-        }
-        float s0, s1, s2, s3;
-        f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
-        f2_unpack(f2_add(acc[2], acc[3]), s2, s3);
-        l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                uint32_t o[32];
-                tmem_ld32(tO + q * 32, o);
-                tmem_wait_ld(o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(tO + q * 32, o);
-            }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(c.bar(B_PFULL + X));
-    }
-
-    bool ok = c.wait(B_ODONE + X, unit_iter & 1, 12 + X);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-    float lo;
-    if (!exchange(l_run, lo)) return;
-    const int qrow = (2 * qp + X) * BM + row;
-    const float inv = p.o_scale / (l_run + lo);
-    const size_t o_off = (((size_t)rd.slot[ti] * g.NC + qrow) * g.H + h) * HD + hf * 64;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        uint32_t o[32];
-        tmem_ld32(tO + q * 32, o);
-        tmem_wait_ld(o);
-        if (qrow < g.NC) {
-            if (p.out_e4m3) {
-                uint32_t w[8];
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    w[v] = pack_e4m3x2(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv) |
-                           (pack_e4m3x2(__uint_as_float(o[4 * v + 2]) * inv,
-                                        __uint_as_float(o[4 * v + 3]) * inv) << 16);
-                uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(p.out) + o_off + q * 32);
-                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-                uint4 *d4 = reinterpret_cast<uint4 *>(p.out + o_off + q * 32);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                    w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                    w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                    w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                    d4[v] = w;
-                }
-            }
-        }
-    }
-}
-
-template <bool F8, bool RS>
-__global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
                    const WfGeom g, const WfRoundDev rd, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -615,7 +429,6 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
     uint32_t *work = p.ctl + WF_SCRATCH_WORK / 4;
     uint32_t *done = p.ctl + WF_SCRATCH_DONE / 4;
 
-    using R = Roles<RS>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(c.bar(B_QFULL), 1);
@@ -625,20 +438,19 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(c.bar(B_SFULL + x), 1);
-            mbar_init(c.bar(B_PFULL + x), RS ? 256 : 128);
+            mbar_init(c.bar(B_PFULL + x), 128);
             mbar_init(c.bar(B_ODONE + x), 1);
         }
         mbar_init(c.bar(B_DRAIN), 1);
-        for (int i = 0; i < 8; ++i) mbar_init(c.bar(B_XCH + i), 64);
         mbar_fence_init();
         *c.abort = 0;
         unit_slot[0] = blockIdx.x;
     }
-    if (warp == R::PRODUCER && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tkv);
     }
-    if (warp == R::MMA) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -648,7 +460,7 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     // Every role walks the same unit sequence; units end on named barrier 1
-    // over all the CTA's threads, after which the next unit index (fetched by
+    // over all 384 threads, after which the next unit index (fetched by
     // thread 0) is read.  Each role has its own loop so that the register
     // budget set right before it applies to the whole loop.
     uint32_t seq = 0, it_base = 0, unit_iter = 0, issued = 0;
@@ -658,41 +470,28 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
         unit_iter += 1;
         if (threadIdx.x == 0) unit_slot[unit_iter & 1] = (int)(gridDim.x + atomicAdd(work, 1u));
         tc_fence_before();
-        named_bar_sync(1, R::THREADS);
+        named_bar_sync(1, NUM_THREADS);
         tc_fence_after();
         return *c.abort ? p.n_units : unit_slot[unit_iter & 1];
     };
-    if (warp < R::SOFTMAX_WARPS) {
-        if constexpr (RS) {
-            float *xch = reinterpret_cast<float *>(smem + LayMisc<F8>::XCH);
-            uint32_t xc = 0;   // exchanges of this row pair so far (mbarrier phase)
-            for (int u = unit_slot[0]; u < p.n_units;) {
-                int ti, h, qp;
-                decode_unit(u, rd, p, g.H, ti, h, qp);
-                const int n = rd.n_ctx[ti] * p.tpc;
-                softmax_half<F8>(c, tmem, xch, g, rd, p, (warp >> 2) & 1, warp >> 3, ti, h, qp, n,
-                                 it_base, unit_iter, xc);
-                u = next_unit(n);
-            }
-        } else {
-            reg_inc<REGS_SOFTMAX>();
-            for (int u = unit_slot[0]; u < p.n_units;) {
-                int ti, h, qp;
-                decode_unit(u, rd, p, g.H, ti, h, qp);
-                const int n = rd.n_ctx[ti] * p.tpc;
-                softmax_tile<F8>(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
-                u = next_unit(n);
-            }
-        }
-    } else {
-        if constexpr (!RS) reg_dec<REGS_AUX>();
+    if (warp < 8) {
+        reg_inc<REGS_SOFTMAX>();
         for (int u = unit_slot[0]; u < p.n_units;) {
             int ti, h, qp;
             decode_unit(u, rd, p, g.H, ti, h, qp);
             const int n = rd.n_ctx[ti] * p.tpc;
-            if (warp == R::PRODUCER && lane == 0)
+            softmax_tile<F8>(c, tmem, g, rd, p, warp >> 2, ti, h, qp, n, it_base, unit_iter);
+            u = next_unit(n);
+        }
+    } else {
+        reg_dec<REGS_AUX>();
+        for (int u = unit_slot[0]; u < p.n_units;) {
+            int ti, h, qp;
+            decode_unit(u, rd, p, g.H, ti, h, qp);
+            const int n = rd.n_ctx[ti] * p.tpc;
+            if (warp == 8 && lane == 0)
                 producer<F8>(c, &tq, &tkv, g, rd, p, ti, h, qp, n, seq, &issued);
-            else if (warp == R::MMA && lane == 0)
+            else if (warp == 9 && lane == 0)
                 mma_issuer<F8>(c, tmem, n, seq, it_base, unit_iter);
             u = next_unit(n);
         }
@@ -701,7 +500,7 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
     if (*c.abort) {
         // give the copies and MMAs this CTA started time to land before TMEM
         // and shared memory are released
-        if (warp == R::PRODUCER && lane == 0) {
+        if (warp == 8 && lane == 0) {
             uint32_t first = issued > (uint32_t)NST ? issued - NST : 0;
             for (uint32_t s = first; s < issued; ++s)
                 mbar_wait(c.bar(B_KVFULL + s % NST), (s / NST) & 1, nullptr, nullptr, nullptr, 0,
@@ -710,7 +509,7 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
                 mbar_wait(c.bar(B_QFULL), (unit_iter - 1) & 1, nullptr, nullptr, nullptr, 0,
                           WAIT_NS);
         }
-        if (warp == R::MMA && lane == 0) {
+        if (warp == 9 && lane == 0) {
             mma_commit(c.bar(B_DRAIN));
             mbar_wait(c.bar(B_DRAIN), 0, nullptr, nullptr, nullptr, 0, WAIT_NS);
         }
@@ -718,7 +517,7 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == R::MMA) tmem_dealloc(tmem, 512);
+    if (warp == 9) tmem_dealloc(tmem, 512);
     if (threadIdx.x == 0) {
         __threadfence();
         uint32_t prev = atomicAdd(done, 1u);
@@ -730,40 +529,18 @@ __global__ void __launch_bounds__(Roles<RS>::THREADS, 1)
 }
 
 // Opt in to the shared-memory size and refuse to launch unless the kernel was
-// compiled to exactly the register count the setmaxnreg split assumes (the
-// row-split variant: at most its cap).
-template <bool F8, bool RS>
+// compiled to exactly the register count the setmaxnreg split assumes.
+template <bool F8>
 cudaError_t prepare_kernel() {
     static std::atomic<unsigned long long> done{0};
     return wf_once_per_device(done, [] {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<F8, RS>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<F8>);
         if (e != cudaSuccess) return e;
-        if (RS ? fa.numRegs > LAUNCH_REGS_RS : fa.numRegs != LAUNCH_REGS)
-            return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(attn_tc_kernel<F8, RS>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, LayMisc<F8>::ALLOC);
+        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        return cudaFuncSetAttribute(attn_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    LayMisc<F8>::ALLOC);
     });
-}
-
-// Kernel variant: WF_ATTN_ROWSPLIT=0 / 1 in the environment selects the
-// one-warpgroup-per-tile or the row-split softmax (read once per process).
-bool use_rowsplit() {
-    static const bool rs = [] {
-        const char *v = std::getenv("WF_ATTN_ROWSPLIT");
-        return v ? std::atoi(v) != 0 : false;
-    }();
-    return rs;
-}
-
-template <bool F8, bool RS>
-cudaError_t launch_variant(int grid, const WfTmaps &maps, const WfGeom &g, const WfRoundDev &rd,
-                           const TcParams &p, cudaStream_t stream) {
-    cudaError_t e = prepare_kernel<F8, RS>();
-    if (e != cudaSuccess) return e;
-    attn_tc_kernel<F8, RS><<<grid, Roles<RS>::THREADS, LayMisc<F8>::ALLOC, stream>>>(maps.q, maps.kv, g,
-                                                                                    rd, p);
-    return cudaGetLastError();
 }
 
 // Parameters and launch of one round's attention (ctl: the scheduler
@@ -772,6 +549,8 @@ cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const Wf
                       void *out, uint32_t *ctl, uint32_t *stat, int num_sms, cudaStream_t stream,
                       int out_e4m3 = 0) {
     const bool f8 = g.dtype == WF_FP8;
+    cudaError_t e = f8 ? prepare_kernel<true>() : prepare_kernel<false>();
+    if (e != cudaSuccess) return e;
     TcParams p;
     p.layer = layer;
     p.tpc = (g.NC + BN - 1) / BN;
@@ -788,12 +567,11 @@ cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const Wf
     p.ctl = ctl;
     p.stat = stat;
     int grid = p.n_units < num_sms ? p.n_units : num_sms;
-    const bool rs = use_rowsplit();
     if (f8)
-        return rs ? launch_variant<true, true>(grid, maps, g, rd, p, stream)
-                  : launch_variant<true, false>(grid, maps, g, rd, p, stream);
-    return rs ? launch_variant<false, true>(grid, maps, g, rd, p, stream)
-              : launch_variant<false, false>(grid, maps, g, rd, p, stream);
+        attn_tc_kernel<true><<<grid, NUM_THREADS, LayMisc<true>::ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
+    else
+        attn_tc_kernel<false><<<grid, NUM_THREADS, LayMisc<false>::ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
