@@ -12,7 +12,11 @@
 //
 // Design (one persistent CTA per SM, 384 threads):
 //  * work unit = (task, head, pair of 128-row query tiles); units are handed
-//    out longest-context-first through an atomic counter in scratch;
+//    out through an atomic counter in scratch, in blocks of a few heads
+//    (longest context first inside a block), the block size chosen on the
+//    host by simulating the hand-out: it sets how the longest units spread
+//    over the waves, and a block whose pages fit in L2 lets the round's
+//    tasks, which share most of their pages, read each page from DRAM once;
 //  * warp 8 (one thread): TMA producer -- both Q tiles, then K_0, K_1, V_0,
 //    K_2, V_1, ... through a 4-stage ring of 32 KB tiles (128B swizzle); the
 //    pages are read through a 3D tensor map [plane][N_C][128], so rows past
@@ -92,6 +96,7 @@ struct TcParams {
     int layer;
     int n_units;
     int qpairs;           // pairs of query tiles per (task, head)
+    int hblk;             // heads per block of the unit order
     int tpc;              // key tiles per chunk
     float sl2;            // log2(e) / sqrt(D) (/ qk_scale^2 for e4m3 Q and K)
     float o_scale;        // 1 (bf16) or 1 / v_scale (e4m3 V)
@@ -115,14 +120,24 @@ struct Ctx {
     }
 };
 
+// Unit order: blocks of hblk heads; inside a block the tasks longest
+// context first (rd.lpt), then the block's heads, then the pairs of query
+// tiles.  The tasks of a round share most of their context pages, so a
+// block whose pages fit in L2 reads each (page, head) from DRAM about once;
+// hblk = H is plain longest-first order over (task, head).
 __device__ __forceinline__ void decode_unit(int u, const WfRoundDev &rd, const TcParams &p, int H,
                                             int &ti, int &h, int &qp) {
-    int per_task = H * p.qpairs;
-    int oi = u / per_task;
-    int rem = u - oi * per_task;
+    const int per_block = rd.n_tasks * p.hblk * p.qpairs;
+    const int b = u / per_block;                       // the last block may hold fewer heads
+    const int h0 = b * p.hblk;
+    const int nh = min(p.hblk, H - h0);
+    const int rem = u - b * per_block;
+    const int per_task = nh * p.qpairs;
+    const int oi = rem / per_task;
+    const int r2 = rem - oi * per_task;
     ti = rd.lpt[oi];
-    h = rem / p.qpairs;
-    qp = rem - h * p.qpairs;
+    h = h0 + r2 / p.qpairs;
+    qp = r2 - (r2 / p.qpairs) * p.qpairs;
 }
 
 // ---- producer ----------------------------------------------------------------
@@ -543,6 +558,97 @@ cudaError_t prepare_kernel() {
     });
 }
 
+// ---- unit order ----------------------------------------------------------------
+// Finish time of the last CTA when `workers` persistent CTAs take the units
+// in decode_unit's order for blocks of hblk heads, each the next unit as
+// soon as it is free; a unit costs its key tiles plus a few tiles' worth of
+// Q loads and O stores.
+double simulate_order(const WfRoundDev &rd, int H, int qpairs, int tpc, int hblk, int workers) {
+    double heap[1024];                       // min-heap of the CTAs' busy-until times
+    for (int i = 0; i < workers; ++i) heap[i] = 0.0;
+    auto take = [&](double cost) {           // the earliest-free CTA takes the unit
+        heap[0] += cost;
+        int i = 0;
+        for (;;) {
+            int c = 2 * i + 1;
+            if (c >= workers) break;
+            if (c + 1 < workers && heap[c + 1] < heap[c]) ++c;
+            if (heap[c] >= heap[i]) break;
+            const double t = heap[c];
+            heap[c] = heap[i];
+            heap[i] = t;
+            i = c;
+        }
+    };
+    for (int h0 = 0; h0 < H; h0 += hblk) {
+        const int nh = hblk < H - h0 ? hblk : H - h0;
+        for (int oi = 0; oi < rd.n_tasks; ++oi) {
+            const double cost = (double)rd.n_ctx[rd.lpt[oi]] * tpc + 3.0;
+            for (int u = 0; u < nh * qpairs; ++u) take(cost);
+        }
+    }
+    double end = 0.0;
+    for (int i = 0; i < workers; ++i) end = heap[i] > end ? heap[i] : end;
+    return end;
+}
+
+// Heads per block of the unit order.  Blocks of a few heads keep the pages
+// the round's tasks share in L2, and the block size also sets how the
+// longest units spread over the waves, so it is chosen by simulating the
+// hand-out above for every candidate (1 .. 16 heads and H) and taking the
+// shortest finish; among near-ties the blocks whose pages (K and V at bf16
+// width) fit in about 80 MB of L2 win.  Cached per round shape (no
+// allocation: a small fixed table).
+int heads_per_block(const WfGeom &g, const WfRoundDev &rd, int qpairs, int tpc, int workers) {
+    if (workers < 1 || workers > 1024 || rd.n_tasks < 1) return g.H;
+    uint64_t key = 1469598103934665603ull;   // FNV-1a over the shape
+    auto mix = [&](uint64_t v) { key = (key ^ v) * 1099511628211ull; };
+    mix((uint64_t)g.H);
+    mix((uint64_t)qpairs);
+    mix((uint64_t)tpc);
+    mix((uint64_t)workers);
+    mix((uint64_t)g.NC);
+    mix((uint64_t)rd.n_tasks);
+    bool seen[256] = {};
+    int distinct = 0;
+    for (int i = 0; i < rd.n_tasks; ++i) {
+        mix((uint64_t)rd.n_ctx[rd.lpt[i]]);
+        for (int e = 0; e < rd.n_ctx[i]; ++e)
+            if (!seen[rd.page[i][e]]) {
+                seen[rd.page[i][e]] = true;
+                ++distinct;
+            }
+    }
+    mix((uint64_t)distinct);
+    constexpr int kSlots = 64;
+    static std::mutex mu;
+    static uint64_t keys[kSlots];
+    static int vals[kSlots];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const int slot = (int)(key % kSlots);
+        if (vals[slot] > 0 && keys[slot] == key) return vals[slot];
+    }
+    const double head_bytes = (double)distinct * g.NC * HD * 2 * 2;
+    const int fit = head_bytes > 0 ? (int)(80e6 / head_bytes) : g.H;
+    int best = g.H;
+    double best_t = 0.0;
+    for (int G = 1; G <= g.H; ++G) {
+        if (G > 16 && G != g.H) continue;
+        double t = simulate_order(rd, g.H, qpairs, tpc, G, workers);
+        if (G > fit) t *= 1.003;             // DRAM re-reads once the block leaves L2
+        if (G == 1 || t < best_t) {
+            best = G;
+            best_t = t;
+        }
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    const int slot = (int)(key % kSlots);
+    keys[slot] = key;
+    vals[slot] = best;
+    return best;
+}
+
 // Parameters and launch of one round's attention (ctl: the scheduler
 // counters; stat: the status and wait-site words).
 cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const WfTmaps &maps,
@@ -556,6 +662,8 @@ cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const Wf
     p.tpc = (g.NC + BN - 1) / BN;
     p.qpairs = ((g.NC + BM - 1) / BM + 1) / 2;
     p.n_units = rd.n_tasks * g.H * p.qpairs;
+    const int grid = p.n_units < num_sms ? p.n_units : num_sms;
+    p.hblk = heads_per_block(g, rd, p.qpairs, p.tpc, grid);
     p.sl2 = 1.4426950408889634f / sqrtf((float)HD);
     p.o_scale = 1.f;
     if (f8) {
@@ -566,7 +674,6 @@ cudaError_t launch_tc(const WfGeom &g, const WfRoundDev &rd, int layer, const Wf
     p.out_e4m3 = out_e4m3;
     p.ctl = ctl;
     p.stat = stat;
-    int grid = p.n_units < num_sms ? p.n_units : num_sms;
     if (f8)
         attn_tc_kernel<true><<<grid, NUM_THREADS, LayMisc<true>::ALLOC, stream>>>(maps.q, maps.kv, g, rd, p);
     else
