@@ -49,7 +49,7 @@ UNIT = "TFLOP/s"
 # again.
 ATTN_TC_SOURCES = ("chunk_causal_dit_round_b300/csrc/attn_tc.cu",
                    "chunk_causal_dit_round_b300/csrc/wf_ptx.cuh")
-ATTN_TC_TRAFFIC = {"bf16": (1.2591e9, "4bc1dbc751bd96d4"), "e4m3": (6.117e8, "4bc1dbc751bd96d4")}
+ATTN_TC_TRAFFIC = {"bf16": (5.2925e8, "d47bd0f5fe615e78"), "e4m3": (2.1823e8, "d47bd0f5fe615e78")}
 
 
 def _sources_sha16(paths):
