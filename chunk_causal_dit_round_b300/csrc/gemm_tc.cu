@@ -89,6 +89,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32
         "r"(c0), "r"(c1), "r"(src)
         : "memory");
 }
+// global[box at (c0, c1)] = the shared-memory box at src
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the bulk copies of this thread have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() {
@@ -563,7 +570,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) mbar_arrive(bar(C::B_TEMPTY + buf));
                 }
                 const int col = n0 + c * 32;
-                if constexpr (EPI == WF_EPI_GATED_RESIDUAL) {
+                // Row-major outputs (bf16, GELU bf16 / e4m3, the QKV
+                // projection's unrotated q | k rows) leave through shared
+                // memory: a warp's 32 rows x 128 bytes (64 bf16 or 128 e4m3
+                // columns, several 32-column chunks) are staged in the TMA's
+                // 128-byte swizzled layout and written by one TMA store, so
+                // the global writes are whole lines instead of one row per
+                // thread; rows past row_end and columns past the output's
+                // width are clipped by the map.
+                constexpr bool STAGEABLE = EPI == WF_EPI_BF16 || EPI == WF_EPI_GELU_BF16 ||
+                                           EPI == WF_EPI_GELU_E4M3 || EPI == WF_EPI_QKV_PUBLISH;
+                constexpr int CPB = EPI == WF_EPI_GELU_E4M3 ? 4 : 2;   // chunks per staged block
+                bool staged = false;
+                if constexpr (STAGEABLE)
+                    staged = p.staged && (EPI != WF_EPI_QKV_PUBLISH || col < 2 * p.g.H * p.g.D);
+                if (staged) {
+                    const int cb = c % CPB;
+                    const int col0 = col - cb * 32;           // first column of the block
+                    uint8_t *stg = smem + C::SM_STAGE + (warp - 2) * 4096;
+                    if (cb == 0) {
+                        if (lane == 0) bulk_wait_read();      // the previous block has left stg
+                        __syncwarp();
+                    }
+                    if (col < p.N) {
+                        uint64_t v2[16];
+                        affine_cols<F8>(u[c & 1], F8 ? p.wscale + col : nullptr, p.bias ? p.bias + col : nullptr, v2);
+                        uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 128);
+                        if constexpr (EPI == WF_EPI_GELU_E4M3) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                w[i] = e4m3x2_of(gelu2_fast(v2[2 * i])) | (e4m3x2_of(gelu2_fast(v2[2 * i + 1])) << 16);
+                            srow[(2 * cb) ^ (lane & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
+                            srow[(2 * cb + 1) ^ (lane & 7)] = make_uint4(w[4], w[5], w[6], w[7]);
+                        } else {
+                            if constexpr (EPI == WF_EPI_GELU_BF16) {
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) v2[q] = gelu2(v2[q]);
+                            }
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    float a, b;
+                                    f2_unpack(v2[4 * q + i], a, b);
+                                    w[i] = pack_bf16(a, b);
+                                }
+                                srow[(4 * cb + q) ^ (lane & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    }
+                    if (cb == CPB - 1 || c == NPW - 1) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && col0 < p.N) {
+                            tma_store_2d(&tc, smem_u32(stg), col0, rel_row0);
+                            bulk_commit();
+                        }
+                    }
+                } else if constexpr (EPI == WF_EPI_GATED_RESIDUAL) {
                     // y = gate[group(row)] * (acc + b) staged as a 32 x 32
                     // block (row = lane, 16-byte units swizzled by row & 7, the
                     // TMA's 128-byte pattern), then x[block] += y by a TMA
@@ -619,9 +685,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 done:
-    if constexpr (EPI == WF_EPI_GATED_RESIDUAL) {
-        // the reduce-adds this warp issued have completed (shared memory is
-        // released when the CTA exits)
+    if constexpr (EPI == WF_EPI_GATED_RESIDUAL || EPI == WF_EPI_BF16 || EPI == WF_EPI_GELU_BF16 ||
+                  EPI == WF_EPI_GELU_E4M3 || EPI == WF_EPI_QKV_PUBLISH) {
+        // the reduce-adds / stores this warp issued have completed (shared
+        // memory is released when the CTA exits)
         if (warp >= 2 && lane == 0) bulk_wait_all();
     }
     if (*r.abort) {
@@ -709,7 +776,32 @@ cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, co
     CUtensorMap ta, tb, tc;
     if (!encode_2d(&ta, a, a_rows, p.K, lda, BM, f8)) return cudaErrorInvalidValue;
     if (!encode_2d(&tb, w, p.N, p.K, p.K, bn, f8)) return cudaErrorInvalidValue;
-    tc = ta;   // unused unless the epilogue reduces into x
+    tc = ta;   // unused unless the epilogue reduces into x or stores through TMA
+    p.staged = 0;
+    const bool qk_rows = epi == WF_EPI_QKV_PUBLISH && p.qk_raw && (p.g.H * p.g.D) % 64 == 0;
+    if (epi == WF_EPI_BF16 || epi == WF_EPI_GELU_BF16 || epi == WF_EPI_GELU_E4M3 || qk_rows) {
+        // row-major output rows [row_begin, row_end), boxes of 32 rows x 128
+        // bytes, 128-byte swizzle; outputs a map cannot describe keep the
+        // per-thread stores
+        const bool e8 = epi == WF_EPI_GELU_E4M3;
+        const long long ncols = qk_rows ? 2LL * p.g.H * p.g.D : p.N;
+        const long long pitch = qk_rows ? ncols : p.ldo;
+        const char *base = qk_rows ? reinterpret_cast<const char *>(p.qk_raw + (size_t)p.row_begin * pitch)
+                                   : static_cast<const char *>(p.out) + (size_t)p.row_begin * pitch * (e8 ? 1 : 2);
+        EncodeFn enc = encoder();
+        if (enc && (reinterpret_cast<uintptr_t>(base) & 15) == 0 && (pitch * (e8 ? 1 : 2)) % 16 == 0 &&
+            pitch >= ncols) {
+            const cuuint64_t dims[2] = {(cuuint64_t)ncols, (cuuint64_t)(p.row_end - p.row_begin)};
+            const cuuint64_t strides[1] = {(cuuint64_t)pitch * (e8 ? 1 : 2)};
+            const cuuint32_t box[2] = {e8 ? 128u : 64u, 32};
+            const cuuint32_t estr[2] = {1, 1};
+            if (enc(&tc, e8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<char *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+                p.staged = 1;
+        }
+    }
     if (epi == WF_EPI_GATED_RESIDUAL) {
         // fp32 x rows [row_begin, row_end), 32 x 32 boxes, 128-byte swizzle
         float *x0 = static_cast<float *>(p.out) + (size_t)p.row_begin * p.ldo;

@@ -134,6 +134,7 @@ struct GemmParams {
     const float *gate;           // gated residual: gate[group][col]
     int gate_ld, rows_per_group;
     uint32_t *status;            // plan scratch control words (timeouts), or null
+    int staged;                  // set by the launcher: row-major output through TMA stores
     // QKV publication
     WfGeom g;
     WfRoundDev rd;               // rows of slots without a task are skipped
