@@ -71,6 +71,40 @@ def test_bf16_and_gelu_epilogues(plan, M, N, K):
         assert err.max() <= 2 ** -8, (epi, err.max())
 
 
+@pytest.mark.parametrize("M,N,K,r0,r1", [(300, 544, 128, 37, 261), (517, 800, 320, 129, 390)])
+def test_staged_outputs_row_range(plan, M, N, K, r0, r1):
+    """Row-major outputs leave through shared memory and TMA stores in
+    32-row x 128-byte blocks: rows [r0, r1) that start and end inside a
+    tile, and a ragged last column block, are written; every other row keeps
+    its sentinel bit for bit (bf16, GELU bf16, and bf16 out of e4m3
+    operands)."""
+    a, w, b = operands(4, M, N, K)
+    ref = ref_linear(a, w, b, r0, r1)
+    sentinel = 7.0
+    for epi, fn in ((wf.WF_EPI_BF16, lambda x: x), (wf.WF_EPI_GELU_BF16, dit.gelu_tanh)):
+        out = torch.full((M, N), sentinel, dtype=torch.bfloat16, device="cuda")
+        plan.linear(a.cuda(), w.cuda(), b.cuda(), out, epi, row_begin=r0, row_end=r1)
+        torch.cuda.synchronize()
+        got = out.cpu().double().numpy()
+        assert np.all(got[:r0] == sentinel) and np.all(got[r1:] == sentinel), epi
+        want = fn(ref)
+        err = np.abs(got[r0:r1] - want) / np.maximum(np.abs(want), 1e-2)
+        assert err.max() <= 2 ** -8, (epi, err.max())
+    a8 = a.float().to(torch.float8_e4m3fn)
+    w8, sc = plan.quantize_weight_e4m3(w.cuda())
+    deq_w = w8.cpu().view(torch.float8_e4m3fn).double().numpy() * sc.cpu().double().numpy()[:, None]
+    ref8 = a8[r0:r1].double().numpy() @ deq_w.T + b.double().numpy()
+    out = torch.full((M, N), sentinel, dtype=torch.bfloat16, device="cuda")
+    plan.linear_e4m3(a8.view(torch.uint8).cuda(), w8, sc, b.cuda(), out, wf.WF_EPI_BF16,
+                     row_begin=r0, row_end=r1)
+    torch.cuda.synchronize()
+    got = out.cpu().double().numpy()
+    assert np.all(got[:r0] == sentinel) and np.all(got[r1:] == sentinel)
+    err = np.abs(got[r0:r1] - ref8) / np.maximum(np.abs(ref8), 1e-2)
+    assert err.max() <= 2 ** -8, err.max()
+    assert plan.sync_status() == wf.WF_OK
+
+
 def test_row_range_and_gated_residual(plan):
     """Rows outside [row_begin, row_end) are untouched; row r is gated by
     gate[r // rows_per_group]."""
