@@ -96,6 +96,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  "r"(c0), "r"(c1), "r"(src)
                  : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the bulk copies of this thread have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() {
@@ -443,7 +449,8 @@ struct QkvRowT<WF_EPI_QKV_PUBLISH> {
 template <int BN, int EPI, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                   const __grid_constant__ CUtensorMap tc, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tc, const __grid_constant__ CUtensorMap td,
+                   const GemmParams p) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -584,7 +591,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 bool staged = false;
                 if constexpr (STAGEABLE)
                     staged = p.staged && (EPI != WF_EPI_QKV_PUBLISH || col < 2 * p.g.H * p.g.D);
-                if (staged) {
+                // V of the QKV projection: a warp's 32 rows of one head's 32
+                // channels go to their page plane by one TMA store when the
+                // rows lie in one slot with a task (all but the block that
+                // straddles two chunks); otherwise per-thread stores below
+                bool vstaged = false;
+                int vslot = 0, vn0 = 0;
+                if constexpr (EPI == WF_EPI_QKV_PUBLISH) {
+                    if (p.staged_v && col >= 2 * p.g.H * p.g.D && col < p.N) {
+                        const int r0abs = p.row_begin + rel_row0;
+                        vslot = r0abs / p.g.NC;
+                        vn0 = r0abs - vslot * p.g.NC;
+                        vstaged = vn0 + 31 < p.g.NC && r0abs + 31 < p.row_end && p.rd.task_of_slot[vslot] >= 0;
+                    }
+                }
+                if (vstaged) {
+                    uint8_t *stg = smem + C::SM_STAGE + (warp - 2) * 4096;
+                    if (lane == 0) bulk_wait_read();          // the previous block has left stg
+                    __syncwarp();
+                    uint64_t v2[16];
+                    affine_cols<F8>(u[c & 1], F8 ? p.wscale + col : nullptr, p.bias ? p.bias + col : nullptr, v2);
+                    if (p.g.dtype == WF_FP8) {
+                        const float sc = p.g.v_scale;
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float a0, a1, a2, a3;
+                            f2_unpack(v2[2 * i], a0, a1);
+                            f2_unpack(v2[2 * i + 1], a2, a3);
+                            w[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a0 * sc, a1 * sc), __NV_SATFINITE, __NV_E4M3) |
+                                   ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a2 * sc, a3 * sc), __NV_SATFINITE,
+                                                                       __NV_E4M3) << 16);
+                        }
+                        uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 32);
+                        srow[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        srow[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+                        uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                float a, b;
+                                f2_unpack(v2[4 * q + i], a, b);
+                                w[i] = pack_bf16(a, b);
+                            }
+                            srow[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int ti = p.rd.task_of_slot[vslot];
+                        const int cc = col - 2 * p.g.H * p.g.D;
+                        const int h = cc / p.g.D;
+                        const int plane = ((p.rd.dest[ti] * p.g.L + p.layer) * 2 + 1) * p.g.H + h;
+                        tma_store_3d(&td, smem_u32(stg), cc - h * p.g.D, vn0, plane);
+                        bulk_commit();
+                    }
+                } else if (staged) {
                     const int cb = c % CPB;
                     const int col0 = col - cb * 32;           // first column of the block
                     uint8_t *stg = smem + C::SM_STAGE + (warp - 2) * 4096;
@@ -711,7 +777,7 @@ done:
 
 template <int BN, int EPI, bool F8>
 cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                   const GemmParams &p, int num_sms, cudaStream_t stream) {
+                   const CUtensorMap &td, const GemmParams &p, int num_sms, cudaStream_t stream) {
     using C = Cfg<BN>;
     static std::atomic<unsigned long long> attr_set{0};
     cudaError_t e = wf_once_per_device(attr_set, [] {
@@ -721,7 +787,7 @@ cudaError_t launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorM
     if (e != cudaSuccess) return e;
     const int n_tiles = p.tiles_m * p.tiles_n;
     const int grid = n_tiles < num_sms ? n_tiles : num_sms;
-    gemm_tc_kernel<BN, EPI, F8><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, tc, p);
+    gemm_tc_kernel<BN, EPI, F8><<<grid, NUM_THREADS, C::SM_ALLOC, stream>>>(ta, tb, tc, td, p);
     return cudaGetLastError();
 }
 
@@ -802,6 +868,27 @@ cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, co
                 p.staged = 1;
         }
     }
+    CUtensorMap td = ta;   // unused unless V is stored through TMA
+    p.staged_v = 0;
+    if (epi == WF_EPI_QKV_PUBLISH && p.pool && p.rd.n_tasks > 0 && p.g.D % 32 == 0) {
+        // the page pool as [plane][N_C][D] (plane = (page, layer, K/V, head)),
+        // over the pages this round writes; boxes of 32 tokens x 32 channels
+        int pages = 0;
+        for (int i = 0; i < p.rd.n_tasks; ++i) pages = p.rd.dest[i] + 1 > pages ? p.rd.dest[i] + 1 : pages;
+        const bool e8 = p.g.dtype == WF_FP8;
+        const int es = e8 ? 1 : 2;
+        EncodeFn enc = encoder();
+        const cuuint64_t dims[3] = {(cuuint64_t)p.g.D, (cuuint64_t)p.g.NC,
+                                    (cuuint64_t)pages * p.g.L * 2 * p.g.H};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.g.D * es, (cuuint64_t)p.g.NC * p.g.D * es};
+        const cuuint32_t box[3] = {32, 32, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (enc && (reinterpret_cast<uintptr_t>(p.pool) & 15) == 0 &&
+            enc(&td, e8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.pool, dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            p.staged_v = 1;
+    }
     if (epi == WF_EPI_GATED_RESIDUAL) {
         // fp32 x rows [row_begin, row_end), 32 x 32 boxes, 128-byte swizzle
         float *x0 = static_cast<float *>(p.out) + (size_t)p.row_begin * p.ldo;
@@ -821,23 +908,23 @@ cudaError_t wf_launch_gemm(int epi, const void *a, long long a_rows, int lda, co
     p.tiles_n = (p.N + bn - 1) / bn;
     if (f8) {
         switch (epi) {
-            case WF_EPI_BF16: return launch<256, WF_EPI_BF16, true>(ta, tb, tc, p, num_sms, stream);
-            case WF_EPI_F32: return launch<256, WF_EPI_F32, true>(ta, tb, tc, p, num_sms, stream);
-            case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, true>(ta, tb, tc, p, num_sms, stream);
-            case WF_EPI_GELU_E4M3: return launch<256, WF_EPI_GELU_E4M3, true>(ta, tb, tc, p, num_sms, stream);
+            case WF_EPI_BF16: return launch<256, WF_EPI_BF16, true>(ta, tb, tc, td, p, num_sms, stream);
+            case WF_EPI_F32: return launch<256, WF_EPI_F32, true>(ta, tb, tc, td, p, num_sms, stream);
+            case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, true>(ta, tb, tc, td, p, num_sms, stream);
+            case WF_EPI_GELU_E4M3: return launch<256, WF_EPI_GELU_E4M3, true>(ta, tb, tc, td, p, num_sms, stream);
             case WF_EPI_GATED_RESIDUAL:
-                return launch<256, WF_EPI_GATED_RESIDUAL, true>(ta, tb, tc, p, num_sms, stream);
-            case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, true>(ta, tb, tc, p, num_sms, stream);
+                return launch<256, WF_EPI_GATED_RESIDUAL, true>(ta, tb, tc, td, p, num_sms, stream);
+            case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, true>(ta, tb, tc, td, p, num_sms, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (epi) {
-        case WF_EPI_BF16: return launch<256, WF_EPI_BF16, false>(ta, tb, tc, p, num_sms, stream);
-        case WF_EPI_F32: return launch<256, WF_EPI_F32, false>(ta, tb, tc, p, num_sms, stream);
-        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, false>(ta, tb, tc, p, num_sms, stream);
-        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL, false>(ta, tb, tc, p, num_sms, stream);
-        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, false>(ta, tb, tc, p, num_sms, stream);
-        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD, false>(ta, tb, tc, p, num_sms, stream);
+        case WF_EPI_BF16: return launch<256, WF_EPI_BF16, false>(ta, tb, tc, td, p, num_sms, stream);
+        case WF_EPI_F32: return launch<256, WF_EPI_F32, false>(ta, tb, tc, td, p, num_sms, stream);
+        case WF_EPI_GELU_BF16: return launch<256, WF_EPI_GELU_BF16, false>(ta, tb, tc, td, p, num_sms, stream);
+        case WF_EPI_GATED_RESIDUAL: return launch<256, WF_EPI_GATED_RESIDUAL, false>(ta, tb, tc, td, p, num_sms, stream);
+        case WF_EPI_QKV_PUBLISH: return launch<256, WF_EPI_QKV_PUBLISH, false>(ta, tb, tc, td, p, num_sms, stream);
+        case WF_EPI_HEAD: return launch<64, WF_EPI_HEAD, false>(ta, tb, tc, td, p, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -135,6 +135,7 @@ struct GemmParams {
     int gate_ld, rows_per_group;
     uint32_t *status;            // plan scratch control words (timeouts), or null
     int staged;                  // set by the launcher: row-major output through TMA stores
+    int staged_v;                // set by the launcher: V pages through TMA stores
     // QKV publication
     WfGeom g;
     WfRoundDev rd;               // rows of slots without a task are skipped
