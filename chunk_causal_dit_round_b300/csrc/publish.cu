@@ -12,6 +12,7 @@
 // the token-major input and stores into the head-major pages are both
 // contiguous 16-byte vectors.
 
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -376,7 +377,25 @@ cudaError_t wf_launch_publish(const WfGeom &g, const WfRoundDev &rd, int layer, 
     long long items = (long long)g.NC * g.H * (g.D / nvec) * (rd.n_tasks + rd.n_rerot);
     if (items >= (1ll << 31)) return cudaErrorInvalidValue;
     long long want = (items + threads - 1) / threads;
-    int blocks = (int)(want < (long long)sms * 8 ? want : (long long)sms * 8);
+    // one wave of the grid-stride loop: as many blocks as fit on the SMs at
+    // once (a second, partial wave of late-starting blocks would finish
+    // after the first one)
+    static std::atomic<int> resident[3];
+    const int kind = dtype == WF_FP8 ? 0 : (dtype == WF_FP32 ? 1 : 2);
+    int per_sm = resident[kind].load(std::memory_order_relaxed);
+    if (per_sm < 1) {
+        cudaError_t e;
+        if (kind == 0)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, publish_fp8_kernel, threads, 0);
+        else if (kind == 1)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, publish_kernel<float>, threads, 0);
+        else
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, publish_kernel<__nv_bfloat16>, threads, 0);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+        resident[kind].store(per_sm, std::memory_order_relaxed);
+    }
+    int blocks = (int)(want < (long long)sms * per_sm ? want : (long long)sms * per_sm);
     if (blocks < 1) blocks = 1;
     const float2 *tab =
         reinterpret_cast<const float2 *>(static_cast<const char *>(scratch) + WF_SCRATCH_TABLES);
