@@ -52,6 +52,26 @@ ATTN_TC_SOURCES = ("chunk_causal_dit_round_b300/csrc/attn_tc.cu",
 ATTN_TC_TRAFFIC = {"bf16": (5.2925e8, "d47bd0f5fe615e78"), "e4m3": (2.1823e8, "d47bd0f5fe615e78")}
 
 
+# Video frames of a request: "Wave Forcing", App. C (VBench-Long protocol),
+# saves 1593 video frames for 399 latent frames -- the first latent frame
+# decodes to one video frame and every later one to four -- so a chunk of
+# grid_t latent frames adds 4 grid_t video frames in steady state.
+def video_frames(n_chunks, latent_frames_per_chunk=3):
+    return 1 + (n_chunks * latent_frames_per_chunk - 1) * 4
+
+
+def frames_per_s(chunks_per_s, latent_frames_per_chunk=3):
+    return 4 * latent_frames_per_chunk * chunks_per_s
+
+
+def eta_slot(n_chunks, S, sequential=False):
+    """Useful fraction of a request's stage slots ("Wave Forcing", App. B.4
+    Eq. 16): a wavefront request of N chunks takes N + S rounds of S + 1
+    slots for N (S + 1) tasks; the sequential schedule keeps one of S + 1
+    stage replicas busy."""
+    return 1 / (S + 1) if sequential else n_chunks / (n_chunks + S)
+
+
 def _sources_sha16(paths):
     import hashlib
     h = hashlib.sha256()
@@ -596,10 +616,10 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
                    "h2d_bytes_per_step": per_step * (h_z.numel() + h_eps.numel()) * 4,
                    "d2h_bytes_per_step": h_out.numel() * 4, "steps": e2e_steps,
                    "clocks": clk_e2e.summary()},
-           "frames_per_s": round(12 * chunks_s, 2),
+           "frames_per_s": round(frames_per_s(chunks_s, cfg["grid"][0]), 2),
            "ms_per_chunk_p50": round(statistics.median(per), 3),
            "chunks_timed": steps,
-           "eta_slot": round(1 / (S + 1) if seq else cfg["n_chunks"] / (cfg["n_chunks"] + S), 4),
+           "eta_slot": round(eta_slot(cfg["n_chunks"], S, seq), 4),
            "flops_per_round": flops / steps,
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak, 1),
                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
