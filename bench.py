@@ -16,9 +16,12 @@ Prints one JSON line (rank 0): the attention TFLOP/s with the attention
 kernel's roofline (CUDA-event time per launch against the measured peak),
 the publish kernel's GB/s against the measured HBM bandwidth, the same
 metric end to end with host buffers (``e2e``), the clocks seen during the
-timed region, the oracle timed on the host cores (``cpu_baseline``), and the
-whole DiT round (chunks/s, frames/s) for the bf16 model (``dit``) and the
-8-bit one (``dit_w8a8``).  ``--config`` selects the other workloads;
+timed region, the oracle timed on the host cores (``cpu_baseline``),
+batched requests (``streams``: the attention layer; ``dit_streams``: whole
+DiT rounds), and the whole DiT round (chunks/s, frames/s) for the bf16 model
+(``dit``), the 8-bit one (``dit_w8a8``), the 5-step long rollout
+(``dit_s5``) and the 14B-scale QKV + attention stack (``qkv_attn14b``).
+``--config`` selects single workloads;
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 round instead.
 """
@@ -1186,9 +1189,11 @@ def main():
     res = run_ours(args, rank, world)
     if not args.no_dit:
         # the other workloads of the measurement plan, each with its clocks and
-        # roofline: the 1.3B DiT (bf16 and 8-bit), the 5-step long rollout and
-        # the 14B-scale QKV + attention stack
+        # roofline: batched requests (attention layer, then whole DiT rounds),
+        # the 1.3B DiT (bf16 and 8-bit), the 5-step long rollout and the
+        # 14B-scale QKV + attention stack
         res["streams"] = run_streams(args, rank, world)
+        res["dit_streams"] = run_dit_streams(args, rank, world)
         res["dit"] = run_dit(args, "dit13", rank, world, steps=args.dit_steps, warmup=3)
         res["dit_w8a8"] = run_dit(args, "dit13_w8a8", rank, world, steps=args.dit_steps, warmup=3)
         res["dit_s5"] = run_dit(args, "dit13_s5", rank, world, steps=args.dit_steps, warmup=3)
