@@ -356,6 +356,9 @@ def measure_peaks(n=8192, seconds=4.0):
             e1.record()
             torch.cuda.synchronize()
             best = min(best, e0.elapsed_time(e1))
+        res[name] = {"burst_tflops": round(2 * n ** 3 / (best * 1e-3) / 1e12, 1)}
+        if seconds <= 0:          # burst launches only (e.g. for a short profiler capture)
+            continue
         with ClockSampler(dev.index) as clk:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             t0, count = time.time(), 0
@@ -367,9 +370,8 @@ def measure_peaks(n=8192, seconds=4.0):
                 torch.cuda.synchronize()
             e1.record()
             torch.cuda.synchronize()
-        res[name] = {"burst_tflops": round(2 * n ** 3 / (best * 1e-3) / 1e12, 1),
-                     "sustained_tflops": round(2 * n ** 3 * count / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
-                     "clocks_sustained": clk.summary()}
+        res[name].update({"sustained_tflops": round(2 * n ** 3 * count / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
+                          "clocks_sustained": clk.summary()})
     return {"workload": f"library dense GEMM {n}^3 (cuBLASLt through torch)", "peaks": res}
 
 
@@ -1153,6 +1155,8 @@ def main():
     ap.add_argument("--dit-steps", type=int, default=20,
                     help="steady chunks timed per DiT leg of the default line (14B leg: half)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--peak-seconds", type=float, default=4.0,
+                    help="--config peaks: seconds of back-to-back launches for the sustained peak (0: burst only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1168,7 +1172,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     if args.config == "peaks":
         if rank == 0:
-            print(json.dumps(measure_peaks()), flush=True)
+            print(json.dumps(measure_peaks(seconds=args.peak_seconds)), flush=True)
         return
     if args.config in ("streams", "dit_streams"):
         fn = run_streams if args.config == "streams" else run_dit_streams
