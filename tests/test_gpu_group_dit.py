@@ -109,7 +109,8 @@ def run_single(cfg, r_id, params, steps, seed, fp8=None, linear_fp8=False):
     return res
 
 
-@pytest.mark.parametrize("fp8,linear_fp8", [(None, False), ((4.0, 2.0), True)], ids=["bf16", "w8a8"])
+@pytest.mark.parametrize("fp8,linear_fp8", [(None, False), ((4.0, 2.0), False), ((4.0, 2.0), True)],
+                         ids=["bf16", "e4m3-attention", "w8a8"])
 def test_group_dit_bit_identical_to_single_plans(fp8, linear_fp8):
     cfg = sch.Cfg(3, 5, 1)
     steps = [1000.0, 700.0, 400.0]
