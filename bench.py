@@ -75,6 +75,12 @@ def eta_slot(n_chunks, S, sequential=False):
     return 1 / (S + 1) if sequential else n_chunks / (n_chunks + S)
 
 
+def _p90(xs):
+    """90th percentile (nearest rank) of a list of times."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, math.ceil(0.9 * len(ys)) - 1))]
+
+
 def _sources_sha16(paths):
     import hashlib
     h = hashlib.sha256()
@@ -221,7 +227,8 @@ def run_qkv_attn(args, name, rank, world, steps=None, warmup=None):
     res = {"workload": name, "desc": cfg["desc"], "layers": L,
            "value": round(world * steps / (ms * 1e-3), 3), "unit": "chunks/s",
            "value_p50": round(world * 1e3 / statistics.median(per), 3),
-           "round_ms_p50": round(statistics.median(per), 3), "rounds": steps,
+           "round_ms_p50": round(statistics.median(per), 3), "round_ms_p90": round(_p90(per), 3),
+           "rounds": steps,
            "flops_per_round": flops / steps,
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                         "unit": "TFLOP/s", "frac": round(tf / peak, 4),
@@ -623,6 +630,7 @@ def run_dit(args, name, rank, world, steps=None, warmup=None):
                    "clocks": clk_e2e.summary()},
            "frames_per_s": round(frames_per_s(chunks_s, cfg["grid"][0]), 2),
            "ms_per_chunk_p50": round(statistics.median(per), 3),
+           "ms_per_chunk_p90": round(_p90(per), 3),
            "chunks_timed": steps,
            "eta_slot": round(eta_slot(cfg["n_chunks"], S, seq), 4),
            "flops_per_round": flops / steps,
